@@ -1,0 +1,233 @@
+/*
+ * dsv4kv -- DeepSeek-V4.1 compressed-KV write and read on one GB300 (sm_103a).
+ *
+ * Plain C ABI.  Every pointer argument is a DEVICE pointer owned by the caller
+ * unless marked "host"; the library keeps no reference to any of them after a
+ * call returns (the reuse buffer only remembers the caller's storage pointer
+ * and the identity of the last source it filled).  Every call that touches the
+ * GPU is asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the
+ * legacy default stream), never synchronises the host, allocates no memory,
+ * and reads its metadata (offsets, page tables, out_loc, ids) on the device,
+ * so a sequence of calls can be captured into a CUDA graph and replayed with
+ * the metadata refreshed in place.
+ *
+ * Return value: DSV4KV_OK (0) or a negative status; see the enum below.
+ * Host-checkable argument errors return before anything is launched.  Faults
+ * that only the device can see (an id or slot outside the pool, a request
+ * whose rows run past the input, a position past the RoPE table) never trap:
+ * the affected row is written as zeros or skipped, as each call documents,
+ * and one is added to *err_word (a caller-zeroed device int32; may be NULL).
+ *
+ * Sources, cited by page title and section:
+ *   [KVL]  sglang PR #39652 "dsv4.1: compression, KV I/O, and metadata
+ *          kernels" -- Summary: KVLayout, PagedKV<layout, page_bits>::row,
+ *          v41::store_row; the c1/c2 compressors; the V4.1 dequantizers;
+ *          review: store_row_fp8's ue8m0 formula, clear_negative_zero.
+ *   [EXT]  sglang PR #46230 (ratio-2 fused compressor in the prefill CUDA
+ *          graph) -- low_ratio_extend_offsets; the | kv | score | projection.
+ *   [BUF]  sglang PR #45909 (sparse-prefill KV dequant reuse) --
+ *          SparsePrefillKVBuffer and get_with_head.
+ *   [TOPK] flashinfer_sparse.py -- _compressed_topk_to_slots and
+ *          compressed_block_size = block_size // compress_ratio.
+ */
+#ifndef DSV4KV_H
+#define DSV4KV_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Paged main-KV row formats [KVL, KVLayout bullet].  One row = one 512-dim
+ * compressed latent (dims 0..447 "nope", 448..511 "rope").
+ *   DSV4KV_V4      584 B: 448 fp8 nope + 64 bf16 rope + 8 ue8m0 bytes.
+ *                  Row size only; store and dequant return DSV4KV_ENOTSUP.
+ *   DSV4KV_V41     528 B: 512 e4m3 codes (byte d = dim d), then 16 ue8m0
+ *                  scale bytes (byte 512+g scales dims 32g..32g+31).
+ *   DSV4KV_V41_FP4 288 B: 256 bytes of e2m1 codes (byte i holds dim 2i in
+ *                  its low nibble, dim 2i+1 in its high nibble), then 32 e4m3
+ *                  scale bytes (byte 256+g scales dims 16g..16g+15). */
+typedef enum {
+    DSV4KV_V4 = 0,
+    DSV4KV_V41 = 1,
+    DSV4KV_V41_FP4 = 2
+} dsv4kv_layout;
+
+enum {
+    DSV4KV_OK = 0,
+    DSV4KV_EINVAL = -1,  /* NULL / misaligned pointer, bad enum, negative size */
+    DSV4KV_ENOTSUP = -2, /* a layout or mode that is not built (V4 rows) */
+    DSV4KV_ERANGE = -3,  /* a size past a documented limit */
+    DSV4KV_ECUDA = -4    /* a CUDA launch failed; see dsv4kv_last_cuda_error */
+};
+
+/* Limits of this build. */
+#define DSV4KV_DIM 512
+#define DSV4KV_MAX_SLOTS 4096          /* request slots per compress_store call */
+#define DSV4KV_MAX_POOL_ROWS 2147483647LL /* slots and ids are int32 */
+
+/* Bytes per row of `layout` (584 / 528 / 288), or DSV4KV_EINVAL.  Host only. */
+int dsv4kv_row_bytes(int layout);
+
+/* The cudaError_t of the last DSV4KV_ECUDA on this host thread (0 if none). */
+int dsv4kv_last_cuda_error(void);
+
+/* Static description of a status code.  Host only. */
+const char *dsv4kv_status_string(int status);
+
+/*
+ * Fused compressor: pool -> RMSNorm -> RoPE -> quantize -> paged store.
+ * [KVL, c1/c2 bullet: "pair-pooling (ratio 2), RMSNorm, RoPE and the main-KV
+ * write in one launch, returning the pre-RoPE latent; out_loc == 0 marks a
+ * padded graph row"; EXT for the offsets and the fused projection.]
+ *
+ * Plan.  extend_offsets is int32 [2, n_slots]: row 0 = first source row of
+ * each request slot, row 1 = its source row count (<= 0: no rows).  Output
+ * rows are numbered request by request: request r contributes
+ * count_r / ratio rows (an odd trailing token of a ratio-2 request yields no
+ * row), row j of request r pools source rows first_r + ratio*j + t, t < ratio,
+ * and sits at position ratio*j.  Output rows k >= the plan's total are
+ * padding: nothing is stored and latent_out / prequant_out rows are zeroed.
+ *
+ * Per row (fp32 on the device):
+ *   ratio 1: x = kv[first_r + j]
+ *   ratio 2: x[d] = sum_t softmax_t(score[src+t][d]) * kv[src+t][d]
+ *   RMSNorm (if rmsnorm_w): x = x / sqrt(mean(x^2) + eps) * w
+ *   latent_out (if given) = bf16(x)                    (post-norm, pre-RoPE)
+ *   RoPE (if freqs_cis): pairs (448+2i, 449+2i), i < 32, rotated by
+ *        (c, s) = freqs_cis[pos][2i], freqs_cis[pos][2i+1]
+ *   prequant_out (if given) = x                        (what is quantized)
+ *   store_row:  V41: per 32 dims e = max((bits(amax)>>23) - 8 +
+ *        ((bits(amax) & 0x7FFFFF) > 0x600000), 114), the ue8m0 byte equal to
+ *        127 + ceil(log2(max(amax/448, 1e-4))); codes e4m3_rn_satfinite(
+ *        x * 2^(127-e)).  V41_FP4: per 16 dims s = e4m3_rn_satfinite(amax/6),
+ *        codes e2m1_rn_satfinite(x / s) (IEEE fp32 divisions), 0 if s == 0.
+ *        A code that rounds to -0 is stored as +0.
+ *   slot = out_loc[k] if out_loc, else
+ *        page_table[r][j >> page_bits] << page_bits | (j & (2^page_bits - 1))
+ *        (compressed pages hold 2^page_bits rows [TOPK]); slot 0 = do not
+ *        store (page 0 is reserved); the row lands at
+ *        pool + (slot >> page_bits) * (row_bytes << page_bits)
+ *             + (slot & (2^page_bits - 1)) * row_bytes      [KVL, PagedKV].
+ *
+ * Arguments:
+ *   layout        DSV4KV_V41 or DSV4KV_V41_FP4.
+ *   ratio         1 or 2.
+ *   rows          bf16 [n_rows, row_stride], 16-B aligned; kv in columns
+ *                 0..511.  For ratio 2 with score == NULL the score sits in
+ *                 columns 512..1023 (the fused | kv | score | projection).
+ *   row_stride    elements, multiple of 8, >= 512 (>= 1024 fused ratio 2).
+ *   score         NULL or bf16 [n_rows, score_stride] (ratio 2 only).
+ *   extend_offsets, n_slots   see Plan; 0 <= n_slots <= DSV4KV_MAX_SLOTS.
+ *   page_table    int32 [n_slots, max_pages]; required when out_loc == NULL.
+ *   page_bits     log2 rows per page, 0..16.
+ *   rmsnorm_w     NULL (no norm) or bf16 [512], 16-B aligned; eps >= 0.
+ *   freqs_cis     NULL (no RoPE) or fp32 [max_pos, 64], 16-B aligned.
+ *   out_loc       NULL or int32 [n_out].
+ *   n_out         output rows (>= the plan's total to store every row);
+ *                 0 is a no-op.
+ *   pool          [pool_rows * row_bytes] bytes, 16-B aligned;
+ *                 1 <= pool_rows <= DSV4KV_MAX_POOL_ROWS.
+ *   latent_out    NULL or bf16 [n_out, 512], 16-B aligned.
+ *   prequant_out  NULL or fp32 [n_out, 512], 16-B aligned.
+ * Device faults (+1 on err_word each): source rows outside [0, n_rows) or a
+ * position >= max_pos (row not computed: zero latent/prequant, not stored);
+ * a slot < 0 or >= pool_rows, or a page index >= max_pages (row computed,
+ * not stored).
+ */
+int dsv4kv_compress_store(int layout, int ratio,
+                          const void *rows, long long n_rows, long long row_stride,
+                          const void *score, long long score_stride,
+                          const int *extend_offsets, int n_slots,
+                          const int *page_table, int max_pages, int page_bits,
+                          const void *rmsnorm_w, float eps,
+                          const float *freqs_cis, int max_pos,
+                          const int *out_loc, int n_out,
+                          void *pool, long long pool_rows,
+                          void *latent_out, float *prequant_out,
+                          int *err_word, void *stream);
+
+/*
+ * Paged gather-dequant [KVL, dequantize_k_cache_paged for the V4.1 layouts]:
+ *   out_bf16[i][d] = bf16(code(ids[i], d) * scale(ids[i], d)), i < n.
+ * V41: scale = 2^(e - 127) of the group's ue8m0 byte; V41_FP4: the group's
+ * e4m3 scale.  Products are exact in bf16 for every row store_row writes.
+ * ids[i] < 0 gives a zero row; ids[i] >= pool_rows gives a zero row and one
+ * fault.  The pool is addressed as rows of row_bytes (pages are unpadded, so
+ * a slot's byte offset is slot * row_bytes whatever the page size).
+ *   pool      [pool_rows * row_bytes] bytes, 16-B aligned.
+ *   ids       int32 [n].
+ *   out_bf16  bf16 [n, 512], 16-B aligned.
+ *   n         0 <= n < 2^31; 0 is a no-op.
+ */
+int dsv4kv_dequant_gather(int layout, const void *pool, long long pool_rows,
+                          const int *ids, long long n, void *out_bf16,
+                          int *err_word, void *stream);
+
+/*
+ * Request-local top-k compressed ids -> physical pool slots [TOPK,
+ * _compressed_topk_to_slots, single-rank branch]:
+ *   slots[t][c] = page_table[req][id >> page_bits] << page_bits
+ *                 | (id & (2^page_bits - 1)),  id = topk[t][c], req = token_to_req[t]
+ * or -1 when id < 0, when is_valid (nullable uint8 [n_tok]) is 0 for t, or on a
+ * fault (req outside [0, n_req), page index >= max_pages).  lens (nullable
+ * int32 [n_tok]) = number of slots >= 0 in the row.
+ *   topk int32 [n_tok, k]; token_to_req int32 [n_tok];
+ *   page_table int32 [n_req, max_pages]; slots int32 [n_tok, k];
+ *   0 <= k <= 65536, page_bits 0..16.
+ */
+int dsv4kv_topk_to_slots(const int *topk, int n_tok, int k,
+                         const int *token_to_req, const unsigned char *is_valid,
+                         const int *page_table, int n_req, int max_pages, int page_bits,
+                         int *slots, int *lens, int *err_word, void *stream);
+
+/*
+ * Source-reuse buffer [BUF]: the shared bf16 buffer the sparse-prefill layers
+ * read.  It remembers the source it last dequantized -- (layout, pool,
+ * pool_rows, ids pointer, n) -- and a get_with_head for that same source is a
+ * hit: the rows are already there and nothing is launched.  A plain get, a
+ * re-init (reallocation) or begin_forward forgets the head.  Reuse is sound
+ * while no call between the fill and the hit writes the pool rows or the ids
+ * (within one forward no later layer writes the source cache, and graph
+ * replay keeps layer order).
+ *
+ * The struct is host memory owned by the caller; `storage` is the caller's
+ * device buffer of capacity_rows x 512 bf16, 16-B aligned.
+ */
+typedef struct dsv4kv_kvbuf {
+    void *storage;
+    long long capacity_rows;
+    int head_valid;
+    int head_layout;
+    const void *head_pool;
+    long long head_pool_rows;
+    const int *head_ids;
+    long long head_n;
+} dsv4kv_kvbuf;
+
+/* (Re)initialise: set storage and capacity, forget the head.  Host only. */
+int dsv4kv_kvbuf_init(dsv4kv_kvbuf *buf, void *storage_bf16, long long capacity_rows);
+
+/* Start of a new forward: forget the head.  Host only. */
+void dsv4kv_kvbuf_begin_forward(dsv4kv_kvbuf *buf);
+
+/* Plain get of the first n rows (host pointer *rows = storage): forgets the
+ * head.  DSV4KV_ERANGE if n > capacity.  Host only. */
+int dsv4kv_kvbuf_get(dsv4kv_kvbuf *buf, long long n, void **rows);
+
+/* The head decision alone: *hit = 1 if (layout, pool, pool_rows, ids, n) is
+ * the head, else 0 and the head becomes that source.  Launches nothing; for
+ * callers that run their own dequant on a miss.  Host only. */
+int dsv4kv_kvbuf_lookup(dsv4kv_kvbuf *buf, int layout, const void *pool,
+                        long long pool_rows, const int *ids, long long n, int *hit);
+
+/* get_with_head: *rows = storage; on a miss runs dsv4kv_dequant_gather into
+ * the storage and sets the head (cleared again if the launch fails); on a hit
+ * launches nothing.  Same argument rules as dsv4kv_dequant_gather. */
+int dsv4kv_kvbuf_get_with_head(dsv4kv_kvbuf *buf, int layout, const void *pool,
+                               long long pool_rows, const int *ids, long long n,
+                               void **rows, int *hit, int *err_word, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSV4KV_H */
