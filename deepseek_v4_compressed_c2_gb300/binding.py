@@ -1,0 +1,270 @@
+"""Thin Python binding of the dsv4kv C ABI (include/dsv4kv.h).
+
+Argument marshalling only: every step of the compressed-KV write and read
+runs in the CUDA library ``_build/libdsv4kv.so``.  PyTorch provides device
+memory and the current stream.  The library must have been built
+(``__graft_entry__.build()`` or ``python -m deepseek_v4_compressed_c2_gb300.build``);
+there is no fallback -- if it is missing, every call raises.
+
+Function names are the C names.  Shapes, dtypes and the error convention are
+documented in the header; a negative status raises ``DSV4KVError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+V4, V41, V41_FP4 = 0, 1, 2
+DIM = 512
+_ROW_BYTES = {V4: 584, V41: 528, V41_FP4: 288}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DSV4KVError(RuntimeError):
+    def __init__(self, fn, status, lib):
+        msg = lib.dsv4kv_status_string(status).decode()
+        if status == -4:
+            msg += f" (cudaError {lib.dsv4kv_last_cuda_error()})"
+        super().__init__(f"{fn}: status {status}: {msg}")
+        self.status = status
+
+
+class dsv4kv_kvbuf(ctypes.Structure):
+    _fields_ = [("storage", ctypes.c_void_p), ("capacity_rows", ctypes.c_longlong),
+                ("head_valid", ctypes.c_int), ("head_layout", ctypes.c_int),
+                ("head_pool", ctypes.c_void_p), ("head_pool_rows", ctypes.c_longlong),
+                ("head_ids", ctypes.c_void_p), ("head_n", ctypes.c_longlong)]
+
+
+def lib():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"dsv4kv CUDA library not built ({_LIB_PATH} missing); "
+                               "run __graft_entry__.build() first")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I, LL, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
+        KB = ctypes.POINTER(dsv4kv_kvbuf)
+        sig = {
+            "dsv4kv_row_bytes": (I, [I]),
+            "dsv4kv_last_cuda_error": (I, []),
+            "dsv4kv_status_string": (ctypes.c_char_p, [I]),
+            "dsv4kv_compress_store": (I, [I, I, P, LL, LL, P, LL, P, I, P, I, I, P, F, P, I,
+                                          P, I, P, LL, P, P, P, P]),
+            "dsv4kv_dequant_gather": (I, [I, P, LL, P, LL, P, P, P]),
+            "dsv4kv_topk_to_slots": (I, [P, I, I, P, P, P, I, I, I, P, P, P, P]),
+            "dsv4kv_kvbuf_init": (I, [KB, P, LL]),
+            "dsv4kv_kvbuf_begin_forward": (None, [KB]),
+            "dsv4kv_kvbuf_get": (I, [KB, LL, ctypes.POINTER(ctypes.c_void_p)]),
+            "dsv4kv_kvbuf_lookup": (I, [KB, I, P, LL, P, LL, ctypes.POINTER(ctypes.c_int)]),
+            "dsv4kv_kvbuf_get_with_head": (I, [KB, I, P, LL, P, LL, ctypes.POINTER(ctypes.c_void_p),
+                                               ctypes.POINTER(ctypes.c_int), P, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+        return L
+
+
+def _check(fn, status):
+    if status != 0:
+        raise DSV4KVError(fn, status, lib())
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _need(t, dtype, name):
+    if t is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def dsv4kv_row_bytes(layout: int) -> int:
+    rb = lib().dsv4kv_row_bytes(layout)
+    _check("dsv4kv_row_bytes", rb if rb < 0 else 0)
+    return rb
+
+
+def dsv4kv_compress_store(layout, ratio, rows, extend_offsets, pool, *, score=None,
+                          page_table=None, page_bits=0, rmsnorm_w=None, eps=1e-6,
+                          freqs_cis=None, out_loc=None, n_out=None, pool_rows=None,
+                          latent_out=None, prequant_out=None, err_word=None, stream=None):
+    """Fused compress -> RMSNorm -> RoPE -> quantize -> paged store.
+    rows: bf16 [n_rows, row_stride] (unit column stride); extend_offsets: int32
+    [2, n_slots]; pool: uint8 tensor of pool_rows * row_bytes bytes."""
+    _need(rows, torch.bfloat16, "rows")
+    _need(score, torch.bfloat16, "score")
+    _need(extend_offsets, torch.int32, "extend_offsets")
+    _need(page_table, torch.int32, "page_table")
+    _need(rmsnorm_w, torch.bfloat16, "rmsnorm_w")
+    _need(freqs_cis, torch.float32, "freqs_cis")
+    _need(out_loc, torch.int32, "out_loc")
+    _need(latent_out, torch.bfloat16, "latent_out")
+    _need(prequant_out, torch.float32, "prequant_out")
+    _need(err_word, torch.int32, "err_word")
+    if rows.dim() != 2 or rows.stride(1) != 1:
+        raise ValueError("rows must be 2-D with unit column stride")
+    if extend_offsets.dim() != 2 or extend_offsets.shape[0] != 2 or not extend_offsets.is_contiguous():
+        raise ValueError("extend_offsets must be a contiguous [2, n_slots] tensor")
+    if n_out is None:
+        if out_loc is None:
+            raise ValueError("n_out is required when out_loc is None")
+        n_out = out_loc.numel()
+    pool_bytes = pool.numel() * pool.element_size()
+    if pool_rows is None:
+        pool_rows = pool_bytes // _ROW_BYTES.get(layout, 1)
+    elif pool_rows * _ROW_BYTES.get(layout, 0) > pool_bytes:
+        raise ValueError("pool_rows exceeds the pool tensor")
+    if out_loc is not None and out_loc.numel() < n_out:
+        raise ValueError("out_loc has fewer than n_out entries")
+    for name, t in (("latent_out", latent_out), ("prequant_out", prequant_out)):
+        if t is not None and (t.numel() < n_out * DIM or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous tensor of >= n_out x 512")
+    if score is not None and (score.dim() != 2 or score.stride(1) != 1
+                              or score.shape[0] < rows.shape[0]):
+        raise ValueError("score must be 2-D, unit column stride, with >= n_rows rows")
+    if rows.shape[1] < (2 * DIM if ratio == 2 and score is None else DIM):
+        raise ValueError("rows are narrower than the layout needs")
+    if rmsnorm_w is not None and rmsnorm_w.numel() < DIM:
+        raise ValueError("rmsnorm_w must hold 512 weights")
+    if freqs_cis is not None and (freqs_cis.dim() != 2 or freqs_cis.shape[1] != 64
+                                  or not freqs_cis.is_contiguous()):
+        raise ValueError("freqs_cis must be a contiguous [max_pos, 64] tensor")
+    if page_table is not None and (page_table.dim() != 2 or not page_table.is_contiguous()
+                                   or page_table.shape[0] < extend_offsets.shape[1]):
+        raise ValueError("page_table must be a contiguous [>= n_slots, max_pages] tensor")
+    s_stride = 0 if score is None else score.stride(0)
+    st = lib().dsv4kv_compress_store(
+        layout, ratio, _ptr(rows), rows.shape[0], rows.stride(0), _ptr(score), s_stride,
+        _ptr(extend_offsets), extend_offsets.shape[1], _ptr(page_table),
+        0 if page_table is None else page_table.shape[1], page_bits, _ptr(rmsnorm_w), eps,
+        _ptr(freqs_cis), 0 if freqs_cis is None else freqs_cis.shape[0], _ptr(out_loc), n_out,
+        _ptr(pool), pool_rows, _ptr(latent_out), _ptr(prequant_out), _ptr(err_word),
+        _stream(stream))
+    _check("dsv4kv_compress_store", st)
+
+
+def dsv4kv_dequant_gather(layout, pool, ids, out=None, *, pool_rows=None, err_word=None,
+                          stream=None):
+    """bf16 [n, 512] rows of the pool at `ids` (int32); returns `out`."""
+    _need(ids, torch.int32, "ids")
+    _need(out, torch.bfloat16, "out")
+    _need(err_word, torch.int32, "err_word")
+    n = ids.numel()
+    if not ids.is_contiguous():
+        raise ValueError("ids must be contiguous")
+    if out is None:
+        out = torch.empty((n, DIM), dtype=torch.bfloat16, device=ids.device)
+    elif out.numel() < n * DIM or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of >= n x 512")
+    pool_bytes = pool.numel() * pool.element_size()
+    if pool_rows is None:
+        pool_rows = pool_bytes // _ROW_BYTES.get(layout, 1)
+    elif pool_rows * _ROW_BYTES.get(layout, 0) > pool_bytes:
+        raise ValueError("pool_rows exceeds the pool tensor")
+    st = lib().dsv4kv_dequant_gather(layout, _ptr(pool), pool_rows, _ptr(ids), n, _ptr(out),
+                                     _ptr(err_word), _stream(stream))
+    _check("dsv4kv_dequant_gather", st)
+    return out
+
+
+def dsv4kv_topk_to_slots(topk, token_to_req, page_table, page_bits, *, is_valid=None,
+                         slots=None, lens=None, err_word=None, stream=None):
+    """Request-local top-k ids -> pool slots (int32 [n_tok, k]) and lens."""
+    _need(topk, torch.int32, "topk")
+    _need(token_to_req, torch.int32, "token_to_req")
+    _need(page_table, torch.int32, "page_table")
+    _need(is_valid, torch.uint8, "is_valid")
+    n_tok, k = topk.shape
+    if not (topk.is_contiguous() and page_table.is_contiguous()) or token_to_req.numel() < n_tok \
+            or (is_valid is not None and is_valid.numel() < n_tok):
+        raise ValueError("topk / page_table must be contiguous; token_to_req, is_valid >= n_tok")
+    if slots is None:
+        slots = torch.empty((n_tok, k), dtype=torch.int32, device=topk.device)
+    if lens is None:
+        lens = torch.empty((n_tok,), dtype=torch.int32, device=topk.device)
+    st = lib().dsv4kv_topk_to_slots(_ptr(topk), n_tok, k, _ptr(token_to_req), _ptr(is_valid),
+                                    _ptr(page_table), page_table.shape[0], page_table.shape[1],
+                                    page_bits, _ptr(slots), _ptr(lens), _ptr(err_word),
+                                    _stream(stream))
+    _check("dsv4kv_topk_to_slots", st)
+    return slots, lens
+
+
+class SparsePrefillKVBuffer:
+    """The shared bf16 buffer sparse-prefill layers read, with the reuse head
+    (sglang PR #45909).  Wraps a caller-owned dsv4kv_kvbuf struct and a
+    storage tensor of capacity_rows x 512 bf16."""
+
+    def __init__(self, storage: torch.Tensor):
+        _need(storage, torch.bfloat16, "storage")
+        self.buf = dsv4kv_kvbuf()
+        self.dequants = 0
+        self.dsv4kv_kvbuf_init(storage)
+
+    def dsv4kv_kvbuf_init(self, storage: torch.Tensor):
+        """(Re)allocation: new storage, head forgotten."""
+        self.storage = storage
+        _check("dsv4kv_kvbuf_init",
+               lib().dsv4kv_kvbuf_init(ctypes.byref(self.buf), _ptr(storage), storage.shape[0]))
+
+    def dsv4kv_kvbuf_begin_forward(self):
+        lib().dsv4kv_kvbuf_begin_forward(ctypes.byref(self.buf))
+
+    def dsv4kv_kvbuf_get(self, n: int) -> torch.Tensor:
+        p = ctypes.c_void_p()
+        _check("dsv4kv_kvbuf_get", lib().dsv4kv_kvbuf_get(ctypes.byref(self.buf), n, ctypes.byref(p)))
+        return self.storage[:n]
+
+    def dsv4kv_kvbuf_lookup(self, layout, pool, pool_rows, ids, n) -> bool:
+        hit = ctypes.c_int(0)
+        _check("dsv4kv_kvbuf_lookup",
+               lib().dsv4kv_kvbuf_lookup(ctypes.byref(self.buf), layout, _ptr(pool), pool_rows,
+                                         _ptr(ids), n, ctypes.byref(hit)))
+        return bool(hit.value)
+
+    def dsv4kv_kvbuf_get_with_head(self, layout, pool, ids, *, pool_rows=None, err_word=None,
+                                   stream=None):
+        """(rows, hit): on a miss the gather-dequant fills the storage."""
+        n = ids.numel()
+        pool_bytes = pool.numel() * pool.element_size()
+        if pool_rows is None:
+            pool_rows = pool_bytes // _ROW_BYTES.get(layout, 1)
+        elif pool_rows * _ROW_BYTES.get(layout, 0) > pool_bytes:
+            raise ValueError("pool_rows exceeds the pool tensor")
+        if not ids.is_contiguous():
+            raise ValueError("ids must be contiguous")
+        p = ctypes.c_void_p()
+        hit = ctypes.c_int(0)
+        st = lib().dsv4kv_kvbuf_get_with_head(ctypes.byref(self.buf), layout, _ptr(pool),
+                                              pool_rows, _ptr(ids), n, ctypes.byref(p),
+                                              ctypes.byref(hit), _ptr(err_word), _stream(stream))
+        _check("dsv4kv_kvbuf_get_with_head", st)
+        if not hit.value and n > 0:
+            self.dequants += 1
+        return self.storage[:n], bool(hit.value)

@@ -1,0 +1,227 @@
+// The C ABI (include/dsv4kv.h): argument validation, dispatch to the
+// launchers, and the source-reuse buffer's head (host state only).
+//
+// Every host-checkable error is rejected here, before any CUDA call, so a
+// failing call launches nothing.  Device-only faults are counted by the
+// kernels in the caller's err_word.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dsv4kv.h"
+#include "internal.cuh"
+#include "layout.cuh"
+
+namespace dsv4kv {
+
+static thread_local int g_last_cuda_error = 0;
+
+static int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DSV4KV_OK;
+  g_last_cuda_error = (int)e;
+  return DSV4KV_ECUDA;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int device_sm_count() {
+  constexpr int kMaxDevices = 64;
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < kMaxDevices) cache[dev] = n;
+  return n;
+}
+
+// layout usable by store / dequant: V41 and V41_FP4; V4 is known but not built
+static int check_rw_layout(int layout) {
+  if (layout == DSV4KV_V41 || layout == DSV4KV_V41_FP4) return DSV4KV_OK;
+  if (layout == DSV4KV_V4) return DSV4KV_ENOTSUP;
+  return DSV4KV_EINVAL;
+}
+
+static int check_gather(int layout, const void* pool, long long pool_rows, const int* ids,
+                        long long n, const void* out) {
+  int st = check_rw_layout(layout);
+  if (st != DSV4KV_OK) return st;
+  if (n < 0 || pool_rows < 0) return DSV4KV_EINVAL;
+  if (n > 2147483647LL || pool_rows > DSV4KV_MAX_POOL_ROWS) return DSV4KV_ERANGE;
+  if (n == 0) return DSV4KV_OK;
+  if (!pool || !ids || !out) return DSV4KV_EINVAL;
+  if (!aligned16(pool) || !aligned16(out) || ((uintptr_t)ids & 3u)) return DSV4KV_EINVAL;
+  return DSV4KV_OK;
+}
+
+}  // namespace dsv4kv
+
+using namespace dsv4kv;
+
+extern "C" {
+
+int dsv4kv_row_bytes(int layout) {
+  const int rb = row_bytes_of(layout);
+  return rb > 0 ? rb : DSV4KV_EINVAL;
+}
+
+int dsv4kv_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* dsv4kv_status_string(int status) {
+  switch (status) {
+    case DSV4KV_OK: return "ok";
+    case DSV4KV_EINVAL: return "invalid argument (null or misaligned pointer, bad enum, negative size)";
+    case DSV4KV_ENOTSUP: return "not supported in this build (V4 rows)";
+    case DSV4KV_ERANGE: return "size outside a documented limit";
+    case DSV4KV_ECUDA: return "CUDA launch failed (see dsv4kv_last_cuda_error)";
+    default: return "unknown status";
+  }
+}
+
+int dsv4kv_compress_store(int layout, int ratio, const void* rows, long long n_rows,
+                          long long row_stride, const void* score, long long score_stride,
+                          const int* extend_offsets, int n_slots, const int* page_table,
+                          int max_pages, int page_bits, const void* rmsnorm_w, float eps,
+                          const float* freqs_cis, int max_pos, const int* out_loc, int n_out,
+                          void* pool, long long pool_rows, void* latent_out, float* prequant_out,
+                          int* err_word, void* stream) {
+  int st = check_rw_layout(layout);
+  if (st != DSV4KV_OK) return st;
+  if (ratio != 1 && ratio != 2) return DSV4KV_EINVAL;
+  if (n_out < 0 || n_rows < 0 || n_slots < 0 || pool_rows < 0) return DSV4KV_EINVAL;
+  if (page_bits < 0 || page_bits > 16) return DSV4KV_EINVAL;
+  if (n_slots > DSV4KV_MAX_SLOTS || pool_rows > DSV4KV_MAX_POOL_ROWS) return DSV4KV_ERANGE;
+  if (!(eps >= 0.f)) return DSV4KV_EINVAL;
+  if (n_out == 0) return DSV4KV_OK;
+  if (!rows || !extend_offsets || !pool || pool_rows < 1) return DSV4KV_EINVAL;
+  if (!aligned16(rows) || !aligned16(pool) || (row_stride % 8) != 0) return DSV4KV_EINVAL;
+  if (row_stride < DSV4KV_DIM || (ratio == 2 && !score && row_stride < 2 * DSV4KV_DIM))
+    return DSV4KV_EINVAL;
+  if (score && (ratio != 2 || !aligned16(score) || (score_stride % 8) != 0 ||
+                score_stride < DSV4KV_DIM))
+    return DSV4KV_EINVAL;
+  if (!out_loc && (!page_table || max_pages < 1)) return DSV4KV_EINVAL;
+  if (page_table && max_pages < 1) return DSV4KV_EINVAL;
+  if (rmsnorm_w && !aligned16(rmsnorm_w)) return DSV4KV_EINVAL;
+  if (freqs_cis && (!aligned16(freqs_cis) || max_pos < 1)) return DSV4KV_EINVAL;
+  if ((latent_out && !aligned16(latent_out)) || (prequant_out && !aligned16(prequant_out)))
+    return DSV4KV_EINVAL;
+  if (((uintptr_t)extend_offsets & 3u) || (out_loc && ((uintptr_t)out_loc & 3u)) ||
+      (page_table && ((uintptr_t)page_table & 3u)))
+    return DSV4KV_EINVAL;
+
+  StoreParams p;
+  p.rows = static_cast<const __nv_bfloat16*>(rows);
+  p.n_rows = n_rows;
+  p.row_stride = row_stride;
+  p.score = static_cast<const __nv_bfloat16*>(score);
+  p.score_stride = score_stride;
+  p.ext = extend_offsets;
+  p.n_slots = n_slots;
+  p.page_table = page_table;
+  p.max_pages = page_table ? max_pages : 0;
+  p.page_bits = page_bits;
+  p.norm_w = static_cast<const __nv_bfloat16*>(rmsnorm_w);
+  p.eps = eps;
+  p.freqs = freqs_cis;
+  p.max_pos = freqs_cis ? max_pos : 0;
+  p.out_loc = out_loc;
+  p.n_out = n_out;
+  p.pool = static_cast<uint8_t*>(pool);
+  p.pool_rows = pool_rows;
+  p.latent_out = static_cast<__nv_bfloat16*>(latent_out);
+  p.prequant_out = prequant_out;
+  p.err = err_word;
+  return cuda_status(launch_compress_store(p, layout, ratio, static_cast<cudaStream_t>(stream)));
+}
+
+int dsv4kv_dequant_gather(int layout, const void* pool, long long pool_rows, const int* ids,
+                          long long n, void* out_bf16, int* err_word, void* stream) {
+  int st = check_gather(layout, pool, pool_rows, ids, n, out_bf16);
+  if (st != DSV4KV_OK || n == 0) return st;
+  return cuda_status(launch_dequant_gather(layout, static_cast<const uint8_t*>(pool), pool_rows,
+                                           ids, n, static_cast<__nv_bfloat16*>(out_bf16),
+                                           err_word, static_cast<cudaStream_t>(stream)));
+}
+
+int dsv4kv_topk_to_slots(const int* topk, int n_tok, int k, const int* token_to_req,
+                         const unsigned char* is_valid, const int* page_table, int n_req,
+                         int max_pages, int page_bits, int* slots, int* lens, int* err_word,
+                         void* stream) {
+  if (n_tok < 0 || k < 0 || n_req < 0 || max_pages < 0) return DSV4KV_EINVAL;
+  if (page_bits < 0 || page_bits > 16) return DSV4KV_EINVAL;
+  if (k > 65536) return DSV4KV_ERANGE;
+  if (n_tok == 0) return DSV4KV_OK;
+  if (!token_to_req || !slots || (k > 0 && !topk)) return DSV4KV_EINVAL;
+  if (n_req > 0 && max_pages > 0 && !page_table) return DSV4KV_EINVAL;
+  if (((uintptr_t)topk & 3u) || ((uintptr_t)token_to_req & 3u) || ((uintptr_t)slots & 3u) ||
+      ((uintptr_t)page_table & 3u) || ((uintptr_t)lens & 3u))
+    return DSV4KV_EINVAL;
+  return cuda_status(launch_topk_to_slots(topk, n_tok, k, token_to_req, is_valid, page_table, n_req,
+                                          max_pages, page_bits, slots, lens, err_word,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+// ----------------------------------------------------------------- reuse
+int dsv4kv_kvbuf_init(dsv4kv_kvbuf* buf, void* storage_bf16, long long capacity_rows) {
+  if (!buf || capacity_rows < 0) return DSV4KV_EINVAL;
+  if (capacity_rows > 0 && (!storage_bf16 || !aligned16(storage_bf16))) return DSV4KV_EINVAL;
+  buf->storage = storage_bf16;
+  buf->capacity_rows = capacity_rows;
+  buf->head_valid = 0;
+  buf->head_layout = -1;
+  buf->head_pool = nullptr;
+  buf->head_pool_rows = 0;
+  buf->head_ids = nullptr;
+  buf->head_n = 0;
+  return DSV4KV_OK;
+}
+
+void dsv4kv_kvbuf_begin_forward(dsv4kv_kvbuf* buf) {
+  if (buf) buf->head_valid = 0;
+}
+
+int dsv4kv_kvbuf_get(dsv4kv_kvbuf* buf, long long n, void** rows) {
+  if (!buf || n < 0) return DSV4KV_EINVAL;
+  if (n > buf->capacity_rows) return DSV4KV_ERANGE;
+  buf->head_valid = 0;
+  if (rows) *rows = buf->storage;
+  return DSV4KV_OK;
+}
+
+int dsv4kv_kvbuf_lookup(dsv4kv_kvbuf* buf, int layout, const void* pool, long long pool_rows,
+                        const int* ids, long long n, int* hit) {
+  if (!buf || !hit || n < 0) return DSV4KV_EINVAL;
+  if (n > buf->capacity_rows) return DSV4KV_ERANGE;
+  const bool same = buf->head_valid && buf->head_layout == layout && buf->head_pool == pool &&
+                    buf->head_pool_rows == pool_rows && buf->head_ids == ids && buf->head_n == n;
+  if (same) {
+    *hit = 1;
+    return DSV4KV_OK;
+  }
+  *hit = 0;
+  buf->head_valid = 1;
+  buf->head_layout = layout;
+  buf->head_pool = pool;
+  buf->head_pool_rows = pool_rows;
+  buf->head_ids = ids;
+  buf->head_n = n;
+  return DSV4KV_OK;
+}
+
+int dsv4kv_kvbuf_get_with_head(dsv4kv_kvbuf* buf, int layout, const void* pool,
+                               long long pool_rows, const int* ids, long long n, void** rows,
+                               int* hit, int* err_word, void* stream) {
+  if (!buf || !hit) return DSV4KV_EINVAL;
+  int st = check_gather(layout, pool, pool_rows, ids, n, buf->storage);
+  if (st != DSV4KV_OK) return st;
+  st = dsv4kv_kvbuf_lookup(buf, layout, pool, pool_rows, ids, n, hit);
+  if (st != DSV4KV_OK) return st;
+  if (rows) *rows = buf->storage;
+  if (*hit || n == 0) return DSV4KV_OK;
+  st = dsv4kv_dequant_gather(layout, pool, pool_rows, ids, n, buf->storage, err_word, stream);
+  if (st != DSV4KV_OK) buf->head_valid = 0;
+  return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// Launch parameters and launchers shared between the kernel files and the
+// C-ABI layer.  Everything here is device-pointer plumbing; argument checks
+// happen in capi.cu before any launcher is reached.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace dsv4kv {
+
+struct StoreParams {
+  const __nv_bfloat16* rows;   // [n_rows, row_stride]
+  long long n_rows;
+  long long row_stride;        // elements
+  const __nv_bfloat16* score;  // nullptr: rows + 512 (fused | kv | score |)
+  long long score_stride;
+  const int* ext;              // [2, n_slots]
+  int n_slots;
+  const int* page_table;       // [n_slots, max_pages] or nullptr (out_loc given)
+  int max_pages;
+  int page_bits;
+  const __nv_bfloat16* norm_w; // [512] or nullptr
+  float eps;
+  const float* freqs;          // [max_pos, 64] or nullptr
+  int max_pos;
+  const int* out_loc;          // [n_out] or nullptr
+  int n_out;
+  uint8_t* pool;
+  long long pool_rows;
+  __nv_bfloat16* latent_out;   // [n_out, 512] or nullptr
+  float* prequant_out;         // [n_out, 512] or nullptr
+  int* err;                    // device fault counter or nullptr
+};
+
+cudaError_t launch_compress_store(const StoreParams& p, int layout, int ratio, cudaStream_t stream);
+
+cudaError_t launch_dequant_gather(int layout, const uint8_t* pool, long long pool_rows,
+                                  const int* ids, long long n, __nv_bfloat16* out, int* err,
+                                  cudaStream_t stream);
+
+cudaError_t launch_topk_to_slots(const int* topk, int n_tok, int k, const int* token_to_req,
+                                 const unsigned char* is_valid, const int* page_table, int n_req,
+                                 int max_pages, int page_bits, int* slots, int* lens, int* err,
+                                 cudaStream_t stream);
+
+// Streaming 16-byte global load that bypasses L1 (inputs read exactly once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+  uint2 v;
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+  uint32_t v;
+  asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// SM count and resident blocks per SM for a kernel, for persistent grids.
+int device_sm_count();
+
+}  // namespace dsv4kv

@@ -1,0 +1,73 @@
+// Request-local top-k compressed ids -> physical pool slots, plus the count
+// of valid slots per row.
+//
+// flashinfer_sparse.py, _compressed_topk_to_slots (single-rank branch,
+// compute_global_topk_indices_and_lens): the indexer's request-local ids map
+// through the request's block table; compressed pages hold
+// block_size // compress_ratio states (here 2^page_bits rows); empty entries
+// become -1; CUDA-graph padding rows (is_valid_token == 0) attend nothing.
+//
+// One CTA per token row; threads stride over the k entries (coalesced int32
+// reads and writes), then a block reduction produces the row's count.
+#include "internal.cuh"
+
+namespace dsv4kv {
+
+constexpr int kTopkThreads = 256;
+
+__global__ void __launch_bounds__(kTopkThreads)
+topk_to_slots_kernel(const int* __restrict__ topk, int n_tok, int k,
+                     const int* __restrict__ token_to_req, const unsigned char* __restrict__ is_valid,
+                     const int* __restrict__ page_table, int n_req, int max_pages, int page_bits,
+                     int* __restrict__ slots, int* __restrict__ lens, int* err) {
+  __shared__ int s_cnt[kTopkThreads / 32];
+  const unsigned mask = (1u << page_bits) - 1u;
+  for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
+    const int r = token_to_req[t];
+    const bool bad_req = r < 0 || r >= n_req;
+    const bool tok_ok = !bad_req && (is_valid == nullptr || is_valid[t] != 0);
+    if (bad_req && threadIdx.x == 0 && err) atomicAdd(err, 1);
+    int cnt = 0;
+    const long long rowoff = (long long)t * k;
+    for (int c = threadIdx.x; c < k; c += blockDim.x) {
+      const int id = topk[rowoff + c];
+      int s = -1;
+      if (tok_ok && id >= 0) {
+        const int lp = id >> page_bits;
+        if (lp < max_pages) {
+          const unsigned phys = (unsigned)page_table[(long long)r * max_pages + lp];
+          s = (int)((phys << page_bits) | ((unsigned)id & mask));
+        } else if (err) {
+          atomicAdd(err, 1);
+        }
+      }
+      slots[rowoff + c] = s;
+      cnt += s >= 0;
+    }
+    if (lens) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      if ((threadIdx.x & 31) == 0) s_cnt[threadIdx.x >> 5] = cnt;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int sum = 0;
+        for (int w = 0; w < kTopkThreads / 32; ++w) sum += s_cnt[w];
+        lens[t] = sum;
+      }
+      __syncthreads();
+    }
+  }
+}
+
+cudaError_t launch_topk_to_slots(const int* topk, int n_tok, int k, const int* token_to_req,
+                                 const unsigned char* is_valid, const int* page_table, int n_req,
+                                 int max_pages, int page_bits, int* slots, int* lens, int* err,
+                                 cudaStream_t stream) {
+  const int grid = n_tok < 65535 * 4 ? n_tok : 65535 * 4;
+  topk_to_slots_kernel<<<grid, kTopkThreads, 0, stream>>>(topk, n_tok, k, token_to_req, is_valid,
+                                                          page_table, n_req, max_pages, page_bits,
+                                                          slots, lens, err);
+  return cudaGetLastError();
+}
+
+}  // namespace dsv4kv

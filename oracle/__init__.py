@@ -68,7 +68,7 @@ def _load():
             "orc_row_offset": (L, [I, I, L]),
             "orc_plan": (L, [I, P, I, P, I, I, L, P, P, P, P, P]),
             "orc_compress_store": (L, [I, I, P, L, L, P, L, P, I, P, I, I, P, F,
-                                       P, I, P, L, P, L, P, P, P, P, P]),
+                                       P, I, P, L, P, L, P, L, P, P, P, P, P]),
             "orc_dequant_gather": (L, [I, P, L, P, L, P]),
             "orc_topk_to_slots": (L, [P, L, I, P, P, P, I, I, I, P, P]),
             "orc_ue8m0_many": (None, [P, L, P]),
@@ -197,10 +197,12 @@ def plan(ratio, ext, page_table=None, page_bits=0):
 def compress_store(layout, ratio, rows, ext, *, score=None, page_table=None,
                    page_bits=0, norm_w=None, eps=1e-6, freqs=None, out_loc=None,
                    n_out=None, pool=None, pool_rows=None, prequant_in=None,
-                   want_f64=True, want_f32=True, want_latent=True):
+                   want_f64=True, want_f32=True, want_latent=True, which=None):
     """Run the fp64 compressor.  rows/score are bf16 bit arrays (uint16) with
     rows of width >= 512 (the fused | kv | score | layout when ratio == 2 and
-    score is None).  pool (uint8, flat) is updated in place.  Returns a dict
+    score is None).  pool (uint8, flat) is updated in place.  `which` (int64
+    output-row indices) restricts the work to those rows; per-row outputs and
+    prequant_in are then indexed by position in `which`.  Returns a dict
     with total, faults and the requested per-row outputs."""
     rows = _c(rows, np.uint16)
     n_rows, row_stride = rows.shape
@@ -221,14 +223,17 @@ def compress_store(layout, ratio, rows, ext, *, score=None, page_table=None,
         if pool_rows is None:
             pool_rows = pool.size // row_bytes(layout)
     pre_in = _c(prequant_in, np.float32)
-    f64 = np.zeros((n_out, D), np.float64) if want_f64 else None
-    f32 = np.zeros((n_out, D), np.float32) if want_f32 else None
-    lat = np.zeros((n_out, D), np.uint16) if want_latent else None
+    which = _c(which, np.int64)
+    n_rows_out = n_out if which is None else which.size
+    f64 = np.zeros((n_rows_out, D), np.float64) if want_f64 else None
+    f32 = np.zeros((n_rows_out, D), np.float32) if want_f32 else None
+    lat = np.zeros((n_rows_out, D), np.uint16) if want_latent else None
     faults = ctypes.c_int64(0)
     total = _load().orc_compress_store(
         layout, ratio, _ptr(rows), n_rows, row_stride, _ptr(score), score_stride,
         _ptr(ext), n_slots, _ptr(pt), max_pages, page_bits, _ptr(norm_w), eps,
-        _ptr(freqs), max_pos, _ptr(out_loc), n_out, _ptr(pool),
+        _ptr(freqs), max_pos, _ptr(out_loc), n_out, _ptr(which),
+        0 if which is None else which.size, _ptr(pool),
         0 if pool_rows is None else pool_rows, _ptr(pre_in), _ptr(f64), _ptr(f32),
         _ptr(lat), ctypes.addressof(faults))
     if total < 0:

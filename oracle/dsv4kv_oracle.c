@@ -325,6 +325,9 @@ int64_t orc_plan(int ratio, const int32_t *ext, int n_slots,
 /*        (cos, sin) per complex pair, or NULL (no RoPE).                    */
 /* out_loc: int32 [n_out] slot per output row (0 = not stored), or NULL to   */
 /*        use the plan's page-table slot.  Rows k >= total have no source.   */
+/* which: NULL, or the output rows to compute (n_which of them, each in      */
+/*        [0, n_out)); per-row outputs and prequant_in are then indexed by  */
+/*        position in `which`.  Used to check sampled rows of large cases.  */
 /* prequant_in: if non-NULL, the fp32 rows fed to the quantizer are these    */
 /*        ("identical-input" mode) instead of this oracle's fp64 result      */
 /*        rounded to fp32.                                                   */
@@ -340,12 +343,13 @@ int64_t orc_compress_store(
     const uint16_t *norm_w, float eps,
     const float *freqs, int max_pos,
     const int32_t *out_loc, int64_t n_out,
+    const int64_t *which, int64_t n_which,
     uint8_t *pool, int64_t pool_rows,
     const float *prequant_in,
     double *prequant_f64, float *prequant_f32, uint16_t *latent_out,
     int64_t *n_faults)
 {
-    int64_t total, k, faults = 0;
+    int64_t total, k, o, faults = 0;
     int32_t *req, *jj, *pos;
     int64_t *src, *pslot;
     int rb = orc_row_bytes(layout);
@@ -355,6 +359,8 @@ int64_t orc_compress_store(
 
     if (ratio != 1 && ratio != 2) return -1;
     if (layout != ORC_V41 && layout != ORC_V41_FP4) return -2;
+    for (o = 0; which && o < n_which; ++o)
+        if (which[o] < 0 || which[o] >= n_out) return -1;
     total = orc_plan(ratio, ext, n_slots, page_table, max_pages, page_bits,
                      0, NULL, NULL, NULL, NULL, NULL);
     req = (int32_t *)calloc((size_t)(total + 1), sizeof(int32_t));
@@ -365,13 +371,14 @@ int64_t orc_compress_store(
     orc_plan(ratio, ext, n_slots, page_table, max_pages, page_bits,
              total, req, jj, src, pos, pslot);
 
-    for (k = 0; k < n_out; ++k) {
+    for (o = 0; o < (which ? n_which : n_out); ++o) {
         int d, t, bad = 0;
         int64_t slot;
+        k = which ? which[o] : o;
         if (k >= total) { /* no source row: nothing computed or stored */
-            if (prequant_f64) memset(prequant_f64 + k * ORC_D, 0, ORC_D * sizeof(double));
-            if (prequant_f32) memset(prequant_f32 + k * ORC_D, 0, ORC_D * sizeof(float));
-            if (latent_out) memset(latent_out + k * ORC_D, 0, ORC_D * sizeof(uint16_t));
+            if (prequant_f64) memset(prequant_f64 + o * ORC_D, 0, ORC_D * sizeof(double));
+            if (prequant_f32) memset(prequant_f32 + o * ORC_D, 0, ORC_D * sizeof(float));
+            if (latent_out) memset(latent_out + o * ORC_D, 0, ORC_D * sizeof(uint16_t));
             continue;
         }
         if (src[k] < 0 || src[k] + ratio > n_rows) bad = 1;
@@ -379,9 +386,9 @@ int64_t orc_compress_store(
         slot = out_loc ? (int64_t)out_loc[k] : pslot[k];
         if (bad) { /* a row that cannot be computed: zero outputs, one fault */
             ++faults;
-            if (prequant_f64) memset(prequant_f64 + k * ORC_D, 0, ORC_D * sizeof(double));
-            if (prequant_f32) memset(prequant_f32 + k * ORC_D, 0, ORC_D * sizeof(float));
-            if (latent_out) memset(latent_out + k * ORC_D, 0, ORC_D * sizeof(uint16_t));
+            if (prequant_f64) memset(prequant_f64 + o * ORC_D, 0, ORC_D * sizeof(double));
+            if (prequant_f32) memset(prequant_f32 + o * ORC_D, 0, ORC_D * sizeof(float));
+            if (latent_out) memset(latent_out + o * ORC_D, 0, ORC_D * sizeof(uint16_t));
             continue;
         }
 
@@ -412,7 +419,7 @@ int64_t orc_compress_store(
             for (d = 0; d < ORC_D; ++d) x[d] = x[d] * inv * orc_bf16_value(norm_w[d]);
         }
         if (latent_out)
-            for (d = 0; d < ORC_D; ++d) latent_out[k * ORC_D + d] = orc_bf16_bits(x[d]);
+            for (d = 0; d < ORC_D; ++d) latent_out[o * ORC_D + d] = orc_bf16_bits(x[d]);
         /* RoPE on the 64 rope dims, interleaved complex pairs
          * (448+2i, 449+2i) rotated by (cos, sin) = freqs[pos][2i], [2i+1] */
         if (freqs) {
@@ -426,9 +433,9 @@ int64_t orc_compress_store(
             }
         }
         for (d = 0; d < ORC_D; ++d) {
-            xf[d] = prequant_in ? prequant_in[k * ORC_D + d] : (float)x[d];
-            if (prequant_f64) prequant_f64[k * ORC_D + d] = x[d];
-            if (prequant_f32) prequant_f32[k * ORC_D + d] = (float)x[d];
+            xf[d] = prequant_in ? prequant_in[o * ORC_D + d] : (float)x[d];
+            if (prequant_f64) prequant_f64[o * ORC_D + d] = x[d];
+            if (prequant_f32) prequant_f32[o * ORC_D + d] = (float)x[d];
         }
         /* quantize and write; out_loc == 0 marks a row that is not stored;
          * a destination outside the pool (or past the page table) is one

@@ -1,0 +1,123 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark times.  Where the oracle cannot redo everything in seconds it
+checks sampled rows one by one (the oracle's row-subset mode), plus
+properties that hold at any size (every planned slot written exactly once,
+every other byte untouched, reuse == fresh dequant)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_v4_compressed_c2_gb300 import workloads as W
+from parity import assert_prequant_close, compare_rows_end_to_end, dev, dev_bf16, host_u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from deepseek_v4_compressed_c2_gb300 import build as b
+    b.build()
+    from deepseek_v4_compressed_c2_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _store(B, cfg, pool, *, prequant=None, err=None):
+    B.dsv4kv_compress_store(
+        cfg["layout"], cfg["ratio"], dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
+        page_table=dev(cfg["page_table"]), page_bits=cfg["page_bits"],
+        rmsnorm_w=None if cfg["norm_w"] is None else dev_bf16(cfg["norm_w"]), eps=cfg["eps"],
+        freqs_cis=None if cfg["freqs"] is None else dev(cfg["freqs"]), n_out=cfg["n_out"],
+        prequant_out=prequant, err_word=err)
+
+
+def test_fp4_store_and_full_dequant_32768_rows(B):
+    cfg = W.cfg3_fp4_store()
+    rb = 288
+    pool = torch.full((cfg["pool_rows"] * rb,), 0xA5, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _store(B, cfg, pool, err=err)
+    ids = dev(np.arange(128, 128 + 32768, dtype=np.int32))
+    out = B.dsv4kv_dequant_gather(cfg["layout"], pool, ids, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref_pool = np.full(cfg["pool_rows"] * rb, 0xA5, np.uint8)
+    oracle.compress_store(cfg["layout"], 1, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
+                          page_bits=cfg["page_bits"], pool=ref_pool, pool_rows=cfg["pool_rows"],
+                          want_f64=False, want_f32=False, want_latent=False)
+    assert np.array_equal(pool.cpu().numpy(), ref_pool)
+    want, _ = oracle.dequant_gather(cfg["layout"], ref_pool, cfg["pool_rows"], ids.cpu().numpy())
+    assert np.array_equal(host_u16(out), want)
+
+
+def test_gather_262144_of_1m_rows_with_4_layer_reuse(B):
+    cfg = W.cfg4_gather()
+    rb = 528
+    pool = torch.zeros(cfg["pool_rows"] * rb, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _store(B, cfg, pool, err=err)
+    ids = dev(cfg["ids"])
+    buf = B.SparsePrefillKVBuffer(torch.empty((len(cfg["ids"]), 512), dtype=torch.bfloat16,
+                                              device="cuda"))
+    buf.dsv4kv_kvbuf_begin_forward()
+    hits = [buf.dsv4kv_kvbuf_get_with_head(1, pool, ids, err_word=err)[1] for _ in range(cfg["layers"])]
+    assert hits == [False, True, True, True] and buf.dequants == 1
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    host_pool = pool.cpu().numpy()
+    # the store: sampled rows against the oracle's quantizer (store-only rows
+    # are the bf16 inputs exactly)
+    rng = np.random.default_rng(0)
+    sample = rng.choice(cfg["n_out"], 4096, replace=False)
+    x = oracle.bf16_to_f64(cfg["rows"][sample]).astype(np.float32)
+    want_rows = oracle.quantize_rows(1, x)
+    got_rows = host_pool.reshape(-1, rb)[64 + sample]
+    assert np.array_equal(got_rows, want_rows)
+    assert not host_pool[:64 * rb].any()                        # page 0 untouched
+    # the gather: every row, bit-exact against the oracle's dequant of the pool
+    want, faults = oracle.dequant_gather(1, host_pool, cfg["pool_rows"], cfg["ids"])
+    assert faults == 0
+    assert np.array_equal(host_u16(buf.storage), want)
+
+
+def test_long_prefill_ratio2_store_and_topk_gather(B):
+    cfg = W.cfg5_long_prefill()
+    rb = 528
+    pool = torch.full((cfg["pool_rows"] * rb,), 0xA5, dtype=torch.uint8, device="cuda")
+    pre = torch.empty((cfg["n_out"], 512), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _store(B, cfg, pool, prequant=pre, err=err)
+    slots, lens = B.dsv4kv_topk_to_slots(dev(cfg["topk"]), dev(cfg["token_to_req"]),
+                                         dev(cfg["page_table"]), cfg["page_bits"], err_word=err)
+    out = B.dsv4kv_dequant_gather(1, pool, slots.view(-1), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    host_pool = pool.cpu().numpy()
+    p = oracle.plan(2, cfg["ext"], cfg["page_table"], cfg["page_bits"])
+    assert p["total"] == cfg["n_out"]
+    # every planned slot written once, every other row untouched
+    untouched = np.all(host_pool.reshape(-1, rb) == 0xA5, axis=1)
+    assert untouched.sum() == cfg["pool_rows"] - p["total"]
+    assert not untouched[p["slot"]].any()
+    # sampled rows: end-to-end tolerance and identical-input bit-exactness
+    rng = np.random.default_rng(1)
+    which = np.sort(rng.choice(p["total"], 2048, replace=False)).astype(np.int64)
+    ref = oracle.compress_store(1, 2, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
+                                page_bits=cfg["page_bits"], norm_w=cfg["norm_w"], eps=cfg["eps"],
+                                freqs=cfg["freqs"], n_out=cfg["n_out"], which=which,
+                                want_latent=False)
+    g_pre = pre.cpu().numpy()[which]
+    assert_prequant_close(g_pre, ref["prequant_f64"])
+    got_rows = host_pool.reshape(-1, rb)[p["slot"][which]]
+    same = oracle.quantize_rows(1, g_pre)
+    assert np.array_equal(got_rows, same)
+    e2e = oracle.quantize_rows(1, ref["prequant_f32"])
+    compare_rows_end_to_end(1, got_rows, e2e, ref["prequant_f64"])
+    # top-k -> slots, then the gather, against the oracle
+    ws, wl, faults = oracle.topk_to_slots(cfg["topk"], cfg["token_to_req"], cfg["page_table"],
+                                          cfg["page_bits"])
+    assert faults == 0
+    assert np.array_equal(slots.cpu().numpy(), ws) and np.array_equal(lens.cpu().numpy(), wl)
+    want, _ = oracle.dequant_gather(1, host_pool, cfg["pool_rows"], ws.reshape(-1))
+    assert np.array_equal(host_u16(out), want)

@@ -1,0 +1,366 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Covers the V41 round trip and ratio-2 compressor workloads, brute-force tiny
+ragged cases over both layouts, both ratios and every norm/rope combination,
+the padding / out_loc == 0 / fault rules, dequant of arbitrary bytes, the
+top-k -> slot mapping, the reuse buffer, CUDA-graph replay with offsets
+refreshed in place, and byte determinism with a negative control."""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_v4_compressed_c2_gb300 import workloads as W
+from parity import (assert_bf16_equal_nan_aware, assert_prequant_close,
+                    compare_rows_end_to_end, dev, dev_bf16, host_u16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from deepseek_v4_compressed_c2_gb300 import build as b
+    b.build()
+    from deepseek_v4_compressed_c2_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def gpu_store(B, cfg, *, out_loc=None, n_out=None, pool_fill=0, want_pre=True, want_lat=True,
+              score=None):
+    rb = oracle.row_bytes(cfg["layout"])
+    n_out = cfg["n_out"] if n_out is None else n_out
+    pool = torch.full((cfg["pool_rows"] * rb,), pool_fill, dtype=torch.uint8, device="cuda")
+    pre = torch.full((n_out, 512), 7.0, dtype=torch.float32, device="cuda") if want_pre else None
+    lat = torch.full((n_out, 512), 7.0, dtype=torch.bfloat16, device="cuda") if want_lat else None
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsv4kv_compress_store(
+        cfg["layout"], cfg["ratio"], dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
+        score=None if score is None else dev_bf16(score),
+        page_table=None if cfg["page_table"] is None else dev(cfg["page_table"]),
+        page_bits=cfg["page_bits"],
+        rmsnorm_w=None if cfg["norm_w"] is None else dev_bf16(cfg["norm_w"]), eps=cfg["eps"],
+        freqs_cis=None if cfg["freqs"] is None else dev(cfg["freqs"]),
+        out_loc=None if out_loc is None else dev(out_loc), n_out=n_out,
+        latent_out=lat, prequant_out=pre, err_word=err)
+    torch.cuda.synchronize()
+    return dict(pool=pool.cpu().numpy(), err=int(err.item()),
+                pre=None if pre is None else pre.cpu().numpy(),
+                lat=None if lat is None else host_u16(lat))
+
+
+def oracle_store(cfg, *, out_loc=None, n_out=None, pool_fill=0, prequant_in=None, score=None):
+    rb = oracle.row_bytes(cfg["layout"])
+    pool = np.full(cfg["pool_rows"] * rb, pool_fill, np.uint8)
+    res = oracle.compress_store(
+        cfg["layout"], cfg["ratio"], cfg["rows"], cfg["ext"], score=score,
+        page_table=cfg["page_table"], page_bits=cfg["page_bits"], norm_w=cfg["norm_w"],
+        eps=cfg["eps"], freqs=cfg["freqs"], out_loc=out_loc,
+        n_out=cfg["n_out"] if n_out is None else n_out, pool=pool, pool_rows=cfg["pool_rows"],
+        prequant_in=prequant_in)
+    res["pool"] = pool
+    return res
+
+
+def check_store(B, cfg, *, out_loc=None, min_allowed=0, exact_codes=False):
+    """Full parity of one compress_store call: identical-input bytes, end-to-end
+    tolerance, latent, padding, untouched bytes."""
+    g = gpu_store(B, cfg, out_loc=out_loc, pool_fill=0xA5)
+    ref = oracle_store(cfg, out_loc=out_loc, pool_fill=0xA5)
+    same = oracle_store(cfg, out_loc=out_loc, pool_fill=0xA5, prequant_in=g["pre"])
+    assert g["err"] == ref["faults"]
+    # codes and scales bit-exact given the GPU's own fp32 pre-quant rows
+    assert np.array_equal(g["pool"], same["pool"])
+    total = ref["total"]
+    assert_prequant_close(g["pre"][:total], ref["prequant_f64"][:total])
+    assert not g["pre"][total:].any() and not g["lat"][total:].any()
+    # latent (bf16, post-norm pre-RoPE) within the same tolerance
+    lat_g = oracle.bf16_to_f64(g["lat"][:total])
+    lat_r = oracle.bf16_to_f64(ref["latent"][:total])
+    ulp = np.abs(lat_r) * 2.0 ** -7
+    assert np.all(np.abs(lat_g - lat_r) <= ulp + 1e-5 * np.abs(lat_r).max(axis=1, keepdims=True))
+    rb = oracle.row_bytes(cfg["layout"])
+    gp = g["pool"].reshape(-1, rb)
+    rp = ref["pool"].reshape(-1, rb)
+    written = ~np.all(rp == 0xA5, axis=1) | ~np.all(gp == 0xA5, axis=1)
+    assert np.array_equal(np.all(gp == 0xA5, axis=1), np.all(rp == 0xA5, axis=1))
+    if exact_codes:
+        assert np.array_equal(gp, rp)
+    elif written.any():
+        pre_by_slot = np.zeros((gp.shape[0], 512))
+        slots = _slots_of(cfg, out_loc, total)
+        ok = (slots > 0) & (slots < cfg["pool_rows"])
+        pre_by_slot[slots[ok]] = ref["prequant_f64"][:total][ok]
+        compare_rows_end_to_end(cfg["layout"], gp[written], rp[written], pre_by_slot[written],
+                                min_allowed=min_allowed)
+    return g, ref
+
+
+def _slots_of(cfg, out_loc, total):
+    if out_loc is not None:
+        return np.asarray(out_loc[:total], np.int64)
+    p = oracle.plan(cfg["ratio"], cfg["ext"], cfg["page_table"], cfg["page_bits"])
+    return p["slot"]
+
+
+# ---------------------------------------------------------------- configs
+def test_v41_round_trip_256_rows_bit_exact(B):
+    cfg = W.cfg1_v41_roundtrip()
+    g, ref = check_store(B, cfg, exact_codes=True)
+    ids = np.arange(64, 64 + 256, dtype=np.int32)
+    out = B.dsv4kv_dequant_gather(cfg["layout"], dev(g["pool"]), dev(ids))
+    want, _ = oracle.dequant_gather(cfg["layout"], ref["pool"], cfg["pool_rows"], ids)
+    assert np.array_equal(host_u16(out), want)
+
+
+def test_ratio2_compressor_4_requests(B):
+    cfg = W.cfg2_ratio2_small()
+    g, ref = check_store(B, cfg)
+    assert ref["total"] == 1809
+    # explicit out_loc from the plan, with some real rows marked 0 (not stored)
+    p = oracle.plan(2, cfg["ext"], cfg["page_table"], cfg["page_bits"])
+    out_loc = np.zeros(cfg["n_out"], np.int32)
+    out_loc[:p["total"]] = p["slot"]
+    out_loc[::7] = 0
+    check_store(B, cfg, out_loc=out_loc)
+
+
+def test_ratio2_separate_score_buffer_matches_fused(B):
+    cfg = W.cfg2_ratio2_small()
+    fused = gpu_store(B, cfg)
+    split = dict(cfg)
+    split["rows"] = np.ascontiguousarray(cfg["rows"][:, :512])
+    score = np.ascontiguousarray(cfg["rows"][:, 512:])
+    g = gpu_store(B, split, score=score)
+    assert np.array_equal(g["pool"], fused["pool"])
+    assert np.array_equal(g["pre"], fused["pre"])
+
+
+# ------------------------------------------------------------ brute force
+def _random_case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    layout = [oracle.V41, oracle.V41_FP4][seed % 2]
+    ratio = 1 + (seed // 2) % 2
+    norm = bool(rng.integers(0, 2))
+    rope = bool(rng.integers(0, 2))
+    n_req = int(rng.integers(0, 6))
+    lens = [int(v) for v in rng.integers(0, 150, n_req)]
+    if n_req and seed % 5 == 0:
+        lens[0] = 1                                           # a lone (odd) token
+    page_bits = int(rng.integers(0, 6))
+    per = [n // ratio for n in lens]
+    pages = [-(-p // (1 << page_bits)) for p in per]
+    phys = rng.permutation(sum(pages) + 3) + 1
+    max_pages = max([1] + pages)
+    pt = np.zeros((max(n_req, 1) + 2, max_pages), np.int32)
+    o = 0
+    for r, p in enumerate(pages):
+        pt[r, :p] = phys[o:o + p]
+        o += p
+    pool_rows = (sum(pages) + 4) << page_bits
+    t = sum(lens) + 3
+    scale = rng.choice([1.0, 1e-3, 30.0])
+    x = (rng.standard_normal((t, 1024)) * scale).astype(np.float32)
+    x[rng.random(x.shape) < 0.01] *= 50
+    rows = W.bf16_from_f32(x)
+    ext = np.zeros((2, max(n_req, 1) + 2), np.int32)
+    ext[0, :n_req] = np.concatenate([[0], np.cumsum(lens)[:-1]]) if n_req else []
+    ext[1, :n_req] = lens
+    total = sum(per)
+    n_out = total + int(rng.integers(0, 40))
+    return dict(layout=layout, ratio=ratio, rows=rows, ext=ext, page_table=pt,
+                page_bits=page_bits, norm_w=W.bf16_from_f32(rng.uniform(0.5, 1.5, 512).astype(np.float32)) if norm else None,
+                freqs=W.rope_table(512) if rope else None, eps=1e-6, n_out=max(n_out, 1),
+                pool_rows=pool_rows)
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_brute_force_tiny_cases(B, seed):
+    cfg = _random_case(seed)
+    check_store(B, cfg, min_allowed=2)
+
+
+def test_every_layout_ratio_norm_rope_combination(B):
+    base = W.cfg2_ratio2_small()
+    for layout in (oracle.V41, oracle.V41_FP4):
+        for ratio in (1, 2):
+            for norm in (False, True):
+                for rope in (False, True):
+                    cfg = dict(base, layout=layout, ratio=ratio,
+                               norm_w=base["norm_w"] if norm else None,
+                               freqs=base["freqs"] if rope else None, n_out=2048)
+                    if ratio == 1:
+                        cfg["n_out"] = 3620 + 20
+                        cfg["pool_rows"] = 130 << 6
+                        pt = np.zeros((8, 64), np.int32)
+                        o = 1
+                        for r, n in enumerate(base["lengths"]):
+                            k = -(-n // 64)
+                            pt[r, :k] = np.arange(o, o + k)
+                            o += k
+                        cfg["page_table"] = pt
+                    check_store(B, cfg, min_allowed=3)
+
+
+# ------------------------------------------------------------ edge cases
+def test_empty_and_all_padding_calls(B):
+    cfg = W.cfg1_v41_roundtrip()
+    cfg0 = dict(cfg, ext=np.zeros((2, 3), np.int32), n_out=50)
+    g = gpu_store(B, cfg0, pool_fill=0x33)
+    assert (g["pool"] == 0x33).all() and not g["pre"].any() and g["err"] == 0
+    cfg_none = dict(cfg, ext=np.zeros((2, 0), np.int32), n_out=8)
+    g = gpu_store(B, cfg_none, pool_fill=0x33)
+    assert (g["pool"] == 0x33).all() and not g["pre"].any()
+    pool = torch.zeros(100, dtype=torch.uint8, device="cuda")
+    B.dsv4kv_compress_store(1, 1, dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
+                            page_table=dev(cfg["page_table"]), page_bits=6, n_out=0)
+    out = B.dsv4kv_dequant_gather(1, pool, torch.zeros(0, dtype=torch.int32, device="cuda"))
+    assert out.shape == (0, 512)
+
+
+def test_device_faults_are_counted_not_trapped(B):
+    cfg = W.cfg2_ratio2_small()
+    bad = dict(cfg, ext=cfg["ext"].copy(), freqs=W.rope_table(600))
+    bad["ext"][1, 3] = 2047 + 2000          # request 3 runs past the rows buffer
+    bad["ext"][0, 2] = -5                   # a negative first row
+    g = gpu_store(B, bad, pool_fill=0xA5)
+    ref = oracle_store(bad, pool_fill=0xA5)
+    assert g["err"] == ref["faults"] > 0
+    same = oracle_store(bad, pool_fill=0xA5, prequant_in=g["pre"])
+    assert np.array_equal(g["pool"], same["pool"])
+    # destinations outside the pool and past the page table
+    cfg1 = W.cfg1_v41_roundtrip()
+    out_loc = np.arange(64, 64 + 256, dtype=np.int32)
+    out_loc[[3, 9]] = [cfg1["pool_rows"], -7]
+    g = gpu_store(B, cfg1, out_loc=out_loc, pool_fill=0xA5)
+    assert g["err"] == 2
+    short_pt = dict(cfg1, page_table=cfg1["page_table"][:, :2].copy())
+    g = gpu_store(B, short_pt, pool_fill=0xA5)
+    assert g["err"] == 128
+    # gather: ids past the pool are faults and zero rows, negative ids zero rows
+    pool = dev(oracle_store(cfg1)["pool"])
+    ids = np.array([64, -1, 320, 1 << 30, 70], np.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = host_u16(B.dsv4kv_dequant_gather(1, pool, dev(ids), err_word=err))
+    want, faults = oracle.dequant_gather(1, pool.cpu().numpy(), cfg1["pool_rows"], ids)
+    assert int(err.item()) == faults == 2
+    assert np.array_equal(out, want)
+
+
+def test_host_argument_errors_raise(B):
+    cfg = W.cfg1_v41_roundtrip()
+    pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device="cuda")
+    with pytest.raises(B.DSV4KVError) as e:
+        B.dsv4kv_compress_store(0, 1, dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
+                                page_table=dev(cfg["page_table"]), page_bits=6, n_out=4)
+    assert e.value.status == -2
+    with pytest.raises(B.DSV4KVError):
+        B.dsv4kv_compress_store(1, 3, dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
+                                page_table=dev(cfg["page_table"]), page_bits=6, n_out=4)
+    with pytest.raises(B.DSV4KVError):
+        B.dsv4kv_dequant_gather(1, pool[1:], torch.zeros(4, dtype=torch.int32, device="cuda"))
+
+
+@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4])
+def test_dequant_of_arbitrary_bytes(B, layout):
+    rng = np.random.default_rng(77 + layout)
+    rb = oracle.row_bytes(layout)
+    n = 777
+    pool = rng.integers(0, 256, (n, rb), dtype=np.uint8)
+    if layout == oracle.V41:
+        pool[:, 512:] = rng.integers(0, 256, (n, 16), dtype=np.uint8)
+        pool[:4, 512:] = [[0], [1], [254], [255]]           # scale-byte extremes
+    ids = rng.permutation(n).astype(np.int32)
+    out = host_u16(B.dsv4kv_dequant_gather(layout, dev(pool.reshape(-1)), dev(ids)))
+    want, _ = oracle.dequant_gather(layout, pool.reshape(-1), n, ids)
+    assert_bf16_equal_nan_aware(out, want)
+
+
+def test_topk_to_slots_matches_oracle(B):
+    rng = np.random.default_rng(8)
+    n_req, k, page_bits = 9, 333, 4
+    pt = rng.integers(1, 5000, (n_req, 40), dtype=np.int32)
+    topk = rng.integers(-2, 40 << page_bits, (50, k), dtype=np.int32)
+    topk[3, 5] = 45 << page_bits                              # past max_pages
+    ttr = rng.integers(0, n_req, 50).astype(np.int32)
+    ttr[7] = n_req + 3                                         # bad request
+    valid = (rng.random(50) > 0.2).astype(np.uint8)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots, lens = B.dsv4kv_topk_to_slots(dev(topk), dev(ttr), dev(pt), page_bits,
+                                         is_valid=dev(valid), err_word=err)
+    ws, wl, faults = oracle.topk_to_slots(topk, ttr, pt, page_bits, is_valid=valid)
+    assert np.array_equal(slots.cpu().numpy(), ws)
+    assert np.array_equal(lens.cpu().numpy(), wl)
+    assert int(err.item()) == faults
+
+
+def test_reuse_buffer_hits_equal_a_fresh_dequant(B):
+    """Layers sharing a kv_source reuse one dequant; the reused rows equal a
+    fresh dequant of the same rows (sglang PR #45909 verification)."""
+    cfg = W.cfg2_ratio2_small()
+    g = gpu_store(B, cfg)
+    pool = dev(g["pool"])
+    ids = dev(np.random.default_rng(3).permutation(np.arange(64, 4160))[:1500].astype(np.int32))
+    buf = B.SparsePrefillKVBuffer(torch.empty((2048, 512), dtype=torch.bfloat16, device="cuda"))
+    buf.dsv4kv_kvbuf_begin_forward()
+    hits = []
+    for _layer in range(4):
+        rows, hit = buf.dsv4kv_kvbuf_get_with_head(1, pool, ids)
+        hits.append(hit)
+    assert hits == [False, True, True, True] and buf.dequants == 1
+    fresh = B.dsv4kv_dequant_gather(1, pool, ids)
+    assert torch.equal(rows.view(torch.int16), fresh.view(torch.int16))
+    buf.dsv4kv_kvbuf_get(10)                                  # plain get forgets
+    _, hit = buf.dsv4kv_kvbuf_get_with_head(1, pool, ids)
+    assert not hit and buf.dequants == 2
+
+
+def test_cuda_graph_replay_with_offsets_refreshed_in_place(B):
+    cfg = W.cfg2_ratio2_small()
+    rb = 528
+    rows = dev_bf16(cfg["rows"])
+    ext = dev(cfg["ext"])
+    pt = dev(cfg["page_table"])
+    w = dev_bf16(cfg["norm_w"])
+    fr = dev(cfg["freqs"])
+    pool = torch.zeros(cfg["pool_rows"] * rb, dtype=torch.uint8, device="cuda")
+    ids = dev(np.arange(64, 64 + 512, dtype=np.int32))
+    out = torch.empty((512, 512), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        B.dsv4kv_compress_store(1, 2, rows, ext, pool, page_table=pt, page_bits=6, rmsnorm_w=w,
+                                freqs_cis=fr, n_out=2048)       # warm-up outside capture
+        B.dsv4kv_dequant_gather(1, pool, ids, out)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        B.dsv4kv_compress_store(1, 2, rows, ext, pool, page_table=pt, page_bits=6, rmsnorm_w=w,
+                                freqs_cis=fr, n_out=2048)
+        B.dsv4kv_dequant_gather(1, pool, ids, out)
+    for lens in ([37, 512, 1024, 2047], [100, 0, 900, 13], [0, 0, 0, 3000]):
+        new_ext = W._ext(lens, n_slots=8, pad_first=sum(lens))
+        ext.copy_(dev(new_ext))                                 # refreshed in place
+        pool.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        c = dict(cfg, ext=new_ext)
+        ref_pool = gpu_store(B, c)["pool"]
+        assert np.array_equal(pool.cpu().numpy(), ref_pool)
+        want = B.dsv4kv_dequant_gather(1, dev(ref_pool), ids)
+        assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+
+
+def test_determinism_and_negative_control(B):
+    cfg = W.cfg2_ratio2_small()
+    h = []
+    for eps in (1e-6, 1e-6, 1e-6 * (1 + 1e-3)):
+        g = gpu_store(B, dict(cfg, eps=eps))
+        m = hashlib.sha256()
+        m.update(g["pool"].tobytes())
+        m.update(g["pre"].tobytes())
+        m.update(g["lat"].tobytes())
+        h.append(m.hexdigest())
+    assert h[0] == h[1]
+    assert h[2] != h[0]

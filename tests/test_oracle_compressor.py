@@ -210,3 +210,17 @@ def test_topk_to_slots_oracle():
     slots, lens, _ = oracle.topk_to_slots(topk, np.array([0, 1], np.int32), pt, 2,
                                           is_valid=np.array([1, 0], np.uint8))
     assert lens.tolist() == [4, 0] and (slots[1] == -1).all()
+
+
+def test_row_subset_mode_equals_the_full_run():
+    rows, ext, w, freqs = _small_case(13, 2, [40, 17, 0, 66])
+    full = oracle.compress_store(oracle.V41, 2, rows, ext, norm_w=w, freqs=freqs,
+                                 out_loc=np.zeros(70, np.int32))
+    which = np.array([69, 0, 5, 33, 60, 61], np.int64)        # 60.. are padding
+    sub = oracle.compress_store(oracle.V41, 2, rows, ext, norm_w=w, freqs=freqs,
+                                out_loc=np.zeros(70, np.int32), which=which)
+    for key in ("prequant_f64", "prequant_f32", "latent"):
+        assert np.array_equal(sub[key], full[key][which])
+    with pytest.raises(ValueError):
+        oracle.compress_store(oracle.V41, 2, rows, ext, out_loc=np.zeros(70, np.int32),
+                              which=np.array([70]))
