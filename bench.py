@@ -1,0 +1,372 @@
+"""Benchmark of the compressed-KV write/read hot path on GB300.
+
+One step = one long-prefill batch through the whole path:
+  1. dsv4kv_compress_store: 64 requests (~262k tokens, lognormal lengths),
+     ratio-2 softmax pair pooling of the fused | kv | score | rows, RMSNorm,
+     RoPE, V41 quantization, paged store (page size 64);
+  2. dsv4kv_topk_to_slots: each request's top-2048 compressed ids -> slots;
+  3. the sparse-prefill read: 4 layers share the source; the first
+     get_with_head runs dsv4kv_dequant_gather, the other three are reuse hits.
+value = (rows stored + rows gathered) / step time, inputs resident in HBM.
+e2e   = the same through host buffers: pinned host -> device copy of the
+        step's inputs and device -> host copy of the gathered rows inside the
+        timed region.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path); rank 0 prints one JSON line.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "compressed-KV rows/s (store, gather-dequant) and achieved HBM GB/s vs 8 TB/s"
+LAYERS = 4
+# algorithmic bytes per unit (what the method must move)
+STORE_BYTES_PER_ROW = 2 * (1024 + 1024) + 256 + 528   # 2 x (kv + score) bf16, RoPE row, V41 row
+GATHER_BYTES_PER_ROW = 528 + 4 + 1024                  # V41 row + id, bf16 row out
+TOPK_BYTES_PER_ENTRY = 4 + 4                           # id in, slot out
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_inputs(seed=7):
+    from deepseek_v4_compressed_c2_gb300 import workloads as W
+    return W.cfg5_long_prefill(seed=seed)
+
+
+def cpu_baseline(cfg, budget_s=10.0):
+    """The oracle as it stands, single-threaded, on a bounded sample of the
+    same workload: the first rows of the batch through the compressor
+    (end-to-end mode, with the store) and as many gathered rows."""
+    import oracle
+    n = cfg["n_out"]
+    pool = np.zeros(cfg["pool_rows"] * 528, np.uint8)
+
+    def run(m):
+        which = np.arange(m, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.compress_store(1, 2, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
+                              page_bits=cfg["page_bits"], norm_w=cfg["norm_w"], eps=cfg["eps"],
+                              freqs=cfg["freqs"], n_out=n, which=which, pool=pool,
+                              pool_rows=cfg["pool_rows"], want_f64=False, want_f32=False,
+                              want_latent=False)
+        ids = np.arange(64, 64 + m, dtype=np.int32)
+        oracle.dequant_gather(1, pool, cfg["pool_rows"], ids)
+        return time.perf_counter() - t0
+
+    probe = min(256, n)
+    t = run(probe)
+    m = int(min(n, max(probe, probe * budget_s / max(t, 1e-6))))
+    t = run(m)
+    return {"value": 2 * m / t, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {m} of {n} compressed rows of the batch (ratio-2 compress, "
+                      f"RMSNorm, RoPE, V41 store) + {m} gathered rows, {t:.1f} s"}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    cfg = make_inputs()
+    steps = []
+    for _ in range(args.warmup):
+        cpu_baseline(cfg, budget_s=1.0)
+    for _ in range(args.steps):
+        steps.append(cpu_baseline(cfg, budget_s=max(1.0, 60.0 / max(args.steps, 1))))
+    v = statistics.median(s["value"] for s in steps)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg["name"], "sample": steps[-1]["sample"]},
+            "cpu_baseline": dict(steps[-1], value=v),
+            "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    from deepseek_v4_compressed_c2_gb300 import binding as B
+    B.lib()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = make_inputs()
+
+    def to_dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    rows = to_dev_bf16(cfg["rows"])
+    ext = torch.from_numpy(cfg["ext"]).to(dev)
+    pt = torch.from_numpy(cfg["page_table"]).to(dev)
+    w = to_dev_bf16(cfg["norm_w"])
+    freqs = torch.from_numpy(cfg["freqs"]).to(dev)
+    topk = torch.from_numpy(cfg["topk"]).to(dev)
+    ttr = torch.from_numpy(cfg["token_to_req"]).to(dev)
+    n_store = cfg["n_out"]
+    n_tok, k = cfg["topk"].shape
+    n_gather = n_tok * k
+    pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device=dev)
+    slots = torch.empty((n_tok, k), dtype=torch.int32, device=dev)
+    lens = torch.empty((n_tok,), dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kvbuf = B.SparsePrefillKVBuffer(torch.empty((n_gather, 512), dtype=torch.bfloat16, device=dev))
+    stream = torch.cuda.Stream(device=dev)
+    launches = [0]
+
+    def prepared(rows_t, ext_t, pt_t, topk_t, ttr_t):
+        """the step's three C-ABI calls, marshalled once"""
+        store = B.prepare_compress_store(1, 2, rows_t, ext_t, pool, page_table=pt_t, page_bits=6,
+                                         rmsnorm_w=w, eps=cfg["eps"], freqs_cis=freqs,
+                                         n_out=n_store, err_word=err, stream=stream)
+        tk = B.prepare_topk_to_slots(topk_t, ttr_t, pt_t, 6, slots, lens, err_word=err,
+                                     stream=stream)
+        gwh = B.prepare_get_with_head(kvbuf, 1, pool, slots.view(-1), err_word=err,
+                                      stream=stream)
+        return store, tk, gwh
+
+    resident = prepared(rows, ext, pt, topk, ttr)
+
+    def step(ev=None, calls=resident):
+        store, tk, gwh = calls
+        if ev is not None:
+            ev[0].record(stream)
+        store()
+        if ev is not None:
+            ev[1].record(stream)
+        tk()
+        if ev is not None:
+            ev[2].record(stream)
+        kvbuf.dsv4kv_kvbuf_begin_forward()
+        hits = [gwh() for _layer in range(LAYERS)]
+        if ev is not None:
+            ev[3].record(stream)
+        assert hits == [False] + [True] * (LAYERS - 1)
+        launches[0] += 3
+        return kvbuf.storage
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    torch.cuda.synchronize(dev)
+    assert int(err.item()) == 0, "device faults during warm-up"
+
+    # ---- device-resident timing
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    launches[0] = 0
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    n_launch = launches[0]
+    elapsed_ms = t0.elapsed_time(t1)
+    store_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    topk_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    gather_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+
+    # ---- end to end through host buffers (pinned host -> device -> host)
+    h_rows = torch.from_numpy(cfg["rows"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_ext = torch.from_numpy(cfg["ext"]).pin_memory()
+    h_pt = torch.from_numpy(cfg["page_table"]).pin_memory()
+    h_topk = torch.from_numpy(cfg["topk"]).pin_memory()
+    h_ttr = torch.from_numpy(cfg["token_to_req"]).pin_memory()
+    h_out = torch.empty((n_gather, 512), dtype=torch.bfloat16).pin_memory()
+    d_rows, d_ext, d_pt, d_topk, d_ttr = (t.clone() for t in (rows, ext, pt, topk, ttr))
+    h2d = sum(t.numel() * t.element_size() for t in (h_rows, h_ext, h_pt, h_topk, h_ttr))
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_steps = max(3, min(args.steps, 30))
+
+    from_host = prepared(d_rows, d_ext, d_pt, d_topk, d_ttr)
+
+    def e2e_step():
+        for d, h in ((d_rows, h_rows), (d_ext, h_ext), (d_pt, h_pt), (d_topk, h_topk), (d_ttr, h_ttr)):
+            d.copy_(h, non_blocking=True)
+        out = step(None, from_host)
+        h_out.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    assert int(err.item()) == 0, "device faults during the timed region"
+
+    # ---- max over ranks
+    vals = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    elapsed_ms, e2e_ms = vals.tolist()
+    if rank != 0:
+        return
+    ms_per_step = elapsed_ms / args.steps
+    units = (n_store + n_gather) * world
+    value = units / (ms_per_step / 1e3)
+    peak, peak_kind = _peaks()
+    store_gbs = STORE_BYTES_PER_ROW * n_store / (store_ms / 1e3) / 1e9
+    gather_gbs = GATHER_BYTES_PER_ROW * n_gather / (gather_ms / 1e3) / 1e9
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            traffic = json.load(f).get("compress_store_long_prefill")
+    except Exception:
+        pass
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": cfg["name"], "requests": len(cfg["lengths"]),
+                   "tokens": int(sum(cfg["lengths"])), "store_rows": n_store,
+                   "gather_rows": n_gather, "layers_reading_source": LAYERS, "layout": "V41",
+                   "ratio": 2, "page_size": 64, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (fused rows %d MB per step)"
+                         % (cfg["rows"].nbytes // 10 ** 6)},
+        "roofline": {"bound": "hbm", "achieved": store_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": store_gbs / peak, "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "compress_store_kernel<V41, ratio 2, norm, rope>",
+                     "bytes_per_row": STORE_BYTES_PER_ROW, "frac_of_8000": store_gbs / 8000.0},
+        "kernels": {
+            "compress_store": {"ms": store_ms, "rows_per_s": n_store / (store_ms / 1e3),
+                               "gbs": store_gbs},
+            "topk_to_slots": {"ms": topk_ms,
+                              "gbs": TOPK_BYTES_PER_ENTRY * n_gather / (topk_ms / 1e3) / 1e9},
+            "dequant_gather_x1_plus_3_hits": {"ms": gather_ms,
+                                              "rows_per_s": n_gather / (gather_ms / 1e3),
+                                              "gbs": gather_gbs}},
+        "e2e": {"value": units / (e2e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": n_launch,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -268,3 +268,95 @@ class SparsePrefillKVBuffer:
         if not hit.value and n > 0:
             self.dequants += 1
         return self.storage[:n], bool(hit.value)
+
+
+class PreparedCall:
+    """A C-ABI call whose arguments were marshalled once (tensor pointers,
+    sizes, stream); calling it issues the launch again with the same
+    arguments.  For loops that relaunch the same step (a prefill loop without
+    a CUDA graph): per call the host cost is one ctypes call, and the C side
+    still checks every argument."""
+
+    def __init__(self, name, args, keep):
+        self._fn = getattr(lib(), name)
+        self._name = name
+        self._args = args
+        self._keep = keep            # tensors whose pointers are baked in
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != 0:
+            raise DSV4KVError(self._name, st, lib())
+
+
+def prepare_compress_store(layout, ratio, rows, extend_offsets, pool, *, score=None,
+                           page_table=None, page_bits=0, rmsnorm_w=None, eps=1e-6,
+                           freqs_cis=None, out_loc=None, n_out=None, pool_rows=None,
+                           latent_out=None, prequant_out=None, err_word=None, stream=None):
+    """dsv4kv_compress_store with its arguments marshalled once."""
+    if n_out is None:
+        n_out = out_loc.numel()
+    if pool_rows is None:
+        pool_rows = pool.numel() * pool.element_size() // _ROW_BYTES.get(layout, 1)
+    args = (layout, ratio, _ptr(rows), rows.shape[0], rows.stride(0), _ptr(score),
+            0 if score is None else score.stride(0), _ptr(extend_offsets),
+            extend_offsets.shape[1], _ptr(page_table),
+            0 if page_table is None else page_table.shape[1], page_bits, _ptr(rmsnorm_w), eps,
+            _ptr(freqs_cis), 0 if freqs_cis is None else freqs_cis.shape[0], _ptr(out_loc),
+            n_out, _ptr(pool), pool_rows, _ptr(latent_out), _ptr(prequant_out), _ptr(err_word),
+            _stream(stream))
+    # one checked call validates shapes through the same path as the plain binding
+    dsv4kv_compress_store(layout, ratio, rows, extend_offsets, pool, score=score,
+                          page_table=page_table, page_bits=page_bits, rmsnorm_w=rmsnorm_w,
+                          eps=eps, freqs_cis=freqs_cis, out_loc=out_loc, n_out=n_out,
+                          pool_rows=pool_rows, latent_out=latent_out, prequant_out=prequant_out,
+                          err_word=err_word, stream=stream)
+    return PreparedCall("dsv4kv_compress_store", args,
+                        (rows, extend_offsets, pool, score, page_table, rmsnorm_w, freqs_cis,
+                         out_loc, latent_out, prequant_out, err_word))
+
+
+def prepare_topk_to_slots(topk, token_to_req, page_table, page_bits, slots, lens, *,
+                          is_valid=None, err_word=None, stream=None):
+    dsv4kv_topk_to_slots(topk, token_to_req, page_table, page_bits, is_valid=is_valid,
+                         slots=slots, lens=lens, err_word=err_word, stream=stream)
+    n_tok, k = topk.shape
+    args = (_ptr(topk), n_tok, k, _ptr(token_to_req), _ptr(is_valid), _ptr(page_table),
+            page_table.shape[0], page_table.shape[1], page_bits, _ptr(slots), _ptr(lens),
+            _ptr(err_word), _stream(stream))
+    return PreparedCall("dsv4kv_topk_to_slots", args,
+                        (topk, token_to_req, page_table, slots, lens, is_valid, err_word))
+
+
+def prepare_dequant_gather(layout, pool, ids, out, *, pool_rows=None, err_word=None, stream=None):
+    dsv4kv_dequant_gather(layout, pool, ids, out, pool_rows=pool_rows, err_word=err_word,
+                          stream=stream)
+    if pool_rows is None:
+        pool_rows = pool.numel() * pool.element_size() // _ROW_BYTES.get(layout, 1)
+    args = (layout, _ptr(pool), pool_rows, _ptr(ids), ids.numel(), _ptr(out), _ptr(err_word),
+            _stream(stream))
+    return PreparedCall("dsv4kv_dequant_gather", args, (pool, ids, out, err_word))
+
+
+def prepare_get_with_head(kvbuf, layout, pool, ids, *, pool_rows=None, err_word=None,
+                          stream=None):
+    """SparsePrefillKVBuffer.get_with_head with its arguments marshalled once;
+    the returned callable gives the hit flag."""
+    if pool_rows is None:
+        pool_rows = pool.numel() * pool.element_size() // _ROW_BYTES.get(layout, 1)
+    hit = ctypes.c_int(0)
+    rows = ctypes.c_void_p()
+    fn = lib().dsv4kv_kvbuf_get_with_head
+    args = (ctypes.byref(kvbuf.buf), layout, _ptr(pool), pool_rows, _ptr(ids), ids.numel(),
+            ctypes.byref(rows), ctypes.byref(hit), _ptr(err_word), _stream(stream))
+    keep = (pool, ids, err_word, kvbuf)
+
+    def call():
+        st = fn(*args)
+        if st != 0:
+            raise DSV4KVError("dsv4kv_kvbuf_get_with_head", st, lib())
+        if not hit.value and ids.numel() > 0:
+            kvbuf.dequants += 1
+        return bool(hit.value)
+    call.keep = keep
+    return call

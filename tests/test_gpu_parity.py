@@ -207,7 +207,8 @@ def test_every_layout_ratio_norm_rope_combination(B):
 # ------------------------------------------------------------ edge cases
 def test_empty_and_all_padding_calls(B):
     cfg = W.cfg1_v41_roundtrip()
-    cfg0 = dict(cfg, ext=np.zeros((2, 3), np.int32), n_out=50)
+    cfg0 = dict(cfg, ext=np.zeros((2, 3), np.int32), n_out=50,
+                page_table=np.ones((3, 4), np.int32))
     g = gpu_store(B, cfg0, pool_fill=0x33)
     assert (g["pool"] == 0x33).all() and not g["pre"].any() and g["err"] == 0
     cfg_none = dict(cfg, ext=np.zeros((2, 0), np.int32), n_out=8)
