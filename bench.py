@@ -39,6 +39,33 @@ GATHER_BYTES_PER_ROW = 528 + 4 + 1024                  # V41 row + id, bf16 row 
 TOPK_BYTES_PER_ENTRY = 4 + 4                           # id in, slot out
 
 
+_CSRC = os.path.join("deepseek_v4_compressed_c2_gb300", "csrc")
+STORE_SOURCES = [os.path.join(_CSRC, f) for f in
+                 ("compress_store.cu", "quant.cuh", "tma.cuh", "layout.cuh", "internal.cuh")]
+
+
+def _profiled_traffic(name, sources):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's sources changed since that capture (hash mismatch)."""
+    import hashlib
+    try:
+        h = hashlib.sha256()
+        for f in sources:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        fields = {}
+        with open(os.path.join(ROOT, "profiles", name + ".md")) as fh:
+            for line in fh:
+                if ":" in line and not line.startswith("|"):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip().split()[0] if v.strip() else ""
+        if fields.get("source_sha256") != h.hexdigest()[:16]:
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -155,6 +182,48 @@ def run_reference(args, rank):
             "cpu_baseline": dict(steps[-1], value=v),
             "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def cold_gather(B, dev, stream, reps):
+    """dsv4kv_dequant_gather timed alone with a cold L2: pool of 1,048,576 V41
+    rows (page 0 reserved) filled by the store kernel from bf16 N(0,1)
+    latents (torch generator, seed 4), ids = 262,144 unique rows (numpy
+    seed 4), a 512 MB buffer written between launches."""
+    import torch
+    pool_rows, n_ids = 1 << 20, 1 << 18
+    g = torch.Generator(device=dev)
+    g.manual_seed(4)
+    lat = torch.randn((pool_rows - 64, 512), generator=g, device=dev).to(torch.bfloat16)
+    ext = torch.tensor([[0], [pool_rows - 64]], dtype=torch.int32, device=dev)
+    pt = torch.arange(1, pool_rows // 64, dtype=torch.int32, device=dev).view(1, -1)
+    pool = torch.zeros(pool_rows * 528, dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.dsv4kv_compress_store(1, 1, lat, ext, pool, page_table=pt, page_bits=6,
+                            n_out=pool_rows - 64, err_word=err, stream=stream)
+    del lat
+    rng = np.random.default_rng(4)
+    ids = torch.from_numpy((rng.choice(pool_rows - 64, n_ids, replace=False) + 64)
+                           .astype(np.int32)).to(dev)
+    out = torch.empty((n_ids, 512), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    call = B.prepare_dequant_gather(1, pool, ids, out, err_word=err, stream=stream)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(reps + 3):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            times.append((a, b))
+    torch.cuda.synchronize(dev)
+    assert int(err.item()) == 0
+    ms = statistics.median(a.elapsed_time(b) for a, b in times[3:])
+    gbs = GATHER_BYTES_PER_ROW * n_ids / (ms / 1e3) / 1e9
+    peak, kind = _peaks()
+    return {"workload": "gather_v41_262144_of_1048576_cold_l2", "ms": ms,
+            "rows_per_s": n_ids / (ms / 1e3), "gbs": gbs, "frac": gbs / peak,
+            "frac_of_8000": gbs / 8000.0, "peak_kind": kind, "bytes_per_row": GATHER_BYTES_PER_ROW}
 
 
 def run_ours(args, rank, world):
@@ -289,6 +358,12 @@ def run_ours(args, rank, world):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     assert int(err.item()) == 0, "device faults during the timed region"
 
+    # ---- the gather alone on a cold L2: a 1 Mi-row V41 pool (553 MB), 262,144
+    # unique random ids, L2 flushed (a 512 MB write) before every launch
+    cold = None
+    if not args.no_cold_gather:
+        cold = cold_gather(B, dev, stream, max(5, min(args.steps, 50)))
+
     # ---- max over ranks
     vals = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -302,12 +377,7 @@ def run_ours(args, rank, world):
     peak, peak_kind = _peaks()
     store_gbs = STORE_BYTES_PER_ROW * n_store / (store_ms / 1e3) / 1e9
     gather_gbs = GATHER_BYTES_PER_ROW * n_gather / (gather_ms / 1e3) / 1e9
-    traffic = None
-    try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            traffic = json.load(f).get("compress_store_long_prefill")
-    except Exception:
-        pass
+    traffic = _profiled_traffic("compress_store_long_prefill", STORE_SOURCES)
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -331,6 +401,7 @@ def run_ours(args, rank, world):
             "dequant_gather_x1_plus_3_hits": {"ms": gather_ms,
                                               "rows_per_s": n_gather / (gather_ms / 1e3),
                                               "gbs": gather_gbs}},
+        "gather_cold_l2": cold,
         "e2e": {"value": units / (e2e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": n_launch,
@@ -344,10 +415,11 @@ def run_ours(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cold-gather", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

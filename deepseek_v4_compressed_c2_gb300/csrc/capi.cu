@@ -13,6 +13,8 @@
 
 namespace dsv4kv {
 
+static_assert(kMaxSlots == DSV4KV_MAX_SLOTS, "plan capacity matches the header");
+
 static thread_local int g_last_cuda_error = 0;
 
 static int cuda_status(cudaError_t e) {
@@ -93,7 +95,7 @@ int dsv4kv_compress_store(int layout, int ratio, const void* rows, long long n_r
   if (n_slots > DSV4KV_MAX_SLOTS || pool_rows > DSV4KV_MAX_POOL_ROWS) return DSV4KV_ERANGE;
   if (!(eps >= 0.f)) return DSV4KV_EINVAL;
   if (n_out == 0) return DSV4KV_OK;
-  if (!rows || !extend_offsets || !pool || pool_rows < 1) return DSV4KV_EINVAL;
+  if (!rows || (n_slots > 0 && !extend_offsets) || !pool || pool_rows < 1) return DSV4KV_EINVAL;
   if (!aligned16(rows) || !aligned16(pool) || (row_stride % 8) != 0) return DSV4KV_EINVAL;
   if (row_stride < DSV4KV_DIM || (ratio == 2 && !score && row_stride < 2 * DSV4KV_DIM))
     return DSV4KV_EINVAL;

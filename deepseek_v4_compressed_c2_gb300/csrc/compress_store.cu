@@ -1,32 +1,66 @@
 // Fused compressor: (ratio-2 pair pooling) -> RMSNorm -> RoPE -> store_row
-// -> paged write, one warp per output row, in one launch.
+// -> paged write, in one launch.
 //
 // sglang PR #39652 "dsv4.1: compression, KV I/O, and metadata kernels",
 // Summary (c1/c2 bullet): the ratio-1 / ratio-2 compressors do pair-pooling
 // (ratio 2), RMSNorm, RoPE and the main-KV write in one launch, returning the
 // pre-RoPE latent; out_loc == 0 marks a padded graph row.  The review's
-// cleanup of the c2 kernel issues the RoPE frequency load before the softmax
-// and the RMSNorm reduction so its latency overlaps them; this kernel does
-// the same.
+// cleanup of the c2 kernel issues the RoPE frequency load early so its
+// latency overlaps the softmax and the RMSNorm reduction; here the
+// frequencies arrive with the row's inputs.
 // sglang PR #46230: the launch reads low_ratio_extend_offsets (int32 [2,
 // request slots]: first row, row count) on the device, so it can sit inside
 // a CUDA graph whose offsets are refreshed in place; ratio-2 input is the
 // fused | kv | score | projection.
 //
-// Work decomposition.  Each CTA first turns the per-slot row counts into an
-// exclusive prefix (shared memory), then its warps walk output rows k in a
-// grid-stride loop: binary search k -> request slot r, row j = k - base[r].
-// Lane l holds dims [16l, 16l+16) of the row in registers; every global
-// access is a 16-byte vector access, and a warp instruction touches 512
-// contiguous bytes.  All loads of a row (kv, score, RoPE frequencies) are
-// issued before any arithmetic.
+// Design (persistent, warp-specialised, two CTAs per SM):
+//  * every CTA turns the per-slot row counts into an exclusive prefix in
+//    shared memory (the plan), then walks tiles of kRows consecutive output
+//    rows, tile = blockIdx.x + i * gridDim.x;
+//  * one producer warp: one lane per row of the tile finds the row's request
+//    (binary search over the prefix), writes a 16-byte descriptor (state,
+//    position, destination slot) and issues cp.async.bulk copies of the row's
+//    source rows (one 4 KB copy for a ratio-2 pair in the fused layout) and
+//    of its RoPE row into a 3-stage shared-memory ring; an mbarrier per stage
+//    counts the bytes in flight;
+//  * eight consumer warps, each owning one row (ratio 2) or two (ratio 1) of
+//    the stage: wait for the stage, pull the row into registers, release the
+//    slot, then pool, normalise, rotate, quantize and store it.  Lane l holds
+//    dims 8l..8l+7 and 256+8l..263+8l, so every shared-memory read is
+//    conflict-free and every global store of a row half is one contiguous
+//    warp access.
+//  All waits are bounded (see tma.cuh).
 #include "internal.cuh"
 #include "quant.cuh"
+#include "tma.cuh"
 
 namespace dsv4kv {
 
-constexpr int kStoreWarps = 8;
-constexpr int kStoreThreads = kStoreWarps * 32;
+constexpr int kConsumerWarps = 8;
+constexpr int kStages = 3;
+constexpr int kStoreThreads = (kConsumerWarps + 1) * 32;
+
+enum RowState : int { kRowNone = 0, kRowPad = 1, kRowBad = 2, kRowOk = 3 };
+
+struct __align__(16) RowDesc {
+  int state;
+  int pos;
+  long long slot;
+};
+
+template <int RATIO, bool ROPE>
+struct StoreTile {
+  static constexpr int kRowsPerWarp = RATIO == 2 ? 1 : 2;
+  static constexpr int kRows = kConsumerWarps * kRowsPerWarp;      // rows per stage
+  static constexpr int kInBytes = RATIO == 2 ? 4096 : 1024;        // kv0|s0|kv1|s1, or kv
+  static constexpr int kRopeBytes = ROPE ? kRopeDim * 4 : 0;
+  static constexpr int kSlotBytes = kInBytes + kRopeBytes;
+  static constexpr int kStageBytes = kRows * kSlotBytes;
+  static constexpr int kFixedSmem = kStages * kStageBytes + kStages * kRows * (int)sizeof(RowDesc)
+                                  + 2 * kStages * 8 + 16;
+  static_assert(kRows <= 32, "one producer lane per row");
+  static_assert(kSlotBytes % 16 == 0 && kStageBytes % 128 == 0, "bulk-copy alignment");
+};
 
 // base[i] = sum_{r < i} max(count_r, 0) / RATIO for i in [0, n_slots]
 template <int RATIO>
@@ -64,8 +98,60 @@ __device__ void block_scan_counts(const int* __restrict__ ext, int n_slots, long
   if (tid == nt - 1) base[n_slots] = excl;
 }
 
+// The plan for output row k: request slot r (last slot whose prefix <= k),
+// j = k - base[r], sources first_r + RATIO*j (+1), position RATIO*j, and the
+// destination slot (out_loc, or the page table; -1 when the page index is
+// past the table).
+template <int RATIO, bool ROPE>
+__device__ __forceinline__ RowDesc plan_row(const StoreParams& p, long long k, long long total,
+                                            const long long* s_base, const int* s_first,
+                                            long long& src) {
+  RowDesc d;
+  d.state = kRowNone; d.pos = 0; d.slot = 0;
+  src = 0;
+  if (k >= p.n_out) return d;
+  if (k >= total) { d.state = kRowPad; return d; }
+  int lo = 0, hi = p.n_slots - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_base[mid] <= k) lo = mid; else hi = mid - 1;
+  }
+  const long long j = k - s_base[lo];
+  src = (long long)s_first[lo] + (long long)RATIO * j;
+  const long long pos = (long long)RATIO * j;
+  d.pos = (int)pos;
+  const bool ok = src >= 0 && src + RATIO <= p.n_rows && (!ROPE || pos < p.max_pos);
+  if (!ok) { d.state = kRowBad; return d; }
+  if (p.out_loc) {
+    d.slot = p.out_loc[k];
+  } else {
+    const long long lp = j >> p.page_bits;
+    d.slot = lp < p.max_pages
+                 ? ((long long)p.page_table[(long long)lo * p.max_pages + lp] << p.page_bits)
+                       | (j & ((1LL << p.page_bits) - 1))
+                 : -1;
+  }
+  d.state = kRowOk;
+  return d;
+}
+
+__device__ __forceinline__ void zero_row_outputs(const StoreParams& p, long long k, int lane) {
+  if (p.latent_out) {
+    uint4* d = reinterpret_cast<uint4*>(p.latent_out + k * kDim);
+    d[lane] = make_uint4(0, 0, 0, 0);
+    d[32 + lane] = make_uint4(0, 0, 0, 0);
+  }
+  if (p.prequant_out) {
+    float4* d = reinterpret_cast<float4*>(p.prequant_out + k * kDim);
+    d[2 * lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    d[2 * lane + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    d[64 + 2 * lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    d[64 + 2 * lane + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
 // fast exp2 / reciprocal: relative error ~2^-22, far inside the 1e-5
-// tolerance on the pre-quant row; exact at 0 and for powers of two
+// tolerance on the pre-quant row; exact at 0 and at powers of two
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -77,165 +163,244 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
-__device__ __forceinline__ void zero_row_outputs(const StoreParams& p, long long k, int lane) {
-  if (p.latent_out) {
-    uint4* d = reinterpret_cast<uint4*>(p.latent_out + k * kDim + 16 * lane);
-    d[0] = make_uint4(0, 0, 0, 0);
-    d[1] = make_uint4(0, 0, 0, 0);
+// One row's inputs, pulled out of the stage into registers.
+template <int RATIO, bool ROPE>
+struct RowIn {
+  uint4 kv0[2], kv1[2], s0[2], s1[2];
+  float4 fr[2];
+};
+
+template <int RATIO, bool ROPE>
+__device__ __forceinline__ void load_row(const uint8_t* slot, int lane, RowIn<RATIO, ROPE>& in) {
+  const uint4* b = reinterpret_cast<const uint4*>(slot);   // 64 uint4 per 1 KB block
+  in.kv0[0] = b[lane];
+  in.kv0[1] = b[32 + lane];
+  if constexpr (RATIO == 2) {
+    in.s0[0] = b[64 + lane];
+    in.s0[1] = b[96 + lane];
+    in.kv1[0] = b[128 + lane];
+    in.kv1[1] = b[160 + lane];
+    in.s1[0] = b[192 + lane];
+    in.s1[1] = b[224 + lane];
   }
-  if (p.prequant_out) {
-    float4* d = reinterpret_cast<float4*>(p.prequant_out + k * kDim + 16 * lane);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if constexpr (ROPE) {
+    if (lane >= 24) {
+      const float4* f = reinterpret_cast<const float4*>(slot + StoreTile<RATIO, ROPE>::kInBytes);
+      in.fr[0] = f[2 * (lane - 24)];
+      in.fr[1] = f[2 * (lane - 24) + 1];
+    }
   }
 }
 
 template <int L, int RATIO, bool NORM, bool ROPE>
-__global__ void __launch_bounds__(kStoreThreads)
+__device__ __forceinline__ void process_row(const StoreParams& p, long long k, const RowDesc& d,
+                                            const RowIn<RATIO, ROPE>& in, const float (&w)[16],
+                                            int lane) {
+  if (d.state == kRowNone) return;
+  if (d.state != kRowOk) {
+    if (d.state == kRowBad && lane == 0 && p.err) atomicAdd(p.err, 1);
+    zero_row_outputs(p, k, lane);
+    return;
+  }
+  float x[16];
+  unpack_bf16x8(in.kv0[0], x);
+  unpack_bf16x8(in.kv0[1], x + 8);
+  if constexpr (RATIO == 2) {
+    // softmax over the pair: weight of the first = 1 / (1 + exp(s1 - s0));
+    // x = k1 + (k0 - k1) * w0 (an ex2 overflow gives w0 = 0, i.e. x = k1)
+    float k1[16], a[16], b[16];
+    unpack_bf16x8(in.kv1[0], k1); unpack_bf16x8(in.kv1[1], k1 + 8);
+    unpack_bf16x8(in.s0[0], a);   unpack_bf16x8(in.s0[1], a + 8);
+    unpack_bf16x8(in.s1[0], b);   unpack_bf16x8(in.s1[1], b + 8);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float w0 = rcp_approx(1.f + ex2_approx((b[i] - a[i]) * 1.4426950408889634f));
+      x[i] = fmaf(x[i] - k1[i], w0, k1[i]);
+    }
+  }
+  if constexpr (NORM) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFullMask, ss, o);
+    const float inv = rsqrtf(fmaf(ss, 1.f / kDim, p.eps));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = (x[i] * inv) * w[i];
+  }
+  if (p.latent_out) {  // post-norm, pre-RoPE
+    uint4* o = reinterpret_cast<uint4*>(p.latent_out + k * kDim);
+    o[lane] = pack_bf16x8(x);
+    o[32 + lane] = pack_bf16x8(x + 8);
+  }
+  if constexpr (ROPE) {
+    // lanes 24..31 hold dims 448+8(l-24) .. +7 in x[8..15]: 4 complex pairs
+    if (lane >= 24) {
+      const float f[8] = {in.fr[0].x, in.fr[0].y, in.fr[0].z, in.fr[0].w,
+                          in.fr[1].x, in.fr[1].y, in.fr[1].z, in.fr[1].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float c = f[2 * q], s = f[2 * q + 1];
+        const float a = x[8 + 2 * q], b = x[9 + 2 * q];
+        x[8 + 2 * q] = fmaf(a, c, -b * s);
+        x[9 + 2 * q] = fmaf(a, s, b * c);
+      }
+    }
+  }
+  if (p.prequant_out) {
+    float4* o = reinterpret_cast<float4*>(p.prequant_out + k * kDim);
+    o[2 * lane] = make_float4(x[0], x[1], x[2], x[3]);
+    o[2 * lane + 1] = make_float4(x[4], x[5], x[6], x[7]);
+    o[64 + 2 * lane] = make_float4(x[8], x[9], x[10], x[11]);
+    o[64 + 2 * lane + 1] = make_float4(x[12], x[13], x[14], x[15]);
+  }
+  if (d.slot == 0) return;  // padded graph row: computed, not stored
+  if (d.slot < 0 || d.slot >= p.pool_rows) {
+    if (lane == 0 && p.err) atomicAdd(p.err, 1);
+    return;
+  }
+  const PagedKV<L> kv{p.pool, p.page_bits};
+  store_row_split<L>(x, kv.row(d.slot), lane);
+}
+
+template <int L, int RATIO, bool NORM, bool ROPE>
+__global__ void __launch_bounds__(kStoreThreads, 2)
 compress_store_kernel(const StoreParams p) {
-  extern __shared__ long long s_base[];  // n_slots + 1
+  using TL = StoreTile<RATIO, ROPE>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* s_stage = smem;
+  RowDesc* s_desc = reinterpret_cast<RowDesc*>(smem + kStages * TL::kStageBytes);
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(s_desc + kStages * TL::kRows);
+  uint64_t* s_empty = s_full + kStages;
+  int* s_abort = reinterpret_cast<int*>(s_empty + kStages);
+  long long* s_base = reinterpret_cast<long long*>(smem + TL::kFixedSmem);
+  int* s_first = reinterpret_cast<int*>(s_base + p.n_slots + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], kConsumerWarps);
+    }
+    *s_abort = 0;
+    mbar_fence_init();
+  }
   block_scan_counts<RATIO>(p.ext, p.n_slots, s_base);
+  for (int i = threadIdx.x; i < p.n_slots; i += blockDim.x) s_first[i] = p.ext[i];
   __syncthreads();
   const long long total = s_base[p.n_slots];
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
+  const long long n_tiles = ((long long)p.n_out + TL::kRows - 1) / TL::kRows;
+  volatile int* abort = s_abort;
 
-  float w[16];
-  if constexpr (NORM) {
-    const uint4* wp = reinterpret_cast<const uint4*>(p.norm_w + 16 * lane);
-    unpack_bf16x8(__ldg(wp), w);
-    unpack_bf16x8(__ldg(wp + 1), w + 8);
-  }
-  const __nv_bfloat16* score_base = p.score ? p.score : p.rows + kDim;
-  const long long sstride = p.score ? p.score_stride : p.row_stride;
-  const long long page_mask = (1LL << p.page_bits) - 1;
-
-  for (long long k = (long long)blockIdx.x * kStoreWarps + warp; k < p.n_out;
-       k += (long long)gridDim.x * kStoreWarps) {
-    if (k >= total) {  // padding row: no source, nothing stored
-      zero_row_outputs(p, k, lane);
-      continue;
-    }
-    int lo = 0, hi = p.n_slots - 1;
-    while (lo < hi) {  // last slot whose base <= k (empty slots share a base)
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_base[mid] <= k) lo = mid; else hi = mid - 1;
-    }
-    const int r = lo;
-    const long long j = k - s_base[r];
-    const long long first = p.ext[r];
-    const long long src = first + (long long)RATIO * j;
-    const long long pos = (long long)RATIO * j;
-    bool ok = src >= 0 && src + RATIO <= p.n_rows;
-    if (ROPE) ok = ok && pos < p.max_pos;
-    if (!ok) {
-      if (lane == 0 && p.err) atomicAdd(p.err, 1);
-      zero_row_outputs(p, k, lane);
-      continue;
-    }
-    // destination (independent of the arithmetic; fetched early)
-    long long slot;
-    if (p.out_loc) {
-      slot = p.out_loc[k];
-    } else {
-      const long long lp = j >> p.page_bits;
-      slot = lp < p.max_pages
-                 ? ((long long)p.page_table[(long long)r * p.max_pages + lp] << p.page_bits) | (j & page_mask)
-                 : -1;
-    }
-
-    // ---- loads: everything this row needs, issued together
-    const __nv_bfloat16* kv0 = p.rows + src * p.row_stride + 16 * lane;
-    uint4 a0 = ld_stream_v4(kv0), a1 = ld_stream_v4(kv0 + 8);
-    uint4 b0, b1, c0, c1, d0, d1;
-    if constexpr (RATIO == 2) {
-      const __nv_bfloat16* kv1 = kv0 + p.row_stride;
-      const __nv_bfloat16* s0 = score_base + src * sstride + 16 * lane;
-      const __nv_bfloat16* s1 = s0 + sstride;
-      b0 = ld_stream_v4(kv1); b1 = ld_stream_v4(kv1 + 8);
-      c0 = ld_stream_v4(s0);  c1 = ld_stream_v4(s0 + 8);
-      d0 = ld_stream_v4(s1);  d1 = ld_stream_v4(s1 + 8);
-    }
-    float4 fr[4];
-    if (ROPE && lane >= 28) {
-      const float4* fp = reinterpret_cast<const float4*>(p.freqs + pos * kRopeDim + 16 * (lane - 28));
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = policy_evict_first();
+    const __nv_bfloat16* score_base = p.score ? p.score : p.rows + kDim;
+    const long long sstride = p.score ? p.score_stride : p.row_stride;
+    const bool fused_pair = p.score == nullptr && p.row_stride == 2 * kDim;
+    long long it = 0;
+    for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+      const int s = (int)(it % kStages);
+      const uint32_t use = (uint32_t)(it / kStages);
+      if (use > 0 && !mbar_wait(&s_empty[s], (use - 1) & 1u, abort, p.err)) break;
+      RowDesc d;
+      d.state = kRowNone;
+      long long src = 0;
+      if (lane < TL::kRows) {
+        d = plan_row<RATIO, ROPE>(p, tile * TL::kRows + lane, total, s_base, s_first, src);
+        s_desc[s * TL::kRows + lane] = d;
+      }
+      uint32_t bytes = d.state == kRowOk ? (uint32_t)TL::kSlotBytes : 0u;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) fr[i] = __ldg(fp + i);
-    }
-
-    // ---- pool
-    float x[16];
-    unpack_bf16x8(a0, x);
-    unpack_bf16x8(a1, x + 8);
-    if constexpr (RATIO == 2) {
-      float k1[16], s0[16], s1[16];
-      unpack_bf16x8(b0, k1); unpack_bf16x8(b1, k1 + 8);
-      unpack_bf16x8(c0, s0); unpack_bf16x8(c1, s0 + 8);
-      unpack_bf16x8(d0, s1); unpack_bf16x8(d1, s1 + 8);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        // softmax over the pair: the larger score gets 1/(1+e), the other
-        // e/(1+e), e = exp(-|s0 - s1|)
-        const float d = s0[i] - s1[i];
-        const float e = ex2_approx(-fabsf(d) * 1.4426950408889634f);
-        const float wb = rcp_approx(1.f + e);
-        const float ws = e * wb;
-        x[i] = d >= 0.f ? fmaf(wb, x[i], ws * k1[i]) : fmaf(ws, x[i], wb * k1[i]);
+      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(kFullMask, bytes, o);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&s_full[s], bytes);
+      __syncwarp();
+      if (d.state == kRowOk) {
+        uint8_t* dst = s_stage + s * TL::kStageBytes + lane * TL::kSlotBytes;
+        const __nv_bfloat16* r0 = p.rows + src * p.row_stride;
+        if constexpr (RATIO == 2) {
+          if (fused_pair) {
+            bulk_g2s(dst, r0, 4096, &s_full[s], pol);             // kv0|s0|kv1|s1
+          } else {
+            const __nv_bfloat16* c0 = score_base + src * sstride;
+            bulk_g2s(dst, r0, 1024, &s_full[s], pol);
+            bulk_g2s(dst + 1024, c0, 1024, &s_full[s], pol);
+            bulk_g2s(dst + 2048, r0 + p.row_stride, 1024, &s_full[s], pol);
+            bulk_g2s(dst + 3072, c0 + sstride, 1024, &s_full[s], pol);
+          }
+        } else {
+          bulk_g2s(dst, r0, 1024, &s_full[s], pol);
+        }
+        if constexpr (ROPE)
+          bulk_g2s(dst + TL::kInBytes, p.freqs + (long long)d.pos * kRopeDim, kRopeDim * 4,
+                   &s_full[s], pol);
       }
     }
-    // ---- RMSNorm over all 512 dims
+    // every issued copy has landed before the CTA may exit (bounded)
+    if (lane == 0) {
+      for (int s = 0; s < kStages && s < it; ++s) {
+        const uint32_t last_use = (uint32_t)((it - 1 - s) / kStages);
+        for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(&s_full[s], last_use & 1u); ++i) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    float w[16];
     if constexpr (NORM) {
-      float ss = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFullMask, ss, o);
-      const float inv = rsqrtf(fmaf(ss, 1.f / kDim, p.eps));
-#pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = (x[i] * inv) * w[i];
+      const uint4* wp = reinterpret_cast<const uint4*>(p.norm_w);
+      unpack_bf16x8(__ldg(wp + lane), w);
+      unpack_bf16x8(__ldg(wp + 32 + lane), w + 8);
     }
-    if (p.latent_out) {  // post-norm, pre-RoPE
-      uint4* d = reinterpret_cast<uint4*>(p.latent_out + k * kDim + 16 * lane);
-      d[0] = pack_bf16x8(x);
-      d[1] = pack_bf16x8(x + 8);
-    }
-    // ---- RoPE on dims 448..511: interleaved pairs rotated by (cos, sin)
-    if (ROPE && lane >= 28) {
-      const float* f = reinterpret_cast<const float*>(fr);
+    long long it = 0;
+    for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+      const int s = (int)(it % kStages);
+      const uint32_t use = (uint32_t)(it / kStages);
+      if (!mbar_wait(&s_full[s], use & 1u, abort, p.err)) break;
+      RowDesc d[TL::kRowsPerWarp];
+      RowIn<RATIO, ROPE> in[TL::kRowsPerWarp];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float c = f[2 * i], s = f[2 * i + 1];
-        const float a = x[2 * i], b = x[2 * i + 1];
-        x[2 * i] = fmaf(a, c, -b * s);
-        x[2 * i + 1] = fmaf(a, s, b * c);
+      for (int q = 0; q < TL::kRowsPerWarp; ++q) {
+        const int t = warp * TL::kRowsPerWarp + q;
+        d[q] = s_desc[s * TL::kRows + t];
+        if (d[q].state == kRowOk)
+          load_row<RATIO, ROPE>(s_stage + s * TL::kStageBytes + t * TL::kSlotBytes, lane, in[q]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[s]);
+#pragma unroll
+      for (int q = 0; q < TL::kRowsPerWarp; ++q) {
+        const long long k = tile * TL::kRows + warp * TL::kRowsPerWarp + q;
+        process_row<L, RATIO, NORM, ROPE>(p, k, d[q], in[q], w, lane);
       }
     }
-    if (p.prequant_out) {
-      float4* d = reinterpret_cast<float4*>(p.prequant_out + k * kDim + 16 * lane);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) d[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
-    }
-    // ---- quantize + paged store
-    if (slot == 0) continue;  // padded graph row
-    if (slot < 0 || slot >= p.pool_rows) {
-      if (lane == 0 && p.err) atomicAdd(p.err, 1);
-      continue;
-    }
-    const PagedKV<L> kv{p.pool, p.page_bits};
-    store_row_lane<L>(x, kv.row(slot), lane);
   }
 }
 
 template <int L, int RATIO, bool NORM, bool ROPE>
 static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
+  using TL = StoreTile<RATIO, ROPE>;
   auto kern = compress_store_kernel<L, RATIO, NORM, ROPE>;
-  const size_t smem = sizeof(long long) * (size_t)(p.n_slots + 1);
-  int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStoreThreads, smem);
+  const size_t smem = (size_t)TL::kFixedSmem + sizeof(long long) * (size_t)(p.n_slots + 1)
+                    + sizeof(int) * (size_t)p.n_slots;
+  static int attr_set_for_device[64] = {0};  // the largest size any call can need, once per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const long long want = ((long long)p.n_out + kStoreWarps - 1) / kStoreWarps;
+  if (dev >= 64 || !attr_set_for_device[dev]) {
+    const size_t max_smem = (size_t)TL::kFixedSmem + sizeof(long long) * (kMaxSlots + 1)
+                          + sizeof(int) * kMaxSlots;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set_for_device[dev] = 1;
+  }
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStoreThreads, smem);
+  if (e != cudaSuccess) return e;
+  const long long tiles = ((long long)p.n_out + TL::kRows - 1) / TL::kRows;
   const long long cap = (long long)device_sm_count() * (per_sm > 0 ? per_sm : 1);
-  const int grid = (int)(want < cap ? want : cap);
+  const int grid = (int)(tiles < cap ? tiles : cap);
   kern<<<grid, kStoreThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }

@@ -8,6 +8,9 @@
 
 namespace dsv4kv {
 
+// request slots per compress_store call (the plan lives in shared memory)
+constexpr int kMaxSlots = 4096;
+
 struct StoreParams {
   const __nv_bfloat16* rows;   // [n_rows, row_stride]
   long long n_rows;

@@ -356,7 +356,7 @@ def test_cuda_graph_replay_with_offsets_refreshed_in_place(B):
 def test_determinism_and_negative_control(B):
     cfg = W.cfg2_ratio2_small()
     h = []
-    for eps in (1e-6, 1e-6, 1e-6 * (1 + 1e-3)):
+    for eps in (1e-6, 1e-6, 1e-6 + 1e-3):
         g = gpu_store(B, dict(cfg, eps=eps))
         m = hashlib.sha256()
         m.update(g["pool"].tobytes())
