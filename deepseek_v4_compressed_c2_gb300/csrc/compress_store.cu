@@ -18,14 +18,16 @@
 //    shared memory (the plan), then walks tiles of kRows consecutive output
 //    rows, tile = blockIdx.x + i * gridDim.x;
 //  * one producer warp: one lane per row of the tile finds the row's request
-//    (binary search over the prefix), writes a 16-byte descriptor (state,
-//    position, destination slot) and issues cp.async.bulk copies of the row's
+//    (binary search over the prefix, shared memory only), writes a 16-byte
+//    descriptor (state, position, request, row) and issues cp.async.bulk
+//    copies of the row's
 //    source rows (one 4 KB copy for a ratio-2 pair in the fused layout) and
 //    of its RoPE row into a 3-stage shared-memory ring; an mbarrier per stage
 //    counts the bytes in flight;
 //  * eight consumer warps, each owning one row (ratio 2) or two (ratio 1) of
 //    the stage: wait for the stage, pull the row into registers, release the
-//    slot, then pool, normalise, rotate, quantize and store it.  Lane l holds
+//    slot, look up the destination (out_loc or the page table) and pool,
+//    normalise, rotate, quantize and store the row.  Lane l holds
 //    dims 8l..8l+7 and 256+8l..263+8l, so every shared-memory read is
 //    conflict-free and every global store of a row half is one contiguous
 //    warp access.
@@ -44,8 +46,9 @@ enum RowState : int { kRowNone = 0, kRowPad = 1, kRowBad = 2, kRowOk = 3 };
 
 struct __align__(16) RowDesc {
   int state;
-  int pos;
-  long long slot;
+  int pos;   // RATIO * j
+  int r;     // request slot
+  int j;     // row index inside the request
 };
 
 template <int RATIO, bool ROPE>
@@ -98,16 +101,15 @@ __device__ void block_scan_counts(const int* __restrict__ ext, int n_slots, long
   if (tid == nt - 1) base[n_slots] = excl;
 }
 
-// The plan for output row k: request slot r (last slot whose prefix <= k),
-// j = k - base[r], sources first_r + RATIO*j (+1), position RATIO*j, and the
-// destination slot (out_loc, or the page table; -1 when the page index is
-// past the table).
+// The plan for output row k (shared memory only, no global loads): request
+// slot r (last slot whose prefix <= k), j = k - base[r], sources
+// first_r + RATIO*j (+1), position RATIO*j.
 template <int RATIO, bool ROPE>
 __device__ __forceinline__ RowDesc plan_row(const StoreParams& p, long long k, long long total,
                                             const long long* s_base, const int* s_first,
                                             long long& src) {
   RowDesc d;
-  d.state = kRowNone; d.pos = 0; d.slot = 0;
+  d.state = kRowNone; d.pos = 0; d.r = 0; d.j = 0;
   src = 0;
   if (k >= p.n_out) return d;
   if (k >= total) { d.state = kRowPad; return d; }
@@ -119,20 +121,22 @@ __device__ __forceinline__ RowDesc plan_row(const StoreParams& p, long long k, l
   const long long j = k - s_base[lo];
   src = (long long)s_first[lo] + (long long)RATIO * j;
   const long long pos = (long long)RATIO * j;
+  d.r = lo;
+  d.j = (int)j;
   d.pos = (int)pos;
   const bool ok = src >= 0 && src + RATIO <= p.n_rows && (!ROPE || pos < p.max_pos);
-  if (!ok) { d.state = kRowBad; return d; }
-  if (p.out_loc) {
-    d.slot = p.out_loc[k];
-  } else {
-    const long long lp = j >> p.page_bits;
-    d.slot = lp < p.max_pages
-                 ? ((long long)p.page_table[(long long)lo * p.max_pages + lp] << p.page_bits)
-                       | (j & ((1LL << p.page_bits) - 1))
-                 : -1;
-  }
-  d.state = kRowOk;
+  d.state = ok ? kRowOk : kRowBad;
   return d;
+}
+
+// Destination slot of a planned row: out_loc[k], or the page table (-1 when
+// the page index is past the table).
+__device__ __forceinline__ long long dest_slot(const StoreParams& p, long long k, const RowDesc& d) {
+  if (p.out_loc) return p.out_loc[k];
+  const long long lp = (long long)d.j >> p.page_bits;
+  if (lp >= p.max_pages) return -1;
+  return ((long long)p.page_table[(long long)d.r * p.max_pages + lp] << p.page_bits)
+         | ((long long)d.j & ((1LL << p.page_bits) - 1));
 }
 
 __device__ __forceinline__ void zero_row_outputs(const StoreParams& p, long long k, int lane) {
@@ -194,8 +198,8 @@ __device__ __forceinline__ void load_row(const uint8_t* slot, int lane, RowIn<RA
 
 template <int L, int RATIO, bool NORM, bool ROPE>
 __device__ __forceinline__ void process_row(const StoreParams& p, long long k, const RowDesc& d,
-                                            const RowIn<RATIO, ROPE>& in, const float (&w)[16],
-                                            int lane) {
+                                            long long slot, const RowIn<RATIO, ROPE>& in,
+                                            const float (&w)[16], int lane) {
   if (d.state == kRowNone) return;
   if (d.state != kRowOk) {
     if (d.state == kRowBad && lane == 0 && p.err) atomicAdd(p.err, 1);
@@ -218,20 +222,29 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
       x[i] = fmaf(x[i] - k1[i], w0, k1[i]);
     }
   }
+  // RMSNorm: x_n = (x * w) * inv with inv = rsqrt(mean(x^2) + eps).  The
+  // product by inv is deferred: RoPE rotates x * w, and the V41 quantizer
+  // folds inv into its power-of-two multiplier, which rounds exactly like
+  // quantizing the explicit x_n (see store_row_v41_scaled).
+  float inv = 1.f;
   if constexpr (NORM) {
-    float ss = 0.f;
+    float ss[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
+    for (int i = 0; i < 16; ++i) ss[i & 3] = fmaf(x[i], x[i], ss[i & 3]);
+    float t = (ss[0] + ss[1]) + (ss[2] + ss[3]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFullMask, ss, o);
-    const float inv = rsqrtf(fmaf(ss, 1.f / kDim, p.eps));
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFullMask, t, o);
+    inv = rsqrtf(fmaf(t, 1.f / kDim, p.eps));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (x[i] * inv) * w[i];
+    for (int i = 0; i < 16; ++i) x[i] *= w[i];
   }
   if (p.latent_out) {  // post-norm, pre-RoPE
+    float xn[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) xn[i] = x[i] * inv;
     uint4* o = reinterpret_cast<uint4*>(p.latent_out + k * kDim);
-    o[lane] = pack_bf16x8(x);
-    o[32 + lane] = pack_bf16x8(x + 8);
+    o[lane] = pack_bf16x8(xn);
+    o[32 + lane] = pack_bf16x8(xn + 8);
   }
   if constexpr (ROPE) {
     // lanes 24..31 hold dims 448+8(l-24) .. +7 in x[8..15]: 4 complex pairs
@@ -247,20 +260,25 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
       }
     }
   }
-  if (p.prequant_out) {
-    float4* o = reinterpret_cast<float4*>(p.prequant_out + k * kDim);
-    o[2 * lane] = make_float4(x[0], x[1], x[2], x[3]);
-    o[2 * lane + 1] = make_float4(x[4], x[5], x[6], x[7]);
-    o[64 + 2 * lane] = make_float4(x[8], x[9], x[10], x[11]);
-    o[64 + 2 * lane + 1] = make_float4(x[12], x[13], x[14], x[15]);
+  const bool store = slot > 0 && slot < p.pool_rows;
+  if (slot != 0 && !store && lane == 0 && p.err) atomicAdd(p.err, 1);   // destination fault
+  if (p.prequant_out || L != kV41 || !NORM) {
+    // explicit pre-quant row (debug output, FP4, or no norm: inv == 1)
+    if constexpr (NORM) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] *= inv;
+    }
+    if (p.prequant_out) {
+      float4* o = reinterpret_cast<float4*>(p.prequant_out + k * kDim);
+      o[2 * lane] = make_float4(x[0], x[1], x[2], x[3]);
+      o[2 * lane + 1] = make_float4(x[4], x[5], x[6], x[7]);
+      o[64 + 2 * lane] = make_float4(x[8], x[9], x[10], x[11]);
+      o[64 + 2 * lane + 1] = make_float4(x[12], x[13], x[14], x[15]);
+    }
+    if (store) store_row_split<L>(x, PagedKV<L>{p.pool, p.page_bits}.row(slot), lane);
+  } else if (store) {
+    store_row_v41_scaled(x, inv, PagedKV<kV41>{p.pool, p.page_bits}.row(slot), lane);
   }
-  if (d.slot == 0) return;  // padded graph row: computed, not stored
-  if (d.slot < 0 || d.slot >= p.pool_rows) {
-    if (lane == 0 && p.err) atomicAdd(p.err, 1);
-    return;
-  }
-  const PagedKV<L> kv{p.pool, p.page_bits};
-  store_row_split<L>(x, kv.row(d.slot), lane);
 }
 
 template <int L, int RATIO, bool NORM, bool ROPE>
@@ -360,10 +378,12 @@ compress_store_kernel(const StoreParams p) {
       if (!mbar_wait(&s_full[s], use & 1u, abort, p.err)) break;
       RowDesc d[TL::kRowsPerWarp];
       RowIn<RATIO, ROPE> in[TL::kRowsPerWarp];
+      long long slot[TL::kRowsPerWarp];
 #pragma unroll
       for (int q = 0; q < TL::kRowsPerWarp; ++q) {
         const int t = warp * TL::kRowsPerWarp + q;
         d[q] = s_desc[s * TL::kRows + t];
+        slot[q] = d[q].state == kRowOk ? dest_slot(p, tile * TL::kRows + t, d[q]) : 0;
         if (d[q].state == kRowOk)
           load_row<RATIO, ROPE>(s_stage + s * TL::kStageBytes + t * TL::kSlotBytes, lane, in[q]);
       }
@@ -372,7 +392,7 @@ compress_store_kernel(const StoreParams p) {
 #pragma unroll
       for (int q = 0; q < TL::kRowsPerWarp; ++q) {
         const long long k = tile * TL::kRows + warp * TL::kRowsPerWarp + q;
-        process_row<L, RATIO, NORM, ROPE>(p, k, d[q], in[q], w, lane);
+        process_row<L, RATIO, NORM, ROPE>(p, k, d[q], slot[q], in[q], w, lane);
       }
     }
   }

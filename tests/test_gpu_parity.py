@@ -365,3 +365,14 @@ def test_determinism_and_negative_control(B):
         h.append(m.hexdigest())
     assert h[0] == h[1]
     assert h[2] != h[0]
+
+
+@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4])
+def test_pool_bytes_do_not_depend_on_the_debug_outputs(B, layout):
+    """With RMSNorm the V41 store folds the norm scale into its power-of-two
+    multiplier when no pre-quant output is requested; the bytes must equal
+    those of the explicit path that writes prequant_out."""
+    cfg = dict(W.cfg2_ratio2_small(), layout=layout)
+    with_dbg = gpu_store(B, cfg, want_pre=True, want_lat=True)
+    without = gpu_store(B, cfg, want_pre=False, want_lat=False)
+    assert np.array_equal(with_dbg["pool"], without["pool"])
