@@ -135,6 +135,23 @@ def make_inputs(seed=7):
     return W.cfg5_long_prefill(seed=seed)
 
 
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise max of per-rank floats over the process group (the bench
+    reports the slowest rank's time); identity when world == 1."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_rank, world, slowest_ms):
+    """Weak scaling: every rank processes its own batch of `units_per_rank`;
+    the job's rate is all units over the slowest rank's time."""
+    return units_per_rank * world / (slowest_ms / 1e3)
+
+
 def cpu_baseline(cfg, budget_s=10.0):
     """The oracle as it stands, single-threaded, on a bounded sample of the
     same workload: the first rows of the batch through the compressor
@@ -365,15 +382,11 @@ def run_ours(args, rank, world):
         cold = cold_gather(B, dev, stream, max(5, min(args.steps, 50)))
 
     # ---- max over ranks
-    vals = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_ms = vals.tolist()
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
     if rank != 0:
         return
     ms_per_step = elapsed_ms / args.steps
-    units = (n_store + n_gather) * world
-    value = units / (ms_per_step / 1e3)
+    value = whole_job_rate(n_store + n_gather, world, ms_per_step)
     peak, peak_kind = _peaks()
     store_gbs = STORE_BYTES_PER_ROW * n_store / (store_ms / 1e3) / 1e9
     gather_gbs = GATHER_BYTES_PER_ROW * n_gather / (gather_ms / 1e3) / 1e9
@@ -402,7 +415,8 @@ def run_ours(args, rank, world):
                                               "rows_per_s": n_gather / (gather_ms / 1e3),
                                               "gbs": gather_gbs}},
         "gather_cold_l2": cold,
-        "e2e": {"value": units / (e2e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rate(n_store + n_gather, world, e2e_ms), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": n_launch,
         "clocks": clk,

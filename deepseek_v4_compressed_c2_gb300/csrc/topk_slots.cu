@@ -7,14 +7,27 @@
 // block_size // compress_ratio states (here 2^page_bits rows); empty entries
 // become -1; CUDA-graph padding rows (is_valid_token == 0) attend nothing.
 //
-// One CTA per token row; threads stride over the k entries (coalesced int32
-// reads and writes), then a block reduction produces the row's count.
 #include "internal.cuh"
 
 namespace dsv4kv {
 
-constexpr int kTopkThreads = 256;
+constexpr int kTopkThreads = 512;
 
+__device__ __forceinline__ int topk_slot(int id, bool tok_ok, int r, const int* __restrict__ page_table,
+                                         int max_pages, int page_bits, unsigned mask, int* err) {
+  if (!tok_ok || id < 0) return -1;
+  const int lp = id >> page_bits;
+  if (lp >= max_pages) {
+    if (err) atomicAdd(err, 1);
+    return -1;
+  }
+  const unsigned phys = (unsigned)page_table[(long long)r * max_pages + lp];
+  return (int)((phys << page_bits) | ((unsigned)id & mask));
+}
+
+// One CTA per token row; each thread maps 4 consecutive entries with 16-byte
+// loads and stores when the rows are 16-byte aligned (k % 4 == 0 and aligned
+// base pointers), so a row of 2048 ids is one pass.
 __global__ void __launch_bounds__(kTopkThreads)
 topk_to_slots_kernel(const int* __restrict__ topk, int n_tok, int k,
                      const int* __restrict__ token_to_req, const unsigned char* __restrict__ is_valid,
@@ -22,6 +35,7 @@ topk_to_slots_kernel(const int* __restrict__ topk, int n_tok, int k,
                      int* __restrict__ slots, int* __restrict__ lens, int* err) {
   __shared__ int s_cnt[kTopkThreads / 32];
   const unsigned mask = (1u << page_bits) - 1u;
+  const bool vec = (k & 3) == 0 && ((reinterpret_cast<uintptr_t>(topk) | reinterpret_cast<uintptr_t>(slots)) & 15) == 0;
   for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
     const int r = token_to_req[t];
     const bool bad_req = r < 0 || r >= n_req;
@@ -29,20 +43,25 @@ topk_to_slots_kernel(const int* __restrict__ topk, int n_tok, int k,
     if (bad_req && threadIdx.x == 0 && err) atomicAdd(err, 1);
     int cnt = 0;
     const long long rowoff = (long long)t * k;
-    for (int c = threadIdx.x; c < k; c += blockDim.x) {
-      const int id = topk[rowoff + c];
-      int s = -1;
-      if (tok_ok && id >= 0) {
-        const int lp = id >> page_bits;
-        if (lp < max_pages) {
-          const unsigned phys = (unsigned)page_table[(long long)r * max_pages + lp];
-          s = (int)((phys << page_bits) | ((unsigned)id & mask));
-        } else if (err) {
-          atomicAdd(err, 1);
-        }
+    if (vec) {
+      const int4* in4 = reinterpret_cast<const int4*>(topk + rowoff);
+      int4* out4 = reinterpret_cast<int4*>(slots + rowoff);
+      for (int c = threadIdx.x; c < (k >> 2); c += blockDim.x) {
+        const int4 id = __ldg(in4 + c);
+        int4 sl;
+        sl.x = topk_slot(id.x, tok_ok, r, page_table, max_pages, page_bits, mask, err);
+        sl.y = topk_slot(id.y, tok_ok, r, page_table, max_pages, page_bits, mask, err);
+        sl.z = topk_slot(id.z, tok_ok, r, page_table, max_pages, page_bits, mask, err);
+        sl.w = topk_slot(id.w, tok_ok, r, page_table, max_pages, page_bits, mask, err);
+        out4[c] = sl;
+        cnt += (sl.x >= 0) + (sl.y >= 0) + (sl.z >= 0) + (sl.w >= 0);
       }
-      slots[rowoff + c] = s;
-      cnt += s >= 0;
+    } else {
+      for (int c = threadIdx.x; c < k; c += blockDim.x) {
+        const int sl = topk_slot(topk[rowoff + c], tok_ok, r, page_table, max_pages, page_bits, mask, err);
+        slots[rowoff + c] = sl;
+        cnt += sl >= 0;
+      }
     }
     if (lens) {
 #pragma unroll

@@ -279,9 +279,10 @@ def test_dequant_of_arbitrary_bytes(B, layout):
     assert_bf16_equal_nan_aware(out, want)
 
 
-def test_topk_to_slots_matches_oracle(B):
-    rng = np.random.default_rng(8)
-    n_req, k, page_bits = 9, 333, 4
+@pytest.mark.parametrize("k,offset", [(333, 0), (332, 0), (332, 1), (2048, 0)])
+def test_topk_to_slots_matches_oracle(B, k, offset):
+    rng = np.random.default_rng(8 + k + offset)
+    n_req, page_bits = 9, 4
     pt = rng.integers(1, 5000, (n_req, 40), dtype=np.int32)
     topk = rng.integers(-2, 40 << page_bits, (50, k), dtype=np.int32)
     topk[3, 5] = 45 << page_bits                              # past max_pages
@@ -289,8 +290,11 @@ def test_topk_to_slots_matches_oracle(B):
     ttr[7] = n_req + 3                                         # bad request
     valid = (rng.random(50) > 0.2).astype(np.uint8)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    slots, lens = B.dsv4kv_topk_to_slots(dev(topk), dev(ttr), dev(pt), page_bits,
-                                         is_valid=dev(valid), err_word=err)
+    # offset 1: topk and slots start 4 bytes past a 16-byte boundary
+    topk_d = dev(np.concatenate([[0] * offset, topk.reshape(-1)]).astype(np.int32))[offset:].view(50, k)
+    slots_buf = torch.empty(50 * k + offset, dtype=torch.int32, device="cuda")
+    slots, lens = B.dsv4kv_topk_to_slots(topk_d, dev(ttr), dev(pt), page_bits, is_valid=dev(valid),
+                                         slots=slots_buf[offset:].view(50, k), err_word=err)
     ws, wl, faults = oracle.topk_to_slots(topk, ttr, pt, page_bits, is_valid=valid)
     assert np.array_equal(slots.cpu().numpy(), ws)
     assert np.array_equal(lens.cpu().numpy(), wl)
