@@ -4,9 +4,9 @@ One step = one long-prefill batch through the whole path:
   1. dsv4kv_compress_store: 64 requests (~262k tokens, lognormal lengths),
      ratio-2 softmax pair pooling of the fused | kv | score | rows, RMSNorm,
      RoPE, V41 quantization, paged store (page size 64);
-  2. dsv4kv_topk_to_slots: each request's top-2048 compressed ids -> slots;
-  3. the sparse-prefill read: 4 layers share the source; the first
-     get_with_head runs dsv4kv_dequant_gather, the other three are reuse hits.
+  2. the sparse-prefill read of each request's top-2048 compressed ids: 4
+     layers share the source; the first get_with_head_topk runs the fused
+     top-k -> slot -> gather-dequant kernel, the other three are reuse hits.
 value = (rows stored + rows gathered) / step time, inputs resident in HBM.
 e2e   = the same through host buffers: pinned host -> device copy of the
         step's inputs and device -> host copy of the gathered rows inside the
@@ -36,7 +36,6 @@ LAYERS = 4
 # algorithmic bytes per unit (what the method must move)
 STORE_BYTES_PER_ROW = 2 * (1024 + 1024) + 256 + 528   # 2 x (kv + score) bf16, RoPE row, V41 row
 GATHER_BYTES_PER_ROW = 528 + 4 + 1024                  # V41 row + id, bf16 row out
-TOPK_BYTES_PER_ENTRY = 4 + 4                           # id in, slot out
 
 
 _CSRC = os.path.join("deepseek_v4_compressed_c2_gb300", "csrc")
@@ -268,8 +267,6 @@ def run_ours(args, rank, world):
     n_tok, k = cfg["topk"].shape
     n_gather = n_tok * k
     pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device=dev)
-    slots = torch.empty((n_tok, k), dtype=torch.int32, device=dev)
-    lens = torch.empty((n_tok,), dtype=torch.int32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     kvbuf = B.SparsePrefillKVBuffer(torch.empty((n_gather, 512), dtype=torch.bfloat16, device=dev))
     stream = torch.cuda.Stream(device=dev)
@@ -280,30 +277,25 @@ def run_ours(args, rank, world):
         store = B.prepare_compress_store(1, 2, rows_t, ext_t, pool, page_table=pt_t, page_bits=6,
                                          rmsnorm_w=w, eps=cfg["eps"], freqs_cis=freqs,
                                          n_out=n_store, err_word=err, stream=stream)
-        tk = B.prepare_topk_to_slots(topk_t, ttr_t, pt_t, 6, slots, lens, err_word=err,
-                                     stream=stream)
-        gwh = B.prepare_get_with_head(kvbuf, 1, pool, slots.view(-1), err_word=err,
-                                      stream=stream)
-        return store, tk, gwh
+        gwh = B.prepare_get_with_head_topk(kvbuf, 1, pool, topk_t, ttr_t, pt_t, 6, err_word=err,
+                                           stream=stream)
+        return store, gwh
 
     resident = prepared(rows, ext, pt, topk, ttr)
 
     def step(ev=None, calls=resident):
-        store, tk, gwh = calls
+        store, gwh = calls
         if ev is not None:
             ev[0].record(stream)
         store()
         if ev is not None:
             ev[1].record(stream)
-        tk()
-        if ev is not None:
-            ev[2].record(stream)
         kvbuf.dsv4kv_kvbuf_begin_forward()
         hits = [gwh() for _layer in range(LAYERS)]
         if ev is not None:
-            ev[3].record(stream)
+            ev[2].record(stream)
         assert hits == [False] + [True] * (LAYERS - 1)
-        launches[0] += 3
+        launches[0] += 2
         return kvbuf.storage
 
     def barrier():
@@ -317,7 +309,7 @@ def run_ours(args, rank, world):
     assert int(err.item()) == 0, "device faults during warm-up"
 
     # ---- device-resident timing
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     barrier()
@@ -335,8 +327,7 @@ def run_ours(args, rank, world):
     n_launch = launches[0]
     elapsed_ms = t0.elapsed_time(t1)
     store_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    topk_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    gather_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    gather_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
 
     # ---- end to end through host buffers (pinned host -> device -> host)
     h_rows = torch.from_numpy(cfg["rows"].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -409,9 +400,7 @@ def run_ours(args, rank, world):
         "kernels": {
             "compress_store": {"ms": store_ms, "rows_per_s": n_store / (store_ms / 1e3),
                                "gbs": store_gbs},
-            "topk_to_slots": {"ms": topk_ms,
-                              "gbs": TOPK_BYTES_PER_ENTRY * n_gather / (topk_ms / 1e3) / 1e9},
-            "dequant_gather_x1_plus_3_hits": {"ms": gather_ms,
+            "dequant_gather_topk_x1_plus_3_hits": {"ms": gather_ms,
                                               "rows_per_s": n_gather / (gather_ms / 1e3),
                                               "gbs": gather_gbs}},
         "gather_cold_l2": cold,

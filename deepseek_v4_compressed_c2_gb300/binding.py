@@ -63,6 +63,10 @@ def lib():
                                           P, I, P, LL, P, P, P, P]),
             "dsv4kv_dequant_gather": (I, [I, P, LL, P, LL, P, P, P]),
             "dsv4kv_topk_to_slots": (I, [P, I, I, P, P, P, I, I, I, P, P, P, P]),
+            "dsv4kv_dequant_gather_topk": (I, [I, P, LL, P, I, I, P, P, P, I, I, I, P, P, P, P]),
+            "dsv4kv_kvbuf_get_with_head_topk": (I, [KB, I, P, LL, P, I, I, P, P, P, I, I, I,
+                                                    ctypes.POINTER(ctypes.c_void_p), P,
+                                                    ctypes.POINTER(ctypes.c_int), P, P]),
             "dsv4kv_kvbuf_init": (I, [KB, P, LL]),
             "dsv4kv_kvbuf_begin_forward": (None, [KB]),
             "dsv4kv_kvbuf_get": (I, [KB, LL, ctypes.POINTER(ctypes.c_void_p)]),
@@ -216,6 +220,46 @@ def dsv4kv_topk_to_slots(topk, token_to_req, page_table, page_bits, *, is_valid=
     return slots, lens
 
 
+def _topk_args(topk, token_to_req, page_table, is_valid):
+    _need(topk, torch.int32, "topk")
+    _need(token_to_req, torch.int32, "token_to_req")
+    _need(page_table, torch.int32, "page_table")
+    _need(is_valid, torch.uint8, "is_valid")
+    n_tok, k = topk.shape
+    if not (topk.is_contiguous() and page_table.is_contiguous()) or token_to_req.numel() < n_tok \
+            or (is_valid is not None and is_valid.numel() < n_tok):
+        raise ValueError("topk / page_table must be contiguous; token_to_req, is_valid >= n_tok")
+    return n_tok, k
+
+
+def dsv4kv_dequant_gather_topk(layout, pool, topk, token_to_req, page_table, page_bits, out=None,
+                               *, is_valid=None, lens=None, pool_rows=None, err_word=None,
+                               stream=None):
+    """Fused top-k -> slot -> gather-dequant; returns out [n_tok * k, 512]."""
+    n_tok, k = _topk_args(topk, token_to_req, page_table, is_valid)
+    _need(out, torch.bfloat16, "out")
+    _need(lens, torch.int32, "lens")
+    _need(err_word, torch.int32, "err_word")
+    n = n_tok * k
+    if out is None:
+        out = torch.empty((n, DIM), dtype=torch.bfloat16, device=topk.device)
+    elif out.numel() < n * DIM or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of >= n_tok * k x 512")
+    if lens is not None and lens.numel() < n_tok:
+        raise ValueError("lens must hold n_tok counts")
+    pool_bytes = pool.numel() * pool.element_size()
+    if pool_rows is None:
+        pool_rows = pool_bytes // _ROW_BYTES.get(layout, 1)
+    elif pool_rows * _ROW_BYTES.get(layout, 0) > pool_bytes:
+        raise ValueError("pool_rows exceeds the pool tensor")
+    st = lib().dsv4kv_dequant_gather_topk(layout, _ptr(pool), pool_rows, _ptr(topk), n_tok, k,
+                                          _ptr(token_to_req), _ptr(is_valid), _ptr(page_table),
+                                          page_table.shape[0], page_table.shape[1], page_bits,
+                                          _ptr(out), _ptr(lens), _ptr(err_word), _stream(stream))
+    _check("dsv4kv_dequant_gather_topk", st)
+    return out
+
+
 class SparsePrefillKVBuffer:
     """The shared bf16 buffer sparse-prefill layers read, with the reuse head
     (sglang PR #45909).  Wraps a caller-owned dsv4kv_kvbuf struct and a
@@ -268,6 +312,29 @@ class SparsePrefillKVBuffer:
         if not hit.value and n > 0:
             self.dequants += 1
         return self.storage[:n], bool(hit.value)
+
+    def dsv4kv_kvbuf_get_with_head_topk(self, layout, pool, topk, token_to_req, page_table,
+                                        page_bits, *, is_valid=None, lens=None, pool_rows=None,
+                                        err_word=None, stream=None):
+        """(rows, hit) with request-local top-k ids as the gather ids; on a
+        miss the fused top-k gather-dequant fills the storage."""
+        n_tok, k = _topk_args(topk, token_to_req, page_table, is_valid)
+        pool_bytes = pool.numel() * pool.element_size()
+        if pool_rows is None:
+            pool_rows = pool_bytes // _ROW_BYTES.get(layout, 1)
+        elif pool_rows * _ROW_BYTES.get(layout, 0) > pool_bytes:
+            raise ValueError("pool_rows exceeds the pool tensor")
+        p = ctypes.c_void_p()
+        hit = ctypes.c_int(0)
+        st = lib().dsv4kv_kvbuf_get_with_head_topk(
+            ctypes.byref(self.buf), layout, _ptr(pool), pool_rows, _ptr(topk), n_tok, k,
+            _ptr(token_to_req), _ptr(is_valid), _ptr(page_table), page_table.shape[0],
+            page_table.shape[1], page_bits, ctypes.byref(p), _ptr(lens), ctypes.byref(hit),
+            _ptr(err_word), _stream(stream))
+        _check("dsv4kv_kvbuf_get_with_head_topk", st)
+        if not hit.value and n_tok * k > 0:
+            self.dequants += 1
+        return self.storage[:n_tok * k], bool(hit.value)
 
 
 class PreparedCall:
@@ -336,6 +403,33 @@ def prepare_dequant_gather(layout, pool, ids, out, *, pool_rows=None, err_word=N
     args = (layout, _ptr(pool), pool_rows, _ptr(ids), ids.numel(), _ptr(out), _ptr(err_word),
             _stream(stream))
     return PreparedCall("dsv4kv_dequant_gather", args, (pool, ids, out, err_word))
+
+
+def prepare_get_with_head_topk(kvbuf, layout, pool, topk, token_to_req, page_table, page_bits, *,
+                               is_valid=None, pool_rows=None, err_word=None, stream=None):
+    """SparsePrefillKVBuffer.get_with_head_topk with its arguments marshalled
+    once; the returned callable gives the hit flag."""
+    n_tok, k = _topk_args(topk, token_to_req, page_table, is_valid)
+    if pool_rows is None:
+        pool_rows = pool.numel() * pool.element_size() // _ROW_BYTES.get(layout, 1)
+    hit = ctypes.c_int(0)
+    rows = ctypes.c_void_p()
+    fn = lib().dsv4kv_kvbuf_get_with_head_topk
+    args = (ctypes.byref(kvbuf.buf), layout, _ptr(pool), pool_rows, _ptr(topk), n_tok, k,
+            _ptr(token_to_req), _ptr(is_valid), _ptr(page_table), page_table.shape[0],
+            page_table.shape[1], page_bits, ctypes.byref(rows), None, ctypes.byref(hit),
+            _ptr(err_word), _stream(stream))
+    keep = (pool, topk, token_to_req, page_table, is_valid, err_word, kvbuf)
+
+    def call():
+        st = fn(*args)
+        if st != 0:
+            raise DSV4KVError("dsv4kv_kvbuf_get_with_head_topk", st, lib())
+        if not hit.value and n_tok * k > 0:
+            kvbuf.dequants += 1
+        return bool(hit.value)
+    call.keep = keep
+    return call
 
 
 def prepare_get_with_head(kvbuf, layout, pool, ids, *, pool_rows=None, err_word=None,

@@ -146,6 +146,36 @@ int dsv4kv_dequant_gather(int layout, const void* pool, long long pool_rows, con
                                            err_word, static_cast<cudaStream_t>(stream)));
 }
 
+static int check_topk(const int* topk, int n_tok, int k, const int* token_to_req,
+                      const int* page_table, int n_req, int max_pages, int page_bits) {
+  if (n_tok < 0 || k < 0 || n_req < 0 || max_pages < 0) return DSV4KV_EINVAL;
+  if (page_bits < 0 || page_bits > 16) return DSV4KV_EINVAL;
+  if (k > 65536) return DSV4KV_ERANGE;
+  if (n_tok == 0 || k == 0) return DSV4KV_OK;
+  if (!token_to_req || !topk) return DSV4KV_EINVAL;
+  if (n_req > 0 && max_pages > 0 && !page_table) return DSV4KV_EINVAL;
+  if (((uintptr_t)topk & 3u) || ((uintptr_t)token_to_req & 3u) || ((uintptr_t)page_table & 3u))
+    return DSV4KV_EINVAL;
+  return DSV4KV_OK;
+}
+
+int dsv4kv_dequant_gather_topk(int layout, const void* pool, long long pool_rows, const int* topk,
+                               int n_tok, int k, const int* token_to_req,
+                               const unsigned char* is_valid, const int* page_table, int n_req,
+                               int max_pages, int page_bits, void* out_bf16, int* lens,
+                               int* err_word, void* stream) {
+  int st = check_topk(topk, n_tok, k, token_to_req, page_table, n_req, max_pages, page_bits);
+  if (st != DSV4KV_OK) return st;
+  const long long n = (long long)n_tok * k;
+  st = check_gather(layout, pool, pool_rows, topk, n, out_bf16);
+  if (st != DSV4KV_OK || n == 0) return st;
+  if ((uintptr_t)lens & 3u) return DSV4KV_EINVAL;
+  return cuda_status(launch_dequant_gather_topk(
+      layout, static_cast<const uint8_t*>(pool), pool_rows, topk, n_tok, k, token_to_req, is_valid,
+      page_table, n_req, max_pages, page_bits, static_cast<__nv_bfloat16*>(out_bf16), lens,
+      err_word, static_cast<cudaStream_t>(stream)));
+}
+
 int dsv4kv_topk_to_slots(const int* topk, int n_tok, int k, const int* token_to_req,
                          const unsigned char* is_valid, const int* page_table, int n_req,
                          int max_pages, int page_bits, int* slots, int* lens, int* err_word,
@@ -222,6 +252,28 @@ int dsv4kv_kvbuf_get_with_head(dsv4kv_kvbuf* buf, int layout, const void* pool,
   if (rows) *rows = buf->storage;
   if (*hit || n == 0) return DSV4KV_OK;
   st = dsv4kv_dequant_gather(layout, pool, pool_rows, ids, n, buf->storage, err_word, stream);
+  if (st != DSV4KV_OK) buf->head_valid = 0;
+  return st;
+}
+
+int dsv4kv_kvbuf_get_with_head_topk(dsv4kv_kvbuf* buf, int layout, const void* pool,
+                                    long long pool_rows, const int* topk, int n_tok, int k,
+                                    const int* token_to_req, const unsigned char* is_valid,
+                                    const int* page_table, int n_req, int max_pages, int page_bits,
+                                    void** rows, int* lens, int* hit, int* err_word, void* stream) {
+  if (!buf || !hit) return DSV4KV_EINVAL;
+  int st = check_topk(topk, n_tok, k, token_to_req, page_table, n_req, max_pages, page_bits);
+  if (st != DSV4KV_OK) return st;
+  const long long n = (long long)n_tok * k;
+  st = check_gather(layout, pool, pool_rows, topk, n, buf->storage);
+  if (st != DSV4KV_OK) return st;
+  st = dsv4kv_kvbuf_lookup(buf, layout, pool, pool_rows, topk, n, hit);
+  if (st != DSV4KV_OK) return st;
+  if (rows) *rows = buf->storage;
+  if (*hit || n == 0) return DSV4KV_OK;
+  st = dsv4kv_dequant_gather_topk(layout, pool, pool_rows, topk, n_tok, k, token_to_req, is_valid,
+                                  page_table, n_req, max_pages, page_bits, buf->storage, lens,
+                                  err_word, stream);
   if (st != DSV4KV_OK) buf->head_valid = 0;
   return st;
 }

@@ -5,6 +5,10 @@
 // dequantizers for fp8 and fp4); sglang PR #45909: this is the sparse-prefill
 // KV dequant whose result the layers sharing a kv_source reuse.
 //
+// The fused variant (TOPK) reads the indexer's request-local top-k ids and
+// maps them through the page table itself, so the sparse-prefill read needs
+// no separate slot pass or slot buffer.
+//
 // One warp per gathered row, kRowsPerWarp rows in flight per warp: the id
 // list is read once per group of rows (one lane per id, then shuffled), all
 // code/scale loads of the group are issued before any conversion, and each
@@ -20,11 +24,45 @@ constexpr int kGatherWarps = 8;
 constexpr int kGatherThreads = kGatherWarps * 32;
 constexpr int kRowsPerWarp = 4;
 
-template <int L>
+// Where a gathered row's pool slot comes from: an id list, or (TOPK) the
+// request-local top-k ids mapped through the request's page table exactly as
+// topk_to_slots does (flashinfer_sparse.py, _compressed_topk_to_slots).
+struct GatherSrc {
+  const int* ids;                  // [n] slots (plain gather)
+  const int* topk;                 // [n_tok, k] request-local compressed ids
+  const int* token_to_req;         // [n_tok]
+  const unsigned char* is_valid;   // [n_tok] or nullptr
+  const int* page_table;           // [n_req, max_pages]
+  int n_req, max_pages, page_bits, k;
+  int* lens;                       // [n_tok], caller-zeroed, or nullptr
+};
+
+// Slot of gathered row i under TOPK; -1 = zero row.  Faults: a token whose
+// request index is outside the table (counted once, at column 0), a page
+// index past the table (per entry).
+__device__ __forceinline__ int topk_row_slot(const GatherSrc& g, long long i, int* err) {
+  const long long t = i / g.k;
+  const int c = (int)(i - t * g.k);
+  const int r = __ldg(g.token_to_req + t);
+  const int id = __ldg(g.topk + i);
+  if (r < 0 || r >= g.n_req) {
+    if (c == 0 && err) atomicAdd(err, 1);
+    return -1;
+  }
+  if ((g.is_valid && g.is_valid[t] == 0) || id < 0) return -1;
+  const int lp = id >> g.page_bits;
+  if (lp >= g.max_pages) {
+    if (err) atomicAdd(err, 1);
+    return -1;
+  }
+  const unsigned phys = (unsigned)__ldg(g.page_table + (long long)r * g.max_pages + lp);
+  return (int)((phys << g.page_bits) | ((unsigned)id & ((1u << g.page_bits) - 1u)));
+}
+
+template <int L, bool TOPK>
 __global__ void __launch_bounds__(kGatherThreads)
-dequant_gather_kernel(const uint8_t* __restrict__ pool, long long pool_rows,
-                      const int* __restrict__ ids, long long n,
-                      __nv_bfloat16* __restrict__ out, int* err) {
+dequant_gather_kernel(const uint8_t* __restrict__ pool, long long pool_rows, const GatherSrc g,
+                      long long n, __nv_bfloat16* __restrict__ out, int* err) {
   constexpr int RB = LayoutTraits<L>::kRowBytes;
   const int lane = threadIdx.x & 31;
   const long long gw = (long long)blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
@@ -32,7 +70,21 @@ dequant_gather_kernel(const uint8_t* __restrict__ pool, long long pool_rows,
 
   for (long long i0 = gw * kRowsPerWarp; i0 < n; i0 += stride) {
     int my_id = -1;
-    if (lane < kRowsPerWarp && i0 + lane < n) my_id = __ldg(ids + i0 + lane);
+    if constexpr (!TOPK) {
+      if (lane < kRowsPerWarp && i0 + lane < n) my_id = __ldg(g.ids + i0 + lane);
+    } else {
+      const bool mine = lane < kRowsPerWarp && i0 + lane < n;
+      if (mine) my_id = topk_row_slot(g, i0 + lane, err);
+      if (g.lens) {
+        // count valid slots per token, one atomic per token present in the group
+        const long long t = mine ? (i0 + lane) / g.k : -1;
+        const long long t0 = __shfl_sync(kFullMask, t, 0);
+        const unsigned same = __ballot_sync(kFullMask, mine && t == t0);
+        const unsigned valid = __ballot_sync(kFullMask, mine && my_id >= 0);
+        if (lane == 0 && (same & valid)) atomicAdd(g.lens + t0, __popc(same & valid));
+        if (mine && t != t0 && my_id >= 0) atomicAdd(g.lens + t, 1);
+      }
+    }
 
     int id[kRowsPerWarp];
     bool valid[kRowsPerWarp];
@@ -103,10 +155,10 @@ dequant_gather_kernel(const uint8_t* __restrict__ pool, long long pool_rows,
   }
 }
 
-template <int L>
-static cudaError_t launch_layout(const uint8_t* pool, long long pool_rows, const int* ids,
+template <int L, bool TOPK>
+static cudaError_t launch_layout(const uint8_t* pool, long long pool_rows, const GatherSrc& g,
                                  long long n, __nv_bfloat16* out, int* err, cudaStream_t s) {
-  auto kern = dequant_gather_kernel<L>;
+  auto kern = dequant_gather_kernel<L, TOPK>;
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGatherThreads, 0);
   if (e != cudaSuccess) return e;
@@ -114,15 +166,37 @@ static cudaError_t launch_layout(const uint8_t* pool, long long pool_rows, const
   const long long want = (n + rows_per_block - 1) / rows_per_block;
   const long long cap = (long long)device_sm_count() * (per_sm > 0 ? per_sm : 1);
   const int grid = (int)(want < cap ? want : cap);
-  kern<<<grid, kGatherThreads, 0, s>>>(pool, pool_rows, ids, n, out, err);
+  kern<<<grid, kGatherThreads, 0, s>>>(pool, pool_rows, g, n, out, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dequant_gather(int layout, const uint8_t* pool, long long pool_rows,
                                   const int* ids, long long n, __nv_bfloat16* out, int* err,
                                   cudaStream_t s) {
-  if (layout == kV41) return launch_layout<kV41>(pool, pool_rows, ids, n, out, err, s);
-  return launch_layout<kV41Fp4>(pool, pool_rows, ids, n, out, err, s);
+  GatherSrc g{};
+  g.ids = ids;
+  if (layout == kV41) return launch_layout<kV41, false>(pool, pool_rows, g, n, out, err, s);
+  return launch_layout<kV41Fp4, false>(pool, pool_rows, g, n, out, err, s);
+}
+
+cudaError_t launch_dequant_gather_topk(int layout, const uint8_t* pool, long long pool_rows,
+                                       const int* topk, int n_tok, int k, const int* token_to_req,
+                                       const unsigned char* is_valid, const int* page_table,
+                                       int n_req, int max_pages, int page_bits,
+                                       __nv_bfloat16* out, int* lens, int* err, cudaStream_t s) {
+  GatherSrc g{};
+  g.topk = topk;
+  g.token_to_req = token_to_req;
+  g.is_valid = is_valid;
+  g.page_table = page_table;
+  g.n_req = n_req;
+  g.max_pages = max_pages;
+  g.page_bits = page_bits;
+  g.k = k;
+  g.lens = lens;
+  const long long n = (long long)n_tok * k;
+  if (layout == kV41) return launch_layout<kV41, true>(pool, pool_rows, g, n, out, err, s);
+  return launch_layout<kV41Fp4, true>(pool, pool_rows, g, n, out, err, s);
 }
 
 }  // namespace dsv4kv

@@ -164,6 +164,23 @@ int dsv4kv_dequant_gather(int layout, const void *pool, long long pool_rows,
                           int *err_word, void *stream);
 
 /*
+ * Fused top-k gather-dequant: dsv4kv_topk_to_slots followed by
+ * dsv4kv_dequant_gather in one launch, without the slot buffer [TOPK; KVL,
+ * dequantize_k_cache_paged]:
+ *   out_bf16[t*k + c] = dequant(pool row slot(t, c)), slot as in
+ *   dsv4kv_topk_to_slots; slot -1 gives a zero row, a slot >= pool_rows a
+ *   zero row and one fault.
+ * lens (nullable int32 [n_tok]) must be zeroed by the caller; the call adds
+ * each token's number of slots >= 0.  Argument rules as for the two calls it
+ * fuses; out_bf16 is [n_tok * k, 512].
+ */
+int dsv4kv_dequant_gather_topk(int layout, const void *pool, long long pool_rows,
+                               const int *topk, int n_tok, int k,
+                               const int *token_to_req, const unsigned char *is_valid,
+                               const int *page_table, int n_req, int max_pages, int page_bits,
+                               void *out_bf16, int *lens, int *err_word, void *stream);
+
+/*
  * Request-local top-k compressed ids -> physical pool slots [TOPK,
  * _compressed_topk_to_slots, single-rank branch]:
  *   slots[t][c] = page_table[req][id >> page_bits] << page_bits
@@ -226,6 +243,16 @@ int dsv4kv_kvbuf_lookup(dsv4kv_kvbuf *buf, int layout, const void *pool,
 int dsv4kv_kvbuf_get_with_head(dsv4kv_kvbuf *buf, int layout, const void *pool,
                                long long pool_rows, const int *ids, long long n,
                                void **rows, int *hit, int *err_word, void *stream);
+
+/* get_with_head whose gather ids are request-local top-k ids: the head is
+ * (layout, pool, pool_rows, topk pointer, n_tok * k); on a miss runs
+ * dsv4kv_dequant_gather_topk into the storage (lens as there, written only on
+ * a miss), on a hit launches nothing. */
+int dsv4kv_kvbuf_get_with_head_topk(dsv4kv_kvbuf *buf, int layout, const void *pool,
+                                    long long pool_rows, const int *topk, int n_tok, int k,
+                                    const int *token_to_req, const unsigned char *is_valid,
+                                    const int *page_table, int n_req, int max_pages, int page_bits,
+                                    void **rows, int *lens, int *hit, int *err_word, void *stream);
 
 #ifdef __cplusplus
 }

@@ -121,3 +121,10 @@ def test_long_prefill_ratio2_store_and_topk_gather(B):
     assert np.array_equal(slots.cpu().numpy(), ws) and np.array_equal(lens.cpu().numpy(), wl)
     want, _ = oracle.dequant_gather(1, host_pool, cfg["pool_rows"], ws.reshape(-1))
     assert np.array_equal(host_u16(out), want)
+    # the fused top-k gather (the benchmark's read path) gives the same rows
+    lens2 = torch.zeros(len(cfg["lengths"]), dtype=torch.int32, device="cuda")
+    fused = B.dsv4kv_dequant_gather_topk(1, pool, dev(cfg["topk"]), dev(cfg["token_to_req"]),
+                                         dev(cfg["page_table"]), cfg["page_bits"], lens=lens2,
+                                         err_word=err)
+    assert np.array_equal(host_u16(fused), want)
+    assert np.array_equal(lens2.cpu().numpy(), wl) and int(err.item()) == 0

@@ -380,3 +380,45 @@ def test_pool_bytes_do_not_depend_on_the_debug_outputs(B, layout):
     with_dbg = gpu_store(B, cfg, want_pre=True, want_lat=True)
     without = gpu_store(B, cfg, want_pre=False, want_lat=False)
     assert np.array_equal(with_dbg["pool"], without["pool"])
+
+
+@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4])
+def test_fused_topk_gather_matches_oracle_composition(B, layout):
+    """dsv4kv_dequant_gather_topk == oracle top-k -> slots then gather, with
+    lens and every fault kind (bad request, page past the table, slot past the
+    pool), on a pool written by the store."""
+    cfg = dict(W.cfg2_ratio2_small(), layout=layout)
+    pool = gpu_store(B, cfg)["pool"]
+    rng = np.random.default_rng(31 + layout)
+    n_tok, k = 37, 515
+    pt = cfg["page_table"].copy()
+    pt[7, 0] = 70                                   # a page past the pool (65 pages)
+    topk = rng.integers(-3, 1100, (n_tok, k), dtype=np.int32)
+    topk[2, :7] = 16 * 64 + np.arange(7)            # page index 16 >= max_pages
+    ttr = rng.integers(0, 8, n_tok).astype(np.int32)
+    ttr[5] = 9                                      # request outside the table
+    ttr[6] = 7
+    valid = (rng.random(n_tok) > 0.15).astype(np.uint8)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lens = torch.zeros(n_tok, dtype=torch.int32, device="cuda")
+    out = B.dsv4kv_dequant_gather_topk(layout, dev(pool), dev(topk), dev(ttr), dev(pt), 6,
+                                       is_valid=dev(valid), lens=lens, err_word=err)
+    ws, wl, f1 = oracle.topk_to_slots(topk, ttr, pt, 6, is_valid=valid)
+    want, f2 = oracle.dequant_gather(layout, pool, cfg["pool_rows"], ws.reshape(-1))
+    assert_bf16_equal_nan_aware(host_u16(out), want)
+    assert np.array_equal(lens.cpu().numpy(), wl)
+    assert int(err.item()) == f1 + f2 and f1 > 0 and f2 > 0
+
+
+def test_fused_topk_reuse_buffer(B):
+    cfg = W.cfg2_ratio2_small()
+    pool = dev(gpu_store(B, cfg)["pool"])
+    topk = dev(np.random.default_rng(4).integers(-1, 1000, (16, 256), dtype=np.int32))
+    ttr = dev(np.arange(16, dtype=np.int32) % 4)
+    pt = dev(cfg["page_table"])
+    buf = B.SparsePrefillKVBuffer(torch.empty((4096, 512), dtype=torch.bfloat16, device="cuda"))
+    buf.dsv4kv_kvbuf_begin_forward()
+    hits = [buf.dsv4kv_kvbuf_get_with_head_topk(1, pool, topk, ttr, pt, 6)[1] for _ in range(4)]
+    assert hits == [False, True, True, True] and buf.dequants == 1
+    fresh = B.dsv4kv_dequant_gather_topk(1, pool, topk, ttr, pt, 6)
+    assert torch.equal(buf.storage[:4096].view(torch.int16), fresh.view(torch.int16))
