@@ -66,8 +66,8 @@ def _load():
             "orc_quantize_row": (I, [I, P, P]),
             "orc_dequant_row": (I, [I, P, P]),
             "orc_row_offset": (L, [I, I, L]),
-            "orc_plan": (L, [I, P, I, P, I, I, L, P, P, P, P, P]),
-            "orc_compress_store": (L, [I, I, P, L, L, P, L, P, I, P, I, I, P, F,
+            "orc_plan": (L, [I, P, I, P, P, I, I, L, P, P, P, P, P, P]),
+            "orc_compress_store": (L, [I, I, P, L, L, P, L, P, I, P, P, I, P, I, I, P, F,
                                        P, I, P, L, P, L, P, L, P, P, P, P, P]),
             "orc_dequant_gather": (L, [I, P, L, P, L, P]),
             "orc_topk_to_slots": (L, [P, L, I, P, P, P, I, I, I, P, P]),
@@ -175,32 +175,38 @@ def row_offset(layout: int, page_bits: int, slot: int) -> int:
     return _load().orc_row_offset(layout, page_bits, slot)
 
 
-def plan(ratio, ext, page_table=None, page_bits=0):
-    """Write plan: dict of per-output-row arrays (req, j, src, pos, slot)."""
+def plan(ratio, ext, page_table=None, page_bits=0, start_pos=None):
+    """Write plan: dict of per-output-row arrays (req, j, c, src, pos, slot);
+    src = -1 marks a pair whose first token comes from the ring."""
     ext = _c(ext, np.int32)
     n_slots = ext.shape[-1]
     pt = _c(page_table, np.int32)
+    sp = _c(start_pos, np.int32)
     max_pages = 0 if pt is None else pt.shape[-1]
     lib = _load()
-    total = lib.orc_plan(ratio, _ptr(ext), n_slots, _ptr(pt), max_pages, page_bits,
-                         0, None, None, None, None, None)
+    total = lib.orc_plan(ratio, _ptr(ext), n_slots, _ptr(sp), _ptr(pt), max_pages, page_bits,
+                         0, None, None, None, None, None, None)
     req = np.zeros(total, np.int32)
     jj = np.zeros(total, np.int32)
+    cc = np.zeros(total, np.int64)
     src = np.zeros(total, np.int64)
-    pos = np.zeros(total, np.int32)
+    pos = np.zeros(total, np.int64)
     slot = np.zeros(total, np.int64)
-    lib.orc_plan(ratio, _ptr(ext), n_slots, _ptr(pt), max_pages, page_bits,
-                 total, _ptr(req), _ptr(jj), _ptr(src), _ptr(pos), _ptr(slot))
-    return dict(total=int(total), req=req, j=jj, src=src, pos=pos, slot=slot)
+    lib.orc_plan(ratio, _ptr(ext), n_slots, _ptr(sp), _ptr(pt), max_pages, page_bits,
+                 total, _ptr(req), _ptr(jj), _ptr(cc), _ptr(src), _ptr(pos), _ptr(slot))
+    return dict(total=int(total), req=req, j=jj, c=cc, src=src, pos=pos, slot=slot)
 
 
 def compress_store(layout, ratio, rows, ext, *, score=None, page_table=None,
                    page_bits=0, norm_w=None, eps=1e-6, freqs=None, out_loc=None,
                    n_out=None, pool=None, pool_rows=None, prequant_in=None,
-                   want_f64=True, want_f32=True, want_latent=True, which=None):
+                   want_f64=True, want_f32=True, want_latent=True, which=None,
+                   start_pos=None, ring=None):
     """Run the fp64 compressor.  rows/score are bf16 bit arrays (uint16) with
     rows of width >= 512 (the fused | kv | score | layout when ratio == 2 and
-    score is None).  pool (uint8, flat) is updated in place.  `which` (int64
+    score is None).  start_pos (int32 [n_slots]) and ring (uint16 bf16 bits
+    [n_slots, R, 1024], updated in place) follow orc_plan / the C header.
+    pool (uint8, flat) is updated in place.  `which` (int64
     output-row indices) restricts the work to those rows; per-row outputs and
     prequant_in are then indexed by position in `which`.  Returns a dict
     with total, faults and the requested per-row outputs."""
@@ -216,8 +222,13 @@ def compress_store(layout, ratio, rows, ext, *, score=None, page_table=None,
     freqs = _c(freqs, np.float32)
     max_pos = 0 if freqs is None else freqs.shape[0]
     out_loc = _c(out_loc, np.int32)
+    sp = _c(start_pos, np.int32)
+    if ring is not None:
+        assert ring.dtype == np.uint16 and ring.flags.c_contiguous and ring.ndim == 3
+    ring_size = 0 if ring is None else ring.shape[1]
     if n_out is None:
-        n_out = out_loc.shape[0] if out_loc is not None else plan(ratio, ext, pt, page_bits)["total"]
+        n_out = out_loc.shape[0] if out_loc is not None else \
+            plan(ratio, ext, pt, page_bits, start_pos=sp)["total"]
     if pool is not None:
         assert pool.dtype == np.uint8 and pool.flags.c_contiguous
         if pool_rows is None:
@@ -231,7 +242,8 @@ def compress_store(layout, ratio, rows, ext, *, score=None, page_table=None,
     faults = ctypes.c_int64(0)
     total = _load().orc_compress_store(
         layout, ratio, _ptr(rows), n_rows, row_stride, _ptr(score), score_stride,
-        _ptr(ext), n_slots, _ptr(pt), max_pages, page_bits, _ptr(norm_w), eps,
+        _ptr(ext), n_slots, _ptr(sp), _ptr(ring), ring_size, _ptr(pt), max_pages, page_bits,
+        _ptr(norm_w), eps,
         _ptr(freqs), max_pos, _ptr(out_loc), n_out, _ptr(which),
         0 if which is None else which.size, _ptr(pool),
         0 if pool_rows is None else pool_rows, _ptr(pre_in), _ptr(f64), _ptr(f32),

@@ -277,36 +277,50 @@ int64_t orc_row_offset(int layout, int page_bits, int64_t slot)
 }
 
 /* ------------------------------------------------------------------------ */
-/* Write plan [P2 low_ratio_extend_offsets; P3 state = pos // ratio].        */
+/* Write plan [P2 low_ratio_extend_offsets; P3 state = pos // ratio;        */
+/* P4 c2 bullet: the ratio-2 decode compressor keeps a pair-state ring].    */
 /* ext is int32 [2, n_slots]: ext[r] = first source row of request slot r,   */
-/* ext[n_slots + r] = its row count.  Output rows are numbered request by    */
-/* request, j = 0 .. count_r / ratio - 1 (an odd trailing token of a ratio-2 */
-/* request yields no row).  Row k of request r, index j: sources             */
-/* first_r + ratio*j + t (t < ratio), position ratio*j, default slot         */
-/* page_table[r][j >> page_bits] << page_bits | (j & mask).                  */
-/* Returns the total row count; fills req/jj/src/pos/slot for k < cap.       */
+/* ext[n_slots + r] = its count n_r of new tokens.  start_pos (NULL = all 0) */
+/* gives the position p0 of the first new token; new token t (t < n_r) sits  */
+/* at position p0 + t in source row first_r + t.                             */
+/* Compressed row c pools the tokens at positions ratio*c .. ratio*c+ratio-1 */
+/* and is produced by the step that holds its last token: ratio 1: c in      */
+/* [p0, p0+n); ratio 2: c in [p0 >> 1, (p0 + n) >> 1) -- an odd trailing     */
+/* token waits for the next step, and when p0 is odd the first pair's first  */
+/* token (position p0 - 1) comes from the ring.  Output rows are numbered    */
+/* request by request.  Per row k: req, j (= k - first row of the request),  */
+/* c, pos = ratio*c, src = source row of the pair's first token (-1 when it  */
+/* is in the ring), default slot page_table[r][c >> page_bits] << page_bits  */
+/* | (c & mask) (-1 past the table).  Returns the total row count; fills the */
+/* arrays for k < cap.                                                       */
 /* ------------------------------------------------------------------------ */
-int64_t orc_plan(int ratio, const int32_t *ext, int n_slots,
+int64_t orc_plan(int ratio, const int32_t *ext, int n_slots, const int32_t *start_pos,
                  const int32_t *page_table, int max_pages, int page_bits,
-                 int64_t cap, int32_t *req, int32_t *jj, int64_t *src,
-                 int32_t *pos, int64_t *slot)
+                 int64_t cap, int32_t *req, int32_t *jj, int64_t *cc, int64_t *src,
+                 int64_t *pos, int64_t *slot)
 {
     int64_t k = 0;
     int r;
     for (r = 0; r < n_slots; ++r) {
-        int64_t cnt = ext[n_slots + r] > 0 ? ext[n_slots + r] : 0;
-        int64_t j;
-        for (j = 0; j < cnt / ratio; ++j, ++k) {
+        int64_t n = ext[n_slots + r] > 0 ? ext[n_slots + r] : 0;
+        int64_t p0 = start_pos ? start_pos[r] : 0;
+        int64_t c_lo = ratio == 2 ? (p0 >> 1) : p0;
+        int64_t c_hi = ratio == 2 ? ((p0 + n) >> 1) : p0 + n;
+        int64_t c;
+        if (n == 0) continue;
+        for (c = c_lo; c < c_hi; ++c, ++k) {
+            int64_t t0 = (int64_t)ratio * c;          /* position of the first token */
             if (k >= cap) continue;
             if (req) req[k] = r;
-            if (jj) jj[k] = (int32_t)j;
-            if (src) src[k] = (int64_t)ext[r] + ratio * j;
-            if (pos) pos[k] = (int32_t)(ratio * j);
+            if (jj) jj[k] = (int32_t)(c - c_lo);
+            if (cc) cc[k] = c;
+            if (src) src[k] = t0 >= p0 ? (int64_t)ext[r] + (t0 - p0) : -1;
+            if (pos) pos[k] = t0;
             if (slot) {
-                int64_t lp = j >> page_bits;
-                slot[k] = (page_table && lp < max_pages)
+                int64_t lp = c >> page_bits;
+                slot[k] = (page_table && c >= 0 && lp < max_pages)
                     ? (((int64_t)page_table[(int64_t)r * max_pages + lp] << page_bits)
-                       | (j & (((int64_t)1 << page_bits) - 1)))
+                       | (c & (((int64_t)1 << page_bits) - 1)))
                     : -1;
             }
         }
@@ -321,6 +335,10 @@ int64_t orc_plan(int ratio, const int32_t *ext, int n_slots,
 /* rows: bf16 bits, row k at rows + k*row_stride; kv in cols [0, 512).       */
 /* score: bf16 bits [n_rows, score_stride], or NULL for the fused layout     */
 /*        (score at rows + 512).  Unused for ratio 1.                        */
+/* start_pos / ring: see orc_plan; ring is bf16 [n_slots, ring_size, 1024]   */
+/*        (kv | score per entry), read for pairs whose first token is       */
+/*        before the step and then updated (NULL: no ring; such a pair is a  */
+/*        fault).                                                            */
 /* norm_w: bf16 [512] or NULL (no RMSNorm).  freqs: fp32 [max_pos, 64]       */
 /*        (cos, sin) per complex pair, or NULL (no RoPE).                    */
 /* out_loc: int32 [n_out] slot per output row (0 = not stored), or NULL to   */
@@ -338,7 +356,8 @@ int64_t orc_compress_store(
     int layout, int ratio,
     const uint16_t *rows, int64_t n_rows, int64_t row_stride,
     const uint16_t *score, int64_t score_stride,
-    const int32_t *ext, int n_slots,
+    const int32_t *ext, int n_slots, const int32_t *start_pos,
+    uint16_t *ring, int ring_size,
     const int32_t *page_table, int max_pages, int page_bits,
     const uint16_t *norm_w, float eps,
     const float *freqs, int max_pos,
@@ -350,8 +369,8 @@ int64_t orc_compress_store(
     int64_t *n_faults)
 {
     int64_t total, k, o, faults = 0;
-    int32_t *req, *jj, *pos;
-    int64_t *src, *pslot;
+    int32_t *req, *jj;
+    int64_t *src, *pslot, *pos, *cc;
     int rb = orc_row_bytes(layout);
     double x[ORC_D];
     float xf[ORC_D];
@@ -359,17 +378,19 @@ int64_t orc_compress_store(
 
     if (ratio != 1 && ratio != 2) return -1;
     if (layout != ORC_V41 && layout != ORC_V41_FP4) return -2;
+    if (ring && (ratio != 2 || ring_size < 1)) return -1;
     for (o = 0; which && o < n_which; ++o)
         if (which[o] < 0 || which[o] >= n_out) return -1;
-    total = orc_plan(ratio, ext, n_slots, page_table, max_pages, page_bits,
-                     0, NULL, NULL, NULL, NULL, NULL);
+    total = orc_plan(ratio, ext, n_slots, start_pos, page_table, max_pages, page_bits,
+                     0, NULL, NULL, NULL, NULL, NULL, NULL);
     req = (int32_t *)calloc((size_t)(total + 1), sizeof(int32_t));
     jj = (int32_t *)calloc((size_t)(total + 1), sizeof(int32_t));
-    pos = (int32_t *)calloc((size_t)(total + 1), sizeof(int32_t));
+    cc = (int64_t *)calloc((size_t)(total + 1), sizeof(int64_t));
+    pos = (int64_t *)calloc((size_t)(total + 1), sizeof(int64_t));
     src = (int64_t *)calloc((size_t)(total + 1), sizeof(int64_t));
     pslot = (int64_t *)calloc((size_t)(total + 1), sizeof(int64_t));
-    orc_plan(ratio, ext, n_slots, page_table, max_pages, page_bits,
-             total, req, jj, src, pos, pslot);
+    orc_plan(ratio, ext, n_slots, start_pos, page_table, max_pages, page_bits,
+             total, req, jj, cc, src, pos, pslot);
 
     for (o = 0; o < (which ? n_which : n_out); ++o) {
         int d, t, bad = 0;
@@ -381,8 +402,14 @@ int64_t orc_compress_store(
             if (latent_out) memset(latent_out + o * ORC_D, 0, ORC_D * sizeof(uint16_t));
             continue;
         }
-        if (src[k] < 0 || src[k] + ratio > n_rows) bad = 1;
-        if (freqs && pos[k] >= max_pos) bad = 1;
+        {   /* the pair's tokens: new rows, or (first token) the ring */
+            int r = req[k];
+            int64_t first_new = src[k] >= 0 ? src[k] : ext[r];    /* first new source row used */
+            int64_t last_new = src[k] >= 0 ? src[k] + ratio - 1 : ext[r];
+            if (first_new < 0 || last_new >= n_rows) bad = 1;
+            if (src[k] < 0 && !ring) bad = 1;
+        }
+        if (freqs && (pos[k] < 0 || pos[k] >= max_pos)) bad = 1;
         slot = out_loc ? (int64_t)out_loc[k] : pslot[k];
         if (bad) { /* a row that cannot be computed: zero outputs, one fault */
             ++faults;
@@ -400,10 +427,17 @@ int64_t orc_compress_store(
             } else {
                 double kv[2], sc[2], m, w[2], den = 0.0, num = 0.0;
                 for (t = 0; t < 2; ++t) {
-                    int64_t rr = src[k] + t;
-                    kv[t] = orc_bf16_value(rows[rr * row_stride + d]);
-                    sc[t] = score ? orc_bf16_value(score[rr * score_stride + d])
-                                  : orc_bf16_value(rows[rr * row_stride + ORC_D + d]);
+                    if (t == 0 && src[k] < 0) {   /* token pos[k] from the pair-state ring */
+                        const uint16_t *e = ring + ((int64_t)req[k] * ring_size
+                                                    + (cc[k] % ring_size)) * (2 * ORC_D);
+                        kv[t] = orc_bf16_value(e[d]);
+                        sc[t] = orc_bf16_value(e[ORC_D + d]);
+                    } else {
+                        int64_t rr = (src[k] >= 0 ? src[k] : ext[req[k]] - 1) + t;
+                        kv[t] = orc_bf16_value(rows[rr * row_stride + d]);
+                        sc[t] = score ? orc_bf16_value(score[rr * score_stride + d])
+                                      : orc_bf16_value(rows[rr * row_stride + ORC_D + d]);
+                    }
                 }
                 m = sc[0] > sc[1] ? sc[0] : sc[1];
                 for (t = 0; t < 2; ++t) { w[t] = exp(sc[t] - m); den += w[t]; }
@@ -445,7 +479,32 @@ int64_t orc_compress_store(
         orc_quantize_row(layout, xf, rowbuf);
         if (pool) memcpy(pool + orc_row_offset(layout, page_bits, slot), rowbuf, (size_t)rb);
     }
-    free(req); free(jj); free(pos); free(src); free(pslot);
+    /* the ring keeps each request's last ring_size even-position new tokens
+     * (kv | score of position q at entry (q / 2) % ring_size), written after
+     * every row of the step has read it */
+    if (ring && !which) {
+        int r;
+        for (r = 0; r < n_slots; ++r) {
+            int64_t n = ext[n_slots + r] > 0 ? ext[n_slots + r] : 0;
+            int64_t p0 = start_pos ? start_pos[r] : 0;
+            int64_t q = p0 + n - 2 * (int64_t)ring_size;
+            if (q < p0) q = p0;
+            for (; q < p0 + n; ++q) {
+                int64_t row = (int64_t)ext[r] + (q - p0);
+                uint16_t *e;
+                int d;
+                if (q & 1) continue;
+                if (row < 0 || row >= n_rows) { ++faults; continue; }
+                e = ring + ((int64_t)r * ring_size + ((q >> 1) % ring_size)) * (2 * ORC_D);
+                for (d = 0; d < ORC_D; ++d) {
+                    e[d] = rows[row * row_stride + d];
+                    e[ORC_D + d] = score ? score[row * score_stride + d]
+                                         : rows[row * row_stride + ORC_D + d];
+                }
+            }
+        }
+    }
+    free(req); free(jj); free(pos); free(src); free(pslot); free(cc);
     if (n_faults) *n_faults = faults;
     return total;
 }
