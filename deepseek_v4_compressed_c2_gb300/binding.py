@@ -61,6 +61,8 @@ def lib():
             "dsv4kv_status_string": (ctypes.c_char_p, [I]),
             "dsv4kv_compress_store": (I, [I, I, P, LL, LL, P, LL, P, I, P, I, I, P, F, P, I,
                                           P, I, P, LL, P, P, P, P]),
+            "dsv4kv_compress_store_ring": (I, [I, I, P, LL, LL, P, LL, P, I, P, P, I, P, I, I, P,
+                                               F, P, I, P, I, P, LL, P, P, P, P]),
             "dsv4kv_dequant_gather": (I, [I, P, LL, P, LL, P, P, P]),
             "dsv4kv_topk_to_slots": (I, [P, I, I, P, P, P, I, I, I, P, P, P, P]),
             "dsv4kv_dequant_gather_topk": (I, [I, P, LL, P, I, I, P, P, P, I, I, I, P, P, P, P]),
@@ -117,10 +119,20 @@ def dsv4kv_row_bytes(layout: int) -> int:
 def dsv4kv_compress_store(layout, ratio, rows, extend_offsets, pool, *, score=None,
                           page_table=None, page_bits=0, rmsnorm_w=None, eps=1e-6,
                           freqs_cis=None, out_loc=None, n_out=None, pool_rows=None,
-                          latent_out=None, prequant_out=None, err_word=None, stream=None):
+                          latent_out=None, prequant_out=None, err_word=None, stream=None,
+                          start_pos=None, ring=None):
     """Fused compress -> RMSNorm -> RoPE -> quantize -> paged store.
     rows: bf16 [n_rows, row_stride] (unit column stride); extend_offsets: int32
-    [2, n_slots]; pool: uint8 tensor of pool_rows * row_bytes bytes."""
+    [2, n_slots]; pool: uint8 tensor of pool_rows * row_bytes bytes.  With
+    start_pos (int32 [n_slots]) and/or ring (bf16 [n_slots, R, 1024]) this is
+    dsv4kv_compress_store_ring."""
+    _need(start_pos, torch.int32, "start_pos")
+    _need(ring, torch.bfloat16, "ring")
+    if start_pos is not None and start_pos.numel() < extend_offsets.shape[1]:
+        raise ValueError("start_pos must hold n_slots positions")
+    if ring is not None and (ring.dim() != 3 or ring.shape[2] != 2 * DIM or not ring.is_contiguous()
+                             or ring.shape[0] < extend_offsets.shape[1]):
+        raise ValueError("ring must be a contiguous [>= n_slots, R, 1024] tensor")
     _need(rows, torch.bfloat16, "rows")
     _need(score, torch.bfloat16, "score")
     _need(extend_offsets, torch.int32, "extend_offsets")
@@ -163,14 +175,16 @@ def dsv4kv_compress_store(layout, ratio, rows, extend_offsets, pool, *, score=No
                                    or page_table.shape[0] < extend_offsets.shape[1]):
         raise ValueError("page_table must be a contiguous [>= n_slots, max_pages] tensor")
     s_stride = 0 if score is None else score.stride(0)
-    st = lib().dsv4kv_compress_store(
+    st = lib().dsv4kv_compress_store_ring(
         layout, ratio, _ptr(rows), rows.shape[0], rows.stride(0), _ptr(score), s_stride,
-        _ptr(extend_offsets), extend_offsets.shape[1], _ptr(page_table),
+        _ptr(extend_offsets), extend_offsets.shape[1], _ptr(start_pos), _ptr(ring),
+        0 if ring is None else ring.shape[1], _ptr(page_table),
         0 if page_table is None else page_table.shape[1], page_bits, _ptr(rmsnorm_w), eps,
         _ptr(freqs_cis), 0 if freqs_cis is None else freqs_cis.shape[0], _ptr(out_loc), n_out,
         _ptr(pool), pool_rows, _ptr(latent_out), _ptr(prequant_out), _ptr(err_word),
         _stream(stream))
-    _check("dsv4kv_compress_store", st)
+    _check("dsv4kv_compress_store_ring" if (start_pos is not None or ring is not None)
+           else "dsv4kv_compress_store", st)
 
 
 def dsv4kv_dequant_gather(layout, pool, ids, out=None, *, pool_rows=None, err_word=None,

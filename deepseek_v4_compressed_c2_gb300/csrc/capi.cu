@@ -87,6 +87,24 @@ int dsv4kv_compress_store(int layout, int ratio, const void* rows, long long n_r
                           const float* freqs_cis, int max_pos, const int* out_loc, int n_out,
                           void* pool, long long pool_rows, void* latent_out, float* prequant_out,
                           int* err_word, void* stream) {
+  return dsv4kv_compress_store_ring(layout, ratio, rows, n_rows, row_stride, score, score_stride,
+                                    extend_offsets, n_slots, nullptr, nullptr, 0, page_table,
+                                    max_pages, page_bits, rmsnorm_w, eps, freqs_cis, max_pos,
+                                    out_loc, n_out, pool, pool_rows, latent_out, prequant_out,
+                                    err_word, stream);
+}
+
+int dsv4kv_compress_store_ring(int layout, int ratio, const void* rows, long long n_rows,
+                               long long row_stride, const void* score, long long score_stride,
+                               const int* extend_offsets, int n_slots, const int* start_pos,
+                               void* ring, int ring_size, const int* page_table, int max_pages,
+                               int page_bits, const void* rmsnorm_w, float eps,
+                               const float* freqs_cis, int max_pos, const int* out_loc, int n_out,
+                               void* pool, long long pool_rows, void* latent_out,
+                               float* prequant_out, int* err_word, void* stream) {
+  if (ring && (ratio != 2 || ring_size < 1 || !aligned16(ring))) return DSV4KV_EINVAL;
+  if (!ring && ring_size != 0) return DSV4KV_EINVAL;
+  if (start_pos && ((uintptr_t)start_pos & 3u)) return DSV4KV_EINVAL;
   int st = check_rw_layout(layout);
   if (st != DSV4KV_OK) return st;
   if (ratio != 1 && ratio != 2) return DSV4KV_EINVAL;
@@ -134,6 +152,9 @@ int dsv4kv_compress_store(int layout, int ratio, const void* rows, long long n_r
   p.latent_out = static_cast<__nv_bfloat16*>(latent_out);
   p.prequant_out = prequant_out;
   p.err = err_word;
+  p.start_pos = start_pos;
+  p.ring = static_cast<__nv_bfloat16*>(ring);
+  p.ring_size = ring ? ring_size : 0;
   return cuda_status(launch_compress_store(p, layout, ratio, static_cast<cudaStream_t>(stream)));
 }
 

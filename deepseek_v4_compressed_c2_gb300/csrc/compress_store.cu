@@ -42,13 +42,15 @@ constexpr int kConsumerWarps = 8;
 constexpr int kStages = 3;
 constexpr int kStoreThreads = (kConsumerWarps + 1) * 32;
 
-enum RowState : int { kRowNone = 0, kRowPad = 1, kRowBad = 2, kRowOk = 3 };
+// kRowRing: the pair's first token is in the ring; the per-request ring phase
+// computes that row (after the tiles), not the tile consumers.
+enum RowState : int { kRowNone = 0, kRowPad = 1, kRowBad = 2, kRowOk = 3, kRowRing = 4 };
 
 struct __align__(16) RowDesc {
   int state;
-  int pos;   // RATIO * j
+  int pos;   // RATIO * c, the position of the row's first token
   int r;     // request slot
-  int j;     // row index inside the request
+  int c;     // compressed index inside the request (the page-table index)
 };
 
 template <int RATIO, bool ROPE>
@@ -65,16 +67,27 @@ struct StoreTile {
   static_assert(kSlotBytes % 16 == 0 && kStageBytes % 128 == 0, "bulk-copy alignment");
 };
 
-// base[i] = sum_{r < i} max(count_r, 0) / RATIO for i in [0, n_slots]
+// Compressed rows a request slot produces: RATIO 1: its n new tokens;
+// RATIO 2: the pairs whose second token is new, (p0 + n) / 2 - p0 / 2.
 template <int RATIO>
-__device__ void block_scan_counts(const int* __restrict__ ext, int n_slots, long long* base) {
+__device__ __forceinline__ long long rows_of_slot(int n, int p0) {
+  if (n <= 0) return 0;
+  if (RATIO == 1) return n;
+  return (((long long)p0 + n) >> 1) - ((long long)p0 >> 1);
+}
+
+// base[i] = sum_{r < i} rows_of_slot(r) for i in [0, n_slots]
+template <int RATIO>
+__device__ void block_scan_counts(const int* __restrict__ ext, const int* __restrict__ start_pos,
+                                  int n_slots, long long* base) {
   __shared__ long long s_warp[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nt = blockDim.x, nwarps = nt >> 5;
   const int per = (n_slots + nt - 1) / nt;
   const int beg = min(tid * per, n_slots), end = min(beg + per, n_slots);
   long long local = 0;
-  for (int i = beg; i < end; ++i) local += max(ext[n_slots + i], 0) / RATIO;
+  for (int i = beg; i < end; ++i)
+    local += rows_of_slot<RATIO>(ext[n_slots + i], start_pos ? start_pos[i] : 0);
   long long v = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -96,20 +109,22 @@ __device__ void block_scan_counts(const int* __restrict__ ext, int n_slots, long
   long long excl = v - local + (warp > 0 ? s_warp[warp - 1] : 0);
   for (int i = beg; i < end; ++i) {
     base[i] = excl;
-    excl += max(ext[n_slots + i], 0) / RATIO;
+    excl += rows_of_slot<RATIO>(ext[n_slots + i], start_pos ? start_pos[i] : 0);
   }
   if (tid == nt - 1) base[n_slots] = excl;
 }
 
 // The plan for output row k (shared memory only, no global loads): request
-// slot r (last slot whose prefix <= k), j = k - base[r], sources
-// first_r + RATIO*j (+1), position RATIO*j.
+// slot r (last slot whose prefix <= k), row j = k - base[r] of the request,
+// compressed index c = c_lo + j (c_lo = p0 for ratio 1, p0 / 2 for ratio 2),
+// first token at position RATIO*c in source row first_r + RATIO*c - p0, or in
+// the ring when that position precedes p0.
 template <int RATIO, bool ROPE>
 __device__ __forceinline__ RowDesc plan_row(const StoreParams& p, long long k, long long total,
                                             const long long* s_base, const int* s_first,
-                                            long long& src) {
+                                            const int* s_start, long long& src) {
   RowDesc d;
-  d.state = kRowNone; d.pos = 0; d.r = 0; d.j = 0;
+  d.state = kRowNone; d.pos = 0; d.r = 0; d.c = 0;
   src = 0;
   if (k >= p.n_out) return d;
   if (k >= total) { d.state = kRowPad; return d; }
@@ -118,25 +133,30 @@ __device__ __forceinline__ RowDesc plan_row(const StoreParams& p, long long k, l
     const int mid = (lo + hi + 1) >> 1;
     if (s_base[mid] <= k) lo = mid; else hi = mid - 1;
   }
-  const long long j = k - s_base[lo];
-  src = (long long)s_first[lo] + (long long)RATIO * j;
-  const long long pos = (long long)RATIO * j;
+  const long long p0 = s_start[lo];
+  const long long c = (RATIO == 2 ? (p0 >> 1) : p0) + (k - s_base[lo]);
+  const long long pos = (long long)RATIO * c;
   d.r = lo;
-  d.j = (int)j;
+  d.c = (int)c;
   d.pos = (int)pos;
-  const bool ok = src >= 0 && src + RATIO <= p.n_rows && (!ROPE || pos < p.max_pos);
+  src = (long long)s_first[lo] + (pos - p0);
+  if (pos < p0) {                                  // first token in the ring
+    d.state = kRowRing;
+    return d;
+  }
+  const bool ok = src >= 0 && src + RATIO <= p.n_rows && pos >= 0 && (!ROPE || pos < p.max_pos);
   d.state = ok ? kRowOk : kRowBad;
   return d;
 }
 
-// Destination slot of a planned row: out_loc[k], or the page table (-1 when
-// the page index is past the table).
+// Destination slot of a planned row: out_loc[k], or the page table at the
+// compressed index c (-1 when the page index is past the table).
 __device__ __forceinline__ long long dest_slot(const StoreParams& p, long long k, const RowDesc& d) {
   if (p.out_loc) return p.out_loc[k];
-  const long long lp = (long long)d.j >> p.page_bits;
-  if (lp >= p.max_pages) return -1;
+  const long long lp = (long long)d.c >> p.page_bits;
+  if (d.c < 0 || lp >= p.max_pages) return -1;
   return ((long long)p.page_table[(long long)d.r * p.max_pages + lp] << p.page_bits)
-         | ((long long)d.j & ((1LL << p.page_bits) - 1));
+         | ((long long)d.c & ((1LL << p.page_bits) - 1));
 }
 
 __device__ __forceinline__ void zero_row_outputs(const StoreParams& p, long long k, int lane) {
@@ -200,7 +220,7 @@ template <int L, int RATIO, bool NORM, bool ROPE>
 __device__ __forceinline__ void process_row(const StoreParams& p, long long k, const RowDesc& d,
                                             long long slot, const RowIn<RATIO, ROPE>& in,
                                             const float (&w)[16], int lane) {
-  if (d.state == kRowNone) return;
+  if (d.state == kRowNone || d.state == kRowRing) return;
   if (d.state != kRowOk) {
     if (d.state == kRowBad && lane == 0 && p.err) atomicAdd(p.err, 1);
     zero_row_outputs(p, k, lane);
@@ -281,6 +301,75 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
   }
 }
 
+// Per-request ring work (ratio 2), one warp per request slot, in program
+// order: (1) the pair whose first token precedes p0 -- token p0 - 1 from the
+// ring entry ((p0 - 1) / 2) % R, token p0 from the first new row -- then
+// (2) the ring update: each even-position new token among the last 2R
+// positions of the step goes to entry (q / 2) % R.  A lane writes exactly the
+// 16-byte words it read, so the read of (1) precedes any write of the same
+// entry; no other warp touches this request's ring.
+template <int L, bool NORM, bool ROPE>
+__device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s_base,
+                                        const int* s_first, const int* s_start,
+                                        const float (&w)[16], int warp, int lane) {
+  const __nv_bfloat16* score_base = p.score ? p.score : p.rows + kDim;
+  const long long sstride = p.score ? p.score_stride : p.row_stride;
+  for (long long r = (long long)blockIdx.x * kConsumerWarps + warp; r < p.n_slots;
+       r += (long long)gridDim.x * kConsumerWarps) {
+    const int n = p.ext[p.n_slots + r];
+    const long long p0 = s_start[r];
+    const long long first = s_first[r];
+    if (n <= 0) continue;
+    const long long k = s_base[r];
+    if ((p0 & 1) && k < p.n_out) {
+      RowDesc d;
+      d.r = (int)r; d.c = (int)(p0 >> 1); d.pos = (int)(p0 - 1);
+      const bool ok = p.ring != nullptr && p0 >= 1 && first >= 0 && first + 1 <= p.n_rows &&
+                      (!ROPE || d.pos < p.max_pos);
+      d.state = ok ? kRowOk : kRowBad;
+      RowIn<2, ROPE> in;
+      long long slot = 0;
+      if (ok) {
+        const uint4* e = reinterpret_cast<const uint4*>(
+            p.ring + ((r * p.ring_size) + (d.c % p.ring_size)) * (2 * kDim));
+        const uint4* kv = reinterpret_cast<const uint4*>(p.rows + first * p.row_stride);
+        const uint4* sc = reinterpret_cast<const uint4*>(score_base + first * sstride);
+        in.kv0[0] = e[lane];       in.kv0[1] = e[32 + lane];
+        in.s0[0] = e[64 + lane];   in.s0[1] = e[96 + lane];
+        in.kv1[0] = kv[lane];      in.kv1[1] = kv[32 + lane];
+        in.s1[0] = sc[lane];       in.s1[1] = sc[32 + lane];
+        if constexpr (ROPE) {
+          if (lane >= 24) {
+            const float4* f = reinterpret_cast<const float4*>(p.freqs + (long long)d.pos * kRopeDim);
+            in.fr[0] = f[2 * (lane - 24)];
+            in.fr[1] = f[2 * (lane - 24) + 1];
+          }
+        }
+        slot = dest_slot(p, k, d);
+      }
+      process_row<L, 2, NORM, ROPE>(p, k, d, slot, in, w, lane);
+    }
+    if (p.ring != nullptr) {
+      long long q = p0 + n - 2LL * p.ring_size;
+      if (q < p0) q = p0;
+      for (; q < p0 + n; ++q) {
+        if (q & 1) continue;
+        const long long row = first + (q - p0);
+        if (row < 0 || row >= p.n_rows) {
+          if (lane == 0 && p.err) atomicAdd(p.err, 1);
+          continue;
+        }
+        uint4* e = reinterpret_cast<uint4*>(
+            p.ring + ((r * p.ring_size) + ((q >> 1) % p.ring_size)) * (2 * kDim));
+        const uint4* kv = reinterpret_cast<const uint4*>(p.rows + row * p.row_stride);
+        const uint4* sc = reinterpret_cast<const uint4*>(score_base + row * sstride);
+        const uint4 a = kv[lane], b = kv[32 + lane], c = sc[lane], dd = sc[32 + lane];
+        e[lane] = a; e[32 + lane] = b; e[64 + lane] = c; e[96 + lane] = dd;
+      }
+    }
+  }
+}
+
 template <int L, int RATIO, bool NORM, bool ROPE>
 __global__ void __launch_bounds__(kStoreThreads, 2)
 compress_store_kernel(const StoreParams p) {
@@ -293,6 +382,7 @@ compress_store_kernel(const StoreParams p) {
   int* s_abort = reinterpret_cast<int*>(s_empty + kStages);
   long long* s_base = reinterpret_cast<long long*>(smem + TL::kFixedSmem);
   int* s_first = reinterpret_cast<int*>(s_base + p.n_slots + 1);
+  int* s_start = s_first + p.n_slots;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -303,8 +393,11 @@ compress_store_kernel(const StoreParams p) {
     *s_abort = 0;
     mbar_fence_init();
   }
-  block_scan_counts<RATIO>(p.ext, p.n_slots, s_base);
-  for (int i = threadIdx.x; i < p.n_slots; i += blockDim.x) s_first[i] = p.ext[i];
+  block_scan_counts<RATIO>(p.ext, p.start_pos, p.n_slots, s_base);
+  for (int i = threadIdx.x; i < p.n_slots; i += blockDim.x) {
+    s_first[i] = p.ext[i];
+    s_start[i] = p.start_pos ? p.start_pos[i] : 0;
+  }
   __syncthreads();
   const long long total = s_base[p.n_slots];
   const long long n_tiles = ((long long)p.n_out + TL::kRows - 1) / TL::kRows;
@@ -325,7 +418,7 @@ compress_store_kernel(const StoreParams p) {
       d.state = kRowNone;
       long long src = 0;
       if (lane < TL::kRows) {
-        d = plan_row<RATIO, ROPE>(p, tile * TL::kRows + lane, total, s_base, s_first, src);
+        d = plan_row<RATIO, ROPE>(p, tile * TL::kRows + lane, total, s_base, s_first, s_start, src);
         s_desc[s * TL::kRows + lane] = d;
       }
       uint32_t bytes = d.state == kRowOk ? (uint32_t)TL::kSlotBytes : 0u;
@@ -395,6 +488,10 @@ compress_store_kernel(const StoreParams p) {
         process_row<L, RATIO, NORM, ROPE>(p, k, d[q], slot[q], in[q], w, lane);
       }
     }
+    if constexpr (RATIO == 2) {
+      if (p.start_pos != nullptr || p.ring != nullptr)
+        ring_phase<L, NORM, ROPE>(p, s_base, s_first, s_start, w, warp, lane);
+    }
   }
 }
 
@@ -403,14 +500,14 @@ static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
   using TL = StoreTile<RATIO, ROPE>;
   auto kern = compress_store_kernel<L, RATIO, NORM, ROPE>;
   const size_t smem = (size_t)TL::kFixedSmem + sizeof(long long) * (size_t)(p.n_slots + 1)
-                    + sizeof(int) * (size_t)p.n_slots;
+                    + 2 * sizeof(int) * (size_t)p.n_slots;
   static int attr_set_for_device[64] = {0};  // the largest size any call can need, once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !attr_set_for_device[dev]) {
     const size_t max_smem = (size_t)TL::kFixedSmem + sizeof(long long) * (kMaxSlots + 1)
-                          + sizeof(int) * kMaxSlots;
+                          + 2 * sizeof(int) * kMaxSlots;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set_for_device[dev] = 1;

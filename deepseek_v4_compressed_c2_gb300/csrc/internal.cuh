@@ -33,6 +33,9 @@ struct StoreParams {
   __nv_bfloat16* latent_out;   // [n_out, 512] or nullptr
   float* prequant_out;         // [n_out, 512] or nullptr
   int* err;                    // device fault counter or nullptr
+  const int* start_pos;        // [n_slots] position of each slot's first new token, or nullptr (0)
+  __nv_bfloat16* ring;         // [n_slots, ring_size, 1024] pair-state ring (ratio 2) or nullptr
+  int ring_size;
 };
 
 cudaError_t launch_compress_store(const StoreParams& p, int layout, int ratio, cudaStream_t stream);

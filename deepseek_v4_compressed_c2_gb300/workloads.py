@@ -200,6 +200,32 @@ def cfg5_long_prefill(seed: int = 7, n_req: int = 64, target: int = 262144,
                 topk=top, token_to_req=np.arange(n_req, dtype=np.int32))
 
 
+def decode_verify(seed: int = 11, n_req: int = 512, n_new: int = 4, ring_size: int = 4,
+                  max_prefix: int = 8192, page_bits: int = 6):
+    """Ratio-2 decode / speculative-verify step: n_req requests, each with a
+    cached prefix of random length (so half start at an odd position and
+    complete their first pair with the token held in the pair-state ring),
+    n_new new tokens (1 = decode, 1 + draft = verify); fused | kv | score |
+    bf16 N(0,1) rows; a ring [n_req, ring_size, 1024] pre-filled with bf16
+    N(0,1) entries standing for earlier steps' tokens; RMSNorm weight
+    U(0.5, 1.5); RoPE theta 10000; random permuted page tables."""
+    rng = np.random.default_rng(seed)
+    p0 = rng.integers(0, max_prefix, n_req).astype(np.int32)
+    rows = bf16_normal(rng, (n_req * n_new, 2 * D))
+    ring = bf16_normal(rng, (n_req, ring_size, 2 * D))
+    w = bf16_from_f32(rng.uniform(0.5, 1.5, D).astype(np.float32))
+    max_c = (max_prefix + n_new) // 2 + 1
+    pages = -(-max_c // (1 << page_bits))
+    pt, n_pages = _page_table(rng, [pages] * n_req)
+    ext = _ext([n_new] * n_req)
+    n_out = int(sum(((int(a) + n_new) >> 1) - (int(a) >> 1) for a in p0))
+    return dict(name=f"decode_verify_{n_req}req_{n_new}tok", layout=V41, ratio=2, rows=rows,
+                score=None, ext=ext, start_pos=p0, ring=ring, page_table=pt,
+                page_bits=page_bits, norm_w=w, freqs=rope_table(max_prefix + n_new + 2),
+                eps=1e-6, n_out=n_out, pool_rows=n_pages << page_bits,
+                lengths=[n_new] * n_req)
+
+
 CONFIGS = {
     1: cfg1_v41_roundtrip,
     2: cfg2_ratio2_small,

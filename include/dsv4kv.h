@@ -147,6 +147,49 @@ int dsv4kv_compress_store(int layout, int ratio,
                           int *err_word, void *stream);
 
 /*
+ * dsv4kv_compress_store with per-request start positions and the ratio-2
+ * pair-state ring: the general extend step that covers prefill with a
+ * cached prefix (chunked prefill), decode (one new token per request) and
+ * speculative verify (1 + draft tokens) [KVL, c1/c2 bullet: the ratio-2
+ * decode compressor keeps a pair-state ring; review: the c2 kernel completes
+ * a pair at an odd position and loads RoPE frequencies at pos - 1].
+ *
+ *   start_pos   NULL (every slot starts at 0) or int32 [n_slots]: position
+ *               p0 of slot r's first new token; new token t (t < count_r) is
+ *               at position p0 + t in source row first_r + t.
+ *   Rows: compressed row c pools the tokens at positions ratio*c ..
+ *         ratio*c + ratio - 1 and is produced by the step that holds its
+ *         last token: ratio 1: c in [p0, p0 + n); ratio 2: c in
+ *         [p0 / 2, (p0 + n) / 2).  Output rows stay numbered request by
+ *         request; the page-table index of a row is c; RoPE position ratio*c.
+ *   ring        NULL or bf16 [n_slots, ring_size, 1024] (ratio 2 only),
+ *               16-B aligned, caller-owned state that lives across steps:
+ *               entry (q / 2) % ring_size holds the kv | score of the token
+ *               at even position q.  When p0 is odd, the first pair reads
+ *               token p0 - 1 from the ring (with ring == NULL that row is a
+ *               fault).  After the step, each even-position new token among
+ *               the step's last 2 * ring_size positions is written to the
+ *               ring, so ring_size >= 1 + (draft tokens) / 2 keeps every
+ *               token a rolled-back verify step can need.
+ *   ring_size   entries per request (0 when ring is NULL).
+ * Every other argument is as in dsv4kv_compress_store (which is this call
+ * with start_pos = ring = NULL).  Within one call the ring is read before
+ * it is written; calls on one stream see each other's ring updates.
+ */
+int dsv4kv_compress_store_ring(int layout, int ratio,
+                               const void *rows, long long n_rows, long long row_stride,
+                               const void *score, long long score_stride,
+                               const int *extend_offsets, int n_slots,
+                               const int *start_pos, void *ring, int ring_size,
+                               const int *page_table, int max_pages, int page_bits,
+                               const void *rmsnorm_w, float eps,
+                               const float *freqs_cis, int max_pos,
+                               const int *out_loc, int n_out,
+                               void *pool, long long pool_rows,
+                               void *latent_out, float *prequant_out,
+                               int *err_word, void *stream);
+
+/*
  * Paged gather-dequant [KVL, dequantize_k_cache_paged for the V4.1 layouts]:
  *   out_bf16[i][d] = bf16(code(ids[i], d) * scale(ids[i], d)), i < n.
  * V41: scale = 2^(e - 127) of the group's ue8m0 byte; V41_FP4: the group's

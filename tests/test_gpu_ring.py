@@ -1,0 +1,104 @@
+"""GPU parity of the start-position / pair-state-ring form of the compressor
+(decode, speculative verify, chunked prefill) against the CPU oracle, and
+chunking invariance on the GPU itself."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_v4_compressed_c2_gb300 import workloads as W
+from parity import assert_prequant_close, compare_rows_end_to_end, dev, dev_bf16, host_u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from deepseek_v4_compressed_c2_gb300 import build as b
+    b.build()
+    from deepseek_v4_compressed_c2_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def gpu_step(B, cfg, pool, ring, *, want_pre=True):
+    pre = torch.zeros((max(cfg["n_out"], 1), 512), dtype=torch.float32, device="cuda") if want_pre else None
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsv4kv_compress_store(cfg["layout"], 2, dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
+                            page_table=dev(cfg["page_table"]), page_bits=cfg["page_bits"],
+                            rmsnorm_w=dev_bf16(cfg["norm_w"]), eps=cfg["eps"],
+                            freqs_cis=dev(cfg["freqs"]), n_out=cfg["n_out"], prequant_out=pre,
+                            err_word=err, start_pos=dev(cfg["start_pos"]), ring=ring)
+    torch.cuda.synchronize()
+    return None if pre is None else pre.cpu().numpy(), int(err.item())
+
+
+@pytest.mark.parametrize("n_new,layout", [(1, oracle.V41), (4, oracle.V41), (4, oracle.V41_FP4),
+                                           (7, oracle.V41)])
+def test_decode_verify_step_matches_oracle(B, n_new, layout):
+    cfg = dict(W.decode_verify(seed=11 + n_new, n_new=n_new, ring_size=4, max_prefix=1024),
+               layout=layout)
+    rb = oracle.row_bytes(layout)
+    pool = torch.full((cfg["pool_rows"] * rb,), 0xA5, dtype=torch.uint8, device="cuda")
+    ring = dev_bf16(cfg["ring"])
+    pre, err = gpu_step(B, cfg, pool, ring)
+    ref_pool = np.full(cfg["pool_rows"] * rb, 0xA5, np.uint8)
+    ref_ring = cfg["ring"].copy()
+    kw = dict(page_table=cfg["page_table"], page_bits=cfg["page_bits"], norm_w=cfg["norm_w"],
+              eps=cfg["eps"], freqs=cfg["freqs"], n_out=cfg["n_out"], start_pos=cfg["start_pos"])
+    ref = oracle.compress_store(layout, 2, cfg["rows"], cfg["ext"], pool=ref_pool,
+                                pool_rows=cfg["pool_rows"], ring=ref_ring, **kw)
+    assert err == ref["faults"] == 0
+    assert ref["total"] == cfg["n_out"]
+    # the ring after the step: an exact copy of the right tokens
+    assert np.array_equal(host_u16(ring).reshape(ref_ring.shape), ref_ring)
+    # pre-quant within tolerance; bytes exact given the GPU's fp32 rows
+    assert_prequant_close(pre[:ref["total"]], ref["prequant_f64"][:ref["total"]])
+    same_pool = np.full(cfg["pool_rows"] * rb, 0xA5, np.uint8)
+    oracle.compress_store(layout, 2, cfg["rows"], cfg["ext"], pool=same_pool,
+                          pool_rows=cfg["pool_rows"], ring=cfg["ring"].copy(), prequant_in=pre, **kw)
+    got = pool.cpu().numpy()
+    assert np.array_equal(got, same_pool)
+    p = oracle.plan(2, cfg["ext"], cfg["page_table"], cfg["page_bits"], start_pos=cfg["start_pos"])
+    gp = got.reshape(-1, rb)[p["slot"]]
+    rp = ref_pool.reshape(-1, rb)[p["slot"]]
+    compare_rows_end_to_end(layout, gp, rp, ref["prequant_f64"], min_allowed=2)
+    assert (p["src"] < 0).sum() > 0                 # ring-sourced rows were exercised
+
+
+def test_gpu_chunked_prefill_with_ring_equals_whole(B):
+    rng = np.random.default_rng(5)
+    n = 301
+    rows = W.bf16_from_f32(rng.standard_normal((n, 1024)).astype(np.float32))
+    w = W.bf16_from_f32(rng.uniform(0.5, 1.5, 512).astype(np.float32))
+    pt = (rng.permutation(3) + 1).astype(np.int32).reshape(1, -1)
+    base = dict(layout=oracle.V41, norm_w=w, freqs=W.rope_table(512), eps=1e-6,
+                page_table=pt, page_bits=6, pool_rows=4 << 6)
+
+    def run(cuts):
+        pool = torch.zeros(base["pool_rows"] * 528, dtype=torch.uint8, device="cuda")
+        ring = torch.zeros((1, 3, 1024), dtype=torch.bfloat16, device="cuda")
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            cfg = dict(base, rows=np.ascontiguousarray(rows[a:b]),
+                       ext=np.array([[0], [b - a]], np.int32), start_pos=np.array([a], np.int32),
+                       n_out=((b >> 1) - (a >> 1)))
+            if cfg["n_out"] == 0:
+                cfg["n_out"] = 1
+            _, err = gpu_step(B, cfg, pool, ring, want_pre=False)
+            assert err == 0
+        return pool.cpu().numpy()
+
+    whole = run([0, n])
+    for cuts in ([0, 1, n], [0, 77, 78, 79, n], [0, 150, 151, 300, n], list(range(0, 40)) + [n]):
+        assert np.array_equal(run(cuts), whole)
+
+
+def test_ring_row_without_ring_is_a_counted_fault(B):
+    cfg = W.decode_verify(seed=3, n_req=64, n_new=1, max_prefix=1024)
+    pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsv4kv_compress_store(1, 2, dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
+                            page_table=dev(cfg["page_table"]), page_bits=cfg["page_bits"],
+                            n_out=cfg["n_out"], err_word=err, start_pos=dev(cfg["start_pos"]))
+    torch.cuda.synchronize()
+    assert int(err.item()) == int((cfg["start_pos"] % 2 == 1).sum()) == cfg["n_out"]
