@@ -242,6 +242,42 @@ def cold_gather(B, dev, stream, reps):
             "frac_of_8000": gbs / 8000.0, "peak_kind": kind, "bytes_per_row": GATHER_BYTES_PER_ROW}
 
 
+def decode_verify_steps(B, dev, stream, reps=50):
+    """The ring form of the compressor on decode-shaped steps (one new token
+    per request; 1 + 3 draft tokens per request), timed per launch.  These
+    are small, latency-bound launches (working set in L2)."""
+    import torch
+    from deepseek_v4_compressed_c2_gb300 import workloads as W
+    res = {}
+    for name, n_req, n_new in (("decode_4096req_1tok", 4096, 1), ("verify_1024req_4tok", 1024, 4)):
+        cfg = W.decode_verify(seed=13, n_req=n_req, n_new=n_new, ring_size=4, max_prefix=4096)
+        bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device=dev)
+        ring = bf(cfg["ring"])
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        rows = bf(cfg["rows"])
+        args_ = dict(page_table=torch.from_numpy(cfg["page_table"]).to(dev), page_bits=6,
+                     rmsnorm_w=bf(cfg["norm_w"]), eps=cfg["eps"],
+                     freqs_cis=torch.from_numpy(cfg["freqs"]).to(dev), n_out=cfg["n_out"],
+                     err_word=err, stream=stream,
+                     start_pos=torch.from_numpy(cfg["start_pos"]).to(dev), ring=ring)
+        ext = torch.from_numpy(cfg["ext"]).to(dev)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                B.dsv4kv_compress_store(1, 2, rows, ext, pool, **args_)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                B.dsv4kv_compress_store(1, 2, rows, ext, pool, **args_)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        assert int(err.item()) == 0
+        us = a.elapsed_time(b) * 1e3 / reps
+        res[name] = {"us_per_launch": us, "rows": cfg["n_out"], "tokens": n_req * n_new,
+                     "rows_per_s": cfg["n_out"] / (us / 1e6)}
+    return res
+
+
 def run_ours(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -371,6 +407,9 @@ def run_ours(args, rank, world):
     cold = None
     if not args.no_cold_gather:
         cold = cold_gather(B, dev, stream, max(5, min(args.steps, 50)))
+        decode = decode_verify_steps(B, dev, stream)
+    else:
+        decode = None
 
     # ---- max over ranks
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
@@ -404,6 +443,7 @@ def run_ours(args, rank, world):
                                               "rows_per_s": n_gather / (gather_ms / 1e3),
                                               "gbs": gather_gbs}},
         "gather_cold_l2": cold,
+        "decode_verify_ring": decode,
         "e2e": {"value": whole_job_rate(n_store + n_gather, world, e2e_ms), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

@@ -37,10 +37,9 @@ int device_sm_count() {
   return n;
 }
 
-// layout usable by store / dequant: V41 and V41_FP4; V4 is known but not built
+// layouts usable by store / dequant: all three KVLayout members
 static int check_rw_layout(int layout) {
-  if (layout == DSV4KV_V41 || layout == DSV4KV_V41_FP4) return DSV4KV_OK;
-  if (layout == DSV4KV_V4) return DSV4KV_ENOTSUP;
+  if (layout == DSV4KV_V4 || layout == DSV4KV_V41 || layout == DSV4KV_V41_FP4) return DSV4KV_OK;
   return DSV4KV_EINVAL;
 }
 
@@ -73,7 +72,7 @@ const char* dsv4kv_status_string(int status) {
   switch (status) {
     case DSV4KV_OK: return "ok";
     case DSV4KV_EINVAL: return "invalid argument (null or misaligned pointer, bad enum, negative size)";
-    case DSV4KV_ENOTSUP: return "not supported in this build (V4 rows)";
+    case DSV4KV_ENOTSUP: return "not supported in this build";
     case DSV4KV_ERANGE: return "size outside a documented limit";
     case DSV4KV_ECUDA: return "CUDA launch failed (see dsv4kv_last_cuda_error)";
     default: return "unknown status";

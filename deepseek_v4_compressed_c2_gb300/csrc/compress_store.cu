@@ -533,7 +533,9 @@ static cudaError_t launch_norm_rope(const StoreParams& p, cudaStream_t s) {
 
 cudaError_t launch_compress_store(const StoreParams& p, int layout, int ratio, cudaStream_t s) {
   if (layout == kV41) return ratio == 1 ? launch_norm_rope<kV41, 1>(p, s) : launch_norm_rope<kV41, 2>(p, s);
-  return ratio == 1 ? launch_norm_rope<kV41Fp4, 1>(p, s) : launch_norm_rope<kV41Fp4, 2>(p, s);
+  if (layout == kV41Fp4)
+    return ratio == 1 ? launch_norm_rope<kV41Fp4, 1>(p, s) : launch_norm_rope<kV41Fp4, 2>(p, s);
+  return ratio == 1 ? launch_norm_rope<kV4, 1>(p, s) : launch_norm_rope<kV4, 2>(p, s);
 }
 
 }  // namespace dsv4kv

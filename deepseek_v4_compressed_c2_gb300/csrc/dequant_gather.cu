@@ -1,4 +1,4 @@
-// Paged gather-dequant: a list of row ids -> bf16 rows.
+// Paged gather-dequant: a list of row ids -> bf16 rows (V41, V41_FP4, V4).
 //
 // sglang PR #39652 "dsv4.1: compression, KV I/O, and metadata kernels",
 // Summary (dequantize_k_cache_paged gains the KVLayout parameter; V4.1
@@ -124,6 +124,45 @@ dequant_gather_kernel(const uint8_t* __restrict__ pool, long long pool_rows, con
         o[lane] = dequant8_v41(c0[t], ue8m0_scale(e0));
         o[32 + lane] = dequant8_v41(c1[t], ue8m0_scale(e1));
       }
+    } else if constexpr (L == kV4) {
+      // half 0: codes of dims 8l.., group l/8; half 1: lanes 0..23 codes of
+      // dims 256+8l.., group 4 + l/8; lanes 24..31 the stored bf16 rope dims
+      uint2 c0[kRowsPerWarp], c1[kRowsPerWarp], c2[kRowsPerWarp], sc[kRowsPerWarp];
+#pragma unroll
+      for (int t = 0; t < kRowsPerWarp; ++t) {
+        if (valid[t]) {
+          const uint8_t* row = pool + (long long)id[t] * RB;
+          c0[t] = ld_stream_v2(row + 8 * lane);
+          if (lane < 24) {
+            c1[t] = ld_stream_v2(row + 256 + 8 * lane);
+          } else {
+            c1[t] = ld_stream_v2(row + kNopeDim + 16 * (lane - 24));
+            c2[t] = ld_stream_v2(row + kNopeDim + 16 * (lane - 24) + 8);
+          }
+          sc[t] = ld_stream_v2(row + LayoutTraits<kV4>::kCodeBytes);   // same 8 B for all lanes
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kRowsPerWarp; ++t) {
+        const long long i = i0 + t;
+        if (i >= n) break;
+        uint4* o = reinterpret_cast<uint4*>(out + i * kDim);
+        if (!valid[t]) {
+          if (id[t] >= pool_rows && lane == 0 && err) atomicAdd(err, 1);
+          o[lane] = make_uint4(0, 0, 0, 0);
+          o[32 + lane] = make_uint4(0, 0, 0, 0);
+          continue;
+        }
+        const int g0 = lane >> 3, g1 = 4 + (lane >> 3);
+        const uint32_t e0 = ((g0 < 4 ? sc[t].x : sc[t].y) >> (8 * (g0 & 3))) & 0xFFu;
+        o[lane] = dequant8_v41(c0[t], ue8m0_scale(e0));
+        if (lane < 24) {
+          const uint32_t e1 = (sc[t].y >> (8 * (g1 & 3))) & 0xFFu;
+          o[32 + lane] = dequant8_v41(c1[t], ue8m0_scale(e1));
+        } else {
+          o[32 + lane] = make_uint4(c1[t].x, c1[t].y, c2[t].x, c2[t].y);
+        }
+      }
     } else {
       uint32_t c0[kRowsPerWarp], c1[kRowsPerWarp], s0[kRowsPerWarp], s1[kRowsPerWarp];
 #pragma unroll
@@ -176,6 +215,7 @@ cudaError_t launch_dequant_gather(int layout, const uint8_t* pool, long long poo
   GatherSrc g{};
   g.ids = ids;
   if (layout == kV41) return launch_layout<kV41, false>(pool, pool_rows, g, n, out, err, s);
+  if (layout == kV4) return launch_layout<kV4, false>(pool, pool_rows, g, n, out, err, s);
   return launch_layout<kV41Fp4, false>(pool, pool_rows, g, n, out, err, s);
 }
 
@@ -196,6 +236,7 @@ cudaError_t launch_dequant_gather_topk(int layout, const uint8_t* pool, long lon
   g.lens = lens;
   const long long n = (long long)n_tok * k;
   if (layout == kV41) return launch_layout<kV41, true>(pool, pool_rows, g, n, out, err, s);
+  if (layout == kV4) return launch_layout<kV4, true>(pool, pool_rows, g, n, out, err, s);
   return launch_layout<kV41Fp4, true>(pool, pool_rows, g, n, out, err, s);
 }
 

@@ -24,9 +24,14 @@ enum KVLayout : int { kV4 = 0, kV41 = 1, kV41Fp4 = 2 };
 
 template <int L> struct LayoutTraits;
 
+// V4 (the pages give the sizes only; the order follows their wording):
+// bytes 0..447 e4m3 codes of dims 0..447, 448..575 the 64 rope dims as bf16,
+// 576..582 one ue8m0 scale per 64 nope dims, 583 zero.  Rows are 8-byte
+// aligned (584 = 8 * 73), so V4 rows move with 8-byte accesses.
 template <> struct LayoutTraits<kV4> {
+  static constexpr int kGroup = 64;                           // nope dims per ue8m0 scale
   static constexpr int kCodeBytes = kNopeDim + 2 * kRopeDim;  // fp8 nope + bf16 rope
-  static constexpr int kScaleBytes = 8;
+  static constexpr int kScaleBytes = 8;                       // 7 scales + 1 zero byte
   static constexpr int kRowBytes = kCodeBytes + kScaleBytes;
 };
 

@@ -39,8 +39,10 @@ extern "C" {
 
 /* Paged main-KV row formats [KVL, KVLayout bullet].  One row = one 512-dim
  * compressed latent (dims 0..447 "nope", 448..511 "rope").
- *   DSV4KV_V4      584 B: 448 fp8 nope + 64 bf16 rope + 8 ue8m0 bytes.
- *                  Row size only; store and dequant return DSV4KV_ENOTSUP.
+ *   DSV4KV_V4      584 B: 448 e4m3 nope codes (byte d = dim d), then the 64
+ *                  rope dims as bf16 (bytes 448..575), then 7 ue8m0 scales
+ *                  (byte 576+g scales dims 64g..64g+63) and a zero byte.
+ *                  Rows are 8-byte aligned only.
  *   DSV4KV_V41     528 B: 512 e4m3 codes (byte d = dim d), then 16 ue8m0
  *                  scale bytes (byte 512+g scales dims 32g..32g+31).
  *   DSV4KV_V41_FP4 288 B: 256 bytes of e2m1 codes (byte i holds dim 2i in
@@ -55,7 +57,7 @@ typedef enum {
 enum {
     DSV4KV_OK = 0,
     DSV4KV_EINVAL = -1,  /* NULL / misaligned pointer, bad enum, negative size */
-    DSV4KV_ENOTSUP = -2, /* a layout or mode that is not built (V4 rows) */
+    DSV4KV_ENOTSUP = -2, /* a layout or mode that is not built */
     DSV4KV_ERANGE = -3,  /* a size past a documented limit */
     DSV4KV_ECUDA = -4    /* a CUDA launch failed; see dsv4kv_last_cuda_error */
 };
@@ -96,7 +98,8 @@ const char *dsv4kv_status_string(int status);
  *   RoPE (if freqs_cis): pairs (448+2i, 449+2i), i < 32, rotated by
  *        (c, s) = freqs_cis[pos][2i], freqs_cis[pos][2i+1]
  *   prequant_out (if given) = x                        (what is quantized)
- *   store_row:  V41: per 32 dims e = max((bits(amax)>>23) - 8 +
+ *   store_row:  V41 (V4: per 64 nope dims, rope dims kept as bf16):
+ *        per 32 dims e = max((bits(amax)>>23) - 8 +
  *        ((bits(amax) & 0x7FFFFF) > 0x600000), 114), the ue8m0 byte equal to
  *        127 + ceil(log2(max(amax/448, 1e-4))); codes e4m3_rn_satfinite(
  *        x * 2^(127-e)).  V41_FP4: per 16 dims s = e4m3_rn_satfinite(amax/6),
@@ -110,7 +113,7 @@ const char *dsv4kv_status_string(int status);
  *             + (slot & (2^page_bits - 1)) * row_bytes      [KVL, PagedKV].
  *
  * Arguments:
- *   layout        DSV4KV_V41 or DSV4KV_V41_FP4.
+ *   layout        DSV4KV_V4, DSV4KV_V41 or DSV4KV_V41_FP4.
  *   ratio         1 or 2.
  *   rows          bf16 [n_rows, row_stride], 16-B aligned; kv in columns
  *                 0..511.  For ratio 2 with score == NULL the score sits in
@@ -192,8 +195,8 @@ int dsv4kv_compress_store_ring(int layout, int ratio,
 /*
  * Paged gather-dequant [KVL, dequantize_k_cache_paged for the V4.1 layouts]:
  *   out_bf16[i][d] = bf16(code(ids[i], d) * scale(ids[i], d)), i < n.
- * V41: scale = 2^(e - 127) of the group's ue8m0 byte; V41_FP4: the group's
- * e4m3 scale.  Products are exact in bf16 for every row store_row writes.
+ * V41 / V4: scale = 2^(e - 127) of the group's ue8m0 byte (V4 rope dims are
+ * copied); V41_FP4: the group's e4m3 scale.  Products are exact in bf16 for every row store_row writes.
  * ids[i] < 0 gives a zero row; ids[i] >= pool_rows gives a zero row and one
  * fault.  The pool is addressed as rows of row_bytes (pages are unpadded, so
  * a slot's byte offset is slot * row_bytes whatever the page size).

@@ -239,7 +239,30 @@ int orc_quantize_row(int layout, const float *x, uint8_t *row)
         }
         return 0;
     }
-    return -2; /* V4 store is not built */
+    if (layout == ORC_V4) {
+        /* V4 (reading of "448 fp8 nope + 64 bf16 rope + ue8m0 scales"):
+         * bytes 0..447 e4m3 codes of dims 0..447 with one ue8m0 per 64 dims
+         * (same closed form), bytes 448..575 the 64 rope dims as bf16 (RNE of
+         * the fp32 value), bytes 576..582 the 7 scales, byte 583 zero. */
+        for (g = 0; g < ORC_NOPE / 64; ++g) {
+            float amax = 0.0f;
+            unsigned e;
+            for (d = 64 * g; d < 64 * g + 64; ++d)
+                if (fabsf(x[d]) > amax) amax = fabsf(x[d]);
+            e = orc_ue8m0(amax);
+            for (d = 64 * g; d < 64 * g + 64; ++d)
+                row[d] = (uint8_t)orc_e4m3_encode(ldexp((double)x[d], 127 - (int)e));
+            row[ORC_NOPE + 2 * ORC_ROPE + g] = (uint8_t)e;
+        }
+        for (d = ORC_NOPE; d < ORC_D; ++d) {
+            uint16_t b = orc_bf16_bits((double)x[d]);
+            row[ORC_NOPE + 2 * (d - ORC_NOPE)] = (uint8_t)(b & 0xFF);
+            row[ORC_NOPE + 2 * (d - ORC_NOPE) + 1] = (uint8_t)(b >> 8);
+        }
+        row[ORC_NOPE + 2 * ORC_ROPE + 7] = 0;
+        return 0;
+    }
+    return -2;
 }
 
 /* Dequantize one row to fp64 (exact: every product fits 8 significant bits). */
@@ -259,6 +282,17 @@ int orc_dequant_row(int layout, const uint8_t *row, double *out)
             unsigned nib = (row[d / 2] >> (4 * (d & 1))) & 15u;
             out[d] = orc_e2m1_value(nib) * orc_e4m3_value(row[ORC_D / 2 + d / 16]);
         }
+        return 0;
+    }
+    if (layout == ORC_V4) {
+        for (d = 0; d < ORC_NOPE; ++d) {
+            unsigned e = row[ORC_NOPE + 2 * ORC_ROPE + d / 64];
+            double scale = (e == 255u) ? NAN : ldexp(1.0, (int)e - 127);
+            out[d] = orc_e4m3_value(row[d]) * scale;
+        }
+        for (d = ORC_NOPE; d < ORC_D; ++d)
+            out[d] = orc_bf16_value((uint16_t)(row[ORC_NOPE + 2 * (d - ORC_NOPE)]
+                                    | (row[ORC_NOPE + 2 * (d - ORC_NOPE) + 1] << 8)));
         return 0;
     }
     return -2;
@@ -375,9 +409,10 @@ int64_t orc_compress_store(
     double x[ORC_D];
     float xf[ORC_D];
     uint8_t rowbuf[600];
+    memset(rowbuf, 0, sizeof(rowbuf));
 
     if (ratio != 1 && ratio != 2) return -1;
-    if (layout != ORC_V41 && layout != ORC_V41_FP4) return -2;
+    if (layout != ORC_V4 && layout != ORC_V41 && layout != ORC_V41_FP4) return -2;
     if (ring && (ratio != 2 || ring_size < 1)) return -1;
     for (o = 0; which && o < n_which; ++o)
         if (which[o] < 0 || which[o] >= n_out) return -1;
@@ -521,7 +556,7 @@ int64_t orc_dequant_gather(int layout, const uint8_t *pool, int64_t pool_rows,
     int64_t i, faults = 0;
     int rb = orc_row_bytes(layout);
     double v[ORC_D];
-    if (layout != ORC_V41 && layout != ORC_V41_FP4) return -2;
+    if (layout != ORC_V4 && layout != ORC_V41 && layout != ORC_V41_FP4) return -2;
     for (i = 0; i < n; ++i) {
         int d;
         int64_t id = ids[i];

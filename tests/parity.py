@@ -62,7 +62,25 @@ def compare_rows_end_to_end(layout, got_rows, ref_rows, ref_prequant_f64, min_al
     budget of that many codes.  Returns (differing codes, total codes,
     flipped scale groups, group size)."""
     n = got_rows.shape[0]
-    if layout == oracle.V41:
+    if layout == oracle.V4:
+        # nope: 7 ue8m0 groups of 64 dims; rope: bf16 values within one bf16
+        # step of the oracle's (its fp32 value differs from the GPU's by
+        # at most the pre-quant tolerance)
+        gs, rs = got_rows[:, 576:583], ref_rows[:, 576:583]
+        amax = np.abs(ref_prequant_f64[:, :448]).reshape(n, 7, 64).max(axis=2)
+        flip = gs != rs
+        if flip.any():
+            assert np.all(np.abs(gs[flip].astype(int) - rs[flip].astype(int)) == 1)
+            assert np.all(_near_pow2(amax[flip] / 448.0)), "scale flip away from a 2^k boundary"
+        assert not got_rows[:, 583].any()
+        gr = oracle.bf16_to_f64(np.ascontiguousarray(got_rows[:, 448:576]).view(np.uint16))
+        rr = oracle.bf16_to_f64(np.ascontiguousarray(ref_rows[:, 448:576]).view(np.uint16))
+        assert np.all(np.abs(gr - rr) <= np.abs(rr) * 2.0 ** -7 + 1e-30)
+        gc = _signed_index(got_rows[:, :448], 8)
+        rc = _signed_index(ref_rows[:, :448], 8)
+        keep = ~np.repeat(flip, 64, axis=1)
+        group = 64
+    elif layout == oracle.V41:
         gs, rs = got_rows[:, 512:], ref_rows[:, 512:]
         amax = np.abs(ref_prequant_f64).reshape(n, 16, 32).max(axis=2)
         flip = gs != rs

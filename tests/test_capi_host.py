@@ -64,8 +64,8 @@ def _store(L, **kw):
 
 def test_compress_store_rejects_bad_arguments_before_any_launch(B):
     L = B.lib()
-    assert _store(L, layout=0) == -2                       # V4 not built
     assert _store(L, layout=7) == -1
+    assert _store(L, layout=-1) == -1
     assert _store(L, ratio=3) == -1
     assert _store(L, page_bits=17) == -1
     assert _store(L, n_out=-1) == -1
@@ -84,8 +84,8 @@ def test_compress_store_rejects_bad_arguments_before_any_launch(B):
 
 def test_dequant_and_topk_reject_bad_arguments(B):
     L = B.lib()
-    assert L.dsv4kv_dequant_gather(0, FAKE, 10, FAKE, 4, FAKE, None, None) == -2
     assert L.dsv4kv_dequant_gather(5, FAKE, 10, FAKE, 4, FAKE, None, None) == -1
+    assert L.dsv4kv_dequant_gather(0, FAKE, 10, None, 4, FAKE, None, None) == -1
     assert L.dsv4kv_dequant_gather(1, FAKE, 10, FAKE, -1, FAKE, None, None) == -1
     assert L.dsv4kv_dequant_gather(1, FAKE, 10, None, 4, FAKE, None, None) == -1
     assert L.dsv4kv_dequant_gather(1, FAKE, 10, FAKE, 4, FAKE + 2, None, None) == -1
@@ -141,3 +141,30 @@ def test_get_with_head_of_zero_rows_needs_no_launch(B):
                                             ctypes.byref(rows), ctypes.byref(hit), None, None) == 0
         assert hit.value == want and rows.value == FAKE
     assert L.dsv4kv_kvbuf_init(ctypes.byref(buf), FAKE + 8, 8) == -1   # misaligned storage
+
+
+def _ring(L, **kw):
+    a = dict(layout=1, ratio=2, rows=FAKE, n_rows=100, row_stride=1024, score=None,
+             score_stride=0, ext=FAKE, n_slots=4, start=FAKE, ring=FAKE, ring_size=4, pt=FAKE,
+             max_pages=4, page_bits=6, w=None, eps=1e-6, freqs=None, max_pos=0, out_loc=None,
+             n_out=10, pool=FAKE, pool_rows=1000, lat=None, pre=None, err=None, stream=None)
+    a.update(kw)
+    return L.dsv4kv_compress_store_ring(*a.values())
+
+
+def test_ring_and_fused_gather_reject_bad_arguments(B):
+    L = B.lib()
+    assert _ring(L, ratio=1) == -1                  # the ring holds pairs: ratio 2 only
+    assert _ring(L, ring_size=0) == -1
+    assert _ring(L, ring=FAKE + 8) == -1            # misaligned ring
+    assert _ring(L, ring=None, ring_size=3) == -1
+    assert _ring(L, start=FAKE + 2) == -1           # misaligned start positions
+    assert _ring(L, layout=5) == -1
+    assert _ring(L, n_out=0) == 0
+    g = L.dsv4kv_dequant_gather_topk
+    assert g(1, FAKE, 10, FAKE, 4, 70000, FAKE, None, FAKE, 2, 2, 6, FAKE, None, None, None) == -3
+    assert g(1, FAKE, 10, FAKE, 4, 8, FAKE, None, FAKE, 2, 2, 17, FAKE, None, None, None) == -1
+    assert g(1, FAKE, 10, FAKE, 4, 8, None, None, FAKE, 2, 2, 6, FAKE, None, None, None) == -1
+    assert g(1, FAKE, 10, FAKE, 4, 8, FAKE, None, FAKE, 2, 2, 6, FAKE + 8, None, None, None) == -1
+    assert g(7, FAKE, 10, FAKE, 4, 8, FAKE, None, FAKE, 2, 2, 6, FAKE, None, None, None) == -1
+    assert g(1, FAKE, 10, FAKE, 0, 8, FAKE, None, FAKE, 2, 2, 6, FAKE, None, None, None) == 0

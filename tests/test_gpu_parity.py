@@ -141,7 +141,7 @@ def test_ratio2_separate_score_buffer_matches_fused(B):
 # ------------------------------------------------------------ brute force
 def _random_case(seed):
     rng = np.random.default_rng(1000 + seed)
-    layout = [oracle.V41, oracle.V41_FP4][seed % 2]
+    layout = [oracle.V41, oracle.V41_FP4, oracle.V4][seed % 3]
     ratio = 1 + (seed // 2) % 2
     norm = bool(rng.integers(0, 2))
     rope = bool(rng.integers(0, 2))
@@ -176,7 +176,7 @@ def _random_case(seed):
                 pool_rows=pool_rows)
 
 
-@pytest.mark.parametrize("seed", range(32))
+@pytest.mark.parametrize("seed", range(36))
 def test_brute_force_tiny_cases(B, seed):
     cfg = _random_case(seed)
     check_store(B, cfg, min_allowed=2)
@@ -184,7 +184,7 @@ def test_brute_force_tiny_cases(B, seed):
 
 def test_every_layout_ratio_norm_rope_combination(B):
     base = W.cfg2_ratio2_small()
-    for layout in (oracle.V41, oracle.V41_FP4):
+    for layout in (oracle.V41, oracle.V41_FP4, oracle.V4):
         for ratio in (1, 2):
             for norm in (False, True):
                 for rope in (False, True):
@@ -254,9 +254,9 @@ def test_host_argument_errors_raise(B):
     cfg = W.cfg1_v41_roundtrip()
     pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device="cuda")
     with pytest.raises(B.DSV4KVError) as e:
-        B.dsv4kv_compress_store(0, 1, dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
+        B.dsv4kv_compress_store(9, 1, dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
                                 page_table=dev(cfg["page_table"]), page_bits=6, n_out=4)
-    assert e.value.status == -2
+    assert e.value.status == -1
     with pytest.raises(B.DSV4KVError):
         B.dsv4kv_compress_store(1, 3, dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
                                 page_table=dev(cfg["page_table"]), page_bits=6, n_out=4)
@@ -264,7 +264,7 @@ def test_host_argument_errors_raise(B):
         B.dsv4kv_dequant_gather(1, pool[1:], torch.zeros(4, dtype=torch.int32, device="cuda"))
 
 
-@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4])
+@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4, oracle.V4])
 def test_dequant_of_arbitrary_bytes(B, layout):
     rng = np.random.default_rng(77 + layout)
     rb = oracle.row_bytes(layout)
@@ -273,6 +273,8 @@ def test_dequant_of_arbitrary_bytes(B, layout):
     if layout == oracle.V41:
         pool[:, 512:] = rng.integers(0, 256, (n, 16), dtype=np.uint8)
         pool[:4, 512:] = [[0], [1], [254], [255]]           # scale-byte extremes
+    if layout == oracle.V4:
+        pool[:4, 576:] = [[0], [1], [254], [255]]
     ids = rng.permutation(n).astype(np.int32)
     out = host_u16(B.dsv4kv_dequant_gather(layout, dev(pool.reshape(-1)), dev(ids)))
     want, _ = oracle.dequant_gather(layout, pool.reshape(-1), n, ids)
@@ -371,7 +373,7 @@ def test_determinism_and_negative_control(B):
     assert h[2] != h[0]
 
 
-@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4])
+@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4, oracle.V4])
 def test_pool_bytes_do_not_depend_on_the_debug_outputs(B, layout):
     """With RMSNorm the V41 store folds the norm scale into its power-of-two
     multiplier when no pre-quant output is requested; the bytes must equal
@@ -382,7 +384,7 @@ def test_pool_bytes_do_not_depend_on_the_debug_outputs(B, layout):
     assert np.array_equal(with_dbg["pool"], without["pool"])
 
 
-@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4])
+@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4, oracle.V4])
 def test_fused_topk_gather_matches_oracle_composition(B, layout):
     """dsv4kv_dequant_gather_topk == oracle top-k -> slots then gather, with
     lens and every fault kind (bad request, page past the table, slot past the

@@ -197,3 +197,23 @@ def test_paged_addressing_brute_force():
         assert np.all(pool[~written] == 0xA5)
         for slot in range(0, pool_rows, 7):
             assert oracle.row_offset(layout, page_bits, slot) == slot * rb
+
+
+def test_v4_store_row_matches_independent_composition():
+    """V4 reading: 448 e4m3 nope codes (ue8m0 per 64 dims, the same closed
+    form), 64 bf16 rope values, 7 scale bytes and a zero pad byte."""
+    x = _tiny_rows(7)
+    rows = oracle.quantize_rows(oracle.V4, x)
+    assert rows.shape == (x.shape[0], 584)
+    amax = np.abs(x[:, :448].reshape(-1, 7, 64)).max(axis=2)
+    e = _bit_formula(amax)
+    assert np.array_equal(rows[:, 576:583], e.astype(np.uint8))
+    assert not rows[:, 583].any()
+    y = x[:, :448].reshape(-1, 7, 64).astype(np.float64) * np.ldexp(1.0, 127 - e)[:, :, None]
+    want = _rint_round(y, -6, 3, 448.0).reshape(-1, 448)
+    got = torch.from_numpy(rows[:, :448].copy()).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(got, want)
+    rope = torch.from_numpy(x[:, 448:].copy()).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(rows[:, 448:576].copy().view(np.int16), rope)
+    deq = oracle.dequant_rows(oracle.V4, rows)
+    assert np.array_equal(deq[:, 448:], oracle.bf16_to_f64(rope.view(np.uint16)))
