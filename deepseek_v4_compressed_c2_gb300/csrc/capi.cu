@@ -214,6 +214,14 @@ int dsv4kv_topk_to_slots(const int* topk, int n_tok, int k, const int* token_to_
                                           static_cast<cudaStream_t>(stream)));
 }
 
+int dsv4kv_selftest_bounded_wait(int polls, int* err_word, int* gave_up, void* stream) {
+  if (polls < 1 || polls > (1 << 24)) return DSV4KV_ERANGE;
+  if (!err_word || !gave_up || ((uintptr_t)err_word & 3u) || ((uintptr_t)gave_up & 3u))
+    return DSV4KV_EINVAL;
+  return cuda_status(launch_bounded_wait_selftest((uint32_t)polls, err_word, gave_up,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
 // ----------------------------------------------------------------- reuse
 int dsv4kv_kvbuf_init(dsv4kv_kvbuf* buf, void* storage_bf16, long long capacity_rows) {
   if (!buf || capacity_rows < 0) return DSV4KV_EINVAL;

@@ -75,6 +75,9 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
   return v;
 }
 
+cudaError_t launch_bounded_wait_selftest(uint32_t polls, int* err, int* gave_up,
+                                         cudaStream_t stream);
+
 // SM count and resident blocks per SM for a kernel, for persistent grids.
 int device_sm_count();
 

@@ -44,16 +44,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of `parity` to complete.  Gives up (returns false) when
-// *abort is raised by another thread, or after kSpinLimit polls -- then it
+// *abort is raised by another thread, or after `limit` polls -- then it
 // raises *abort itself and counts one timeout fault.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* err) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, int* err, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
   }
   if (atomicExch(const_cast<int*>(abort), 1) == 0 && err) atomicAdd(err, kFaultTimeout);
   return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          int* err) {
+  return mbar_wait_bounded(bar, parity, abort, err, kSpinLimit);
 }
 
 // L2 policy for data read exactly once

@@ -244,6 +244,19 @@ int dsv4kv_topk_to_slots(const int *topk, int n_tok, int k,
                          int *slots, int *lens, int *err_word, void *stream);
 
 /*
+ * Self-test of the bounded waits (no counterpart on the pages; failure
+ * detection of this library).  Every pipelined kernel waits on mbarriers
+ * with a poll limit; when a limit runs out the kernel adds
+ * DSV4KV_FAULT_TIMEOUT to err_word and returns instead of hanging.  This call
+ * runs that wait on a barrier nothing arrives on: one warp gives up after
+ * `polls` polls (1..2^24) and a second warp must see its abort flag and give
+ * up too.  Expected result: *err_word += DSV4KV_FAULT_TIMEOUT and
+ * *gave_up += 2 (both device int32, caller-zeroed).
+ */
+#define DSV4KV_FAULT_TIMEOUT (1 << 24)
+int dsv4kv_selftest_bounded_wait(int polls, int *err_word, int *gave_up, void *stream);
+
+/*
  * Source-reuse buffer [BUF]: the shared bf16 buffer the sparse-prefill layers
  * read.  It remembers the source it last dequantized -- (layout, pool,
  * pool_rows, ids pointer, n) -- and a get_with_head for that same source is a

@@ -424,3 +424,50 @@ def test_fused_topk_reuse_buffer(B):
     assert hits == [False, True, True, True] and buf.dequants == 1
     fresh = B.dsv4kv_dequant_gather_topk(1, pool, topk, ttr, pt, 6)
     assert torch.equal(buf.storage[:4096].view(torch.int16), fresh.view(torch.int16))
+
+
+def test_maximum_slots_and_page_size(B):
+    """4096 request slots (the plan's capacity, many of them empty or odd) and
+    2^16-row pages (page_bits 16) against the oracle."""
+    rng = np.random.default_rng(44)
+    n_slots = 4096
+    lens = rng.integers(0, 6, n_slots)
+    lens[rng.random(n_slots) < 0.5] = 0
+    rows = W.bf16_from_f32(rng.standard_normal((int(lens.sum()) + 1, 1024)).astype(np.float32))
+    ext = W._ext([int(v) for v in lens])
+    pt = np.zeros((n_slots, 1), np.int32)
+    per = lens // 2
+    # every request's rows fit in one 2^16-row page: give each slot its own
+    # in-page window by using out_loc for the destination instead
+    p = oracle.plan(2, ext, None, 0)
+    out_loc = np.zeros(p["total"] + 7, np.int32)
+    out_loc[:p["total"]] = 1 + rng.permutation(p["total"])
+    cfg = dict(layout=oracle.V41, ratio=2, rows=rows, ext=ext, page_table=pt, page_bits=16,
+               norm_w=None, freqs=W.rope_table(16), eps=1e-6, n_out=p["total"] + 7,
+               pool_rows=p["total"] + 1)
+    check_store(B, cfg, out_loc=out_loc, min_allowed=2)
+    # page_bits 16 through the page table: 3 pages of 65536 rows
+    big = dict(layout=oracle.V41_FP4, ratio=1, rows=W.bf16_from_f32(
+        rng.standard_normal((70000, 512)).astype(np.float32)), ext=W._ext([70000]),
+        page_table=np.array([[2, 1]], np.int32), page_bits=16, norm_w=None, freqs=None,
+        eps=1e-6, n_out=70000, pool_rows=3 << 16)
+    check_store(B, big, exact_codes=True)
+
+
+def test_bounded_wait_reports_a_timeout_instead_of_hanging(B):
+    """A wait on an mbarrier nothing arrives on gives up after its poll limit,
+    reports exactly one timeout fault, the other waiter leaves through the
+    abort flag, and the context stays usable."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gave_up = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = B.lib().dsv4kv_selftest_bounded_wait(1 << 14, err.data_ptr(), gave_up.data_ptr(),
+                                              torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1 << 24 and int(gave_up.item()) == 2
+    assert B.lib().dsv4kv_selftest_bounded_wait(0, err.data_ptr(), gave_up.data_ptr(), None) == -3
+    # the context still works
+    cfg = W.cfg1_v41_roundtrip()
+    g = gpu_store(B, cfg)
+    ref = oracle_store(cfg)
+    assert np.array_equal(g["pool"], ref["pool"])
