@@ -10,7 +10,7 @@ One step = one long-prefill batch through the whole path:
 value = (rows stored + rows gathered) / step time, inputs resident in HBM.
 e2e   = the same through host buffers: pinned host -> device copy of the
         step's inputs and device -> host copy of the gathered rows inside the
-        timed region.
+        timed region (request chunks, copies overlapped with the kernels).
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own batch (weak scaling, no collective on
@@ -33,6 +33,7 @@ if ROOT not in sys.path:
 
 METRIC = "compressed-KV rows/s (store, gather-dequant) and achieved HBM GB/s vs 8 TB/s"
 LAYERS = 4
+E2E_CHUNKS = 8
 # algorithmic bytes per unit (what the method must move)
 STORE_BYTES_PER_ROW = 2 * (1024 + 1024) + 256 + 528   # 2 x (kv + score) bf16, RoPE row, V41 row
 GATHER_BYTES_PER_ROW = 528 + 4 + 1024                  # V41 row + id, bf16 row out
@@ -151,60 +152,90 @@ def whole_job_rate(units_per_rank, world, slowest_ms):
     return units_per_rank * world / (slowest_ms / 1e3)
 
 
-def cpu_baseline(cfg, budget_s=10.0):
-    """The oracle as it stands, single-threaded, on a bounded sample of the
-    same workload: the first rows of the batch through the compressor
-    (end-to-end mode, with the store) and as many gathered rows."""
+def _oracle_sample(cfg, m):
+    """The oracle as it stands, single-threaded: the batch's first m
+    compressed rows (ratio-2 compress, RMSNorm, RoPE, V41 store) and m
+    gathered rows.  Returns seconds."""
     import oracle
     n = cfg["n_out"]
     pool = np.zeros(cfg["pool_rows"] * 528, np.uint8)
+    which = np.arange(m, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.compress_store(1, 2, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
+                          page_bits=cfg["page_bits"], norm_w=cfg["norm_w"], eps=cfg["eps"],
+                          freqs=cfg["freqs"], n_out=n, which=which, pool=pool,
+                          pool_rows=cfg["pool_rows"], want_f64=False, want_f32=False,
+                          want_latent=False)
+    oracle.dequant_gather(1, pool, cfg["pool_rows"], np.arange(64, 64 + m, dtype=np.int32))
+    return time.perf_counter() - t0
 
-    def run(m):
-        which = np.arange(m, dtype=np.int64)
-        t0 = time.perf_counter()
-        oracle.compress_store(1, 2, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
-                              page_bits=cfg["page_bits"], norm_w=cfg["norm_w"], eps=cfg["eps"],
-                              freqs=cfg["freqs"], n_out=n, which=which, pool=pool,
-                              pool_rows=cfg["pool_rows"], want_f64=False, want_f32=False,
-                              want_latent=False)
-        ids = np.arange(64, 64 + m, dtype=np.int32)
-        oracle.dequant_gather(1, pool, cfg["pool_rows"], ids)
-        return time.perf_counter() - t0
 
-    probe = min(256, n)
-    t = run(probe)
-    m = int(min(n, max(probe, probe * budget_s / max(t, 1e-6))))
-    t = run(m)
+def _sample_rows(cfg, budget_s):
+    """rows per oracle sample so that one sample takes about budget_s"""
+    probe = min(256, cfg["n_out"])
+    t = _oracle_sample(cfg, probe)
+    return int(min(cfg["n_out"], max(16, probe * budget_s / max(t, 1e-6))))
+
+
+def cpu_baseline(cfg, budget_s=10.0):
+    """The oracle timed on the host cores on a bounded sample (~budget_s) of
+    the same workload."""
+    m = _sample_rows(cfg, budget_s)
+    t = _oracle_sample(cfg, m)
     return {"value": 2 * m / t, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {m} of {n} compressed rows of the batch (ratio-2 compress, "
-                      f"RMSNorm, RoPE, V41 store) + {m} gathered rows, {t:.1f} s"}
+            "sample": f"first {m} of {cfg['n_out']} compressed rows of the batch (ratio-2 "
+                      f"compress, RMSNorm, RoPE, V41 store) + {m} gathered rows, {t:.2f} s"}
 
 
 def run_reference(args, rank):
+    """The reference arm: the CPU oracle, on rank 0 only, each step a bounded
+    sample sized so that warm-up + steps take about two minutes in all."""
     if rank != 0:
         return
     cfg = make_inputs()
-    steps = []
+    per_step = max(0.005, 120.0 / (args.steps + args.warmup))
+    m = _sample_rows(cfg, per_step)
     for _ in range(args.warmup):
-        cpu_baseline(cfg, budget_s=1.0)
-    for _ in range(args.steps):
-        steps.append(cpu_baseline(cfg, budget_s=max(1.0, 60.0 / max(args.steps, 1))))
-    v = statistics.median(s["value"] for s in steps)
+        _oracle_sample(cfg, m)
+    secs = [_oracle_sample(cfg, m) for _ in range(args.steps)]
+    t = statistics.median(secs)
+    v = 2 * m / t
+    sample = (f"first {m} of {cfg['n_out']} compressed rows (ratio-2 compress, RMSNorm, RoPE, "
+              f"V41 store) + {m} gathered rows per step, median {t * 1e3:.1f} ms")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "rows/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg["name"], "sample": steps[-1]["sample"]},
-            "cpu_baseline": dict(steps[-1], value=v),
-            "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "config": {"workload": cfg["name"], "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+def _timed(fn, flush, stream, reps):
+    """median CUDA-event time of fn() in ms, L2 flushed before each launch"""
+    import torch
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(reps + 3):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            times.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in times[3:])
+
+
 def cold_gather(B, dev, stream, reps):
-    """dsv4kv_dequant_gather timed alone with a cold L2: pool of 1,048,576 V41
-    rows (page 0 reserved) filled by the store kernel from bf16 N(0,1)
-    latents (torch generator, seed 4), ids = 262,144 unique rows (numpy
-    seed 4), a 512 MB buffer written between launches."""
+    """The store-only fill and the gather, each timed alone with a cold L2:
+    1,048,576-row pools (page 0 reserved) in V41 and V41_FP4 layouts, filled
+    by the ratio-1 store from bf16 N(0,1) latents (torch generator, seed 4);
+    262,144 unique row ids (numpy seed 4); a 512 MB buffer written between
+    launches."""
     import torch
     pool_rows, n_ids = 1 << 20, 1 << 18
     g = torch.Generator(device=dev)
@@ -212,34 +243,34 @@ def cold_gather(B, dev, stream, reps):
     lat = torch.randn((pool_rows - 64, 512), generator=g, device=dev).to(torch.bfloat16)
     ext = torch.tensor([[0], [pool_rows - 64]], dtype=torch.int32, device=dev)
     pt = torch.arange(1, pool_rows // 64, dtype=torch.int32, device=dev).view(1, -1)
-    pool = torch.zeros(pool_rows * 528, dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    B.dsv4kv_compress_store(1, 1, lat, ext, pool, page_table=pt, page_bits=6,
-                            n_out=pool_rows - 64, err_word=err, stream=stream)
-    del lat
     rng = np.random.default_rng(4)
     ids = torch.from_numpy((rng.choice(pool_rows - 64, n_ids, replace=False) + 64)
                            .astype(np.int32)).to(dev)
     out = torch.empty((n_ids, 512), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    call = B.prepare_dequant_gather(1, pool, ids, out, err_word=err, stream=stream)
-    times = []
-    with torch.cuda.stream(stream):
-        for i in range(reps + 3):
-            flush.fill_(i & 0xFF)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            call()
-            b.record(stream)
-            times.append((a, b))
-    torch.cuda.synchronize(dev)
-    assert int(err.item()) == 0
-    ms = statistics.median(a.elapsed_time(b) for a, b in times[3:])
-    gbs = GATHER_BYTES_PER_ROW * n_ids / (ms / 1e3) / 1e9
     peak, kind = _peaks()
-    return {"workload": "gather_v41_262144_of_1048576_cold_l2", "ms": ms,
-            "rows_per_s": n_ids / (ms / 1e3), "gbs": gbs, "frac": gbs / peak,
-            "frac_of_8000": gbs / 8000.0, "peak_kind": kind, "bytes_per_row": GATHER_BYTES_PER_ROW}
+    res = {}
+    for layout, name, rb in ((1, "v41", 528), (2, "fp4", 288)):
+        pool = torch.zeros(pool_rows * rb, dtype=torch.uint8, device=dev)
+        store = B.prepare_compress_store(layout, 1, lat, ext, pool, page_table=pt, page_bits=6,
+                                         n_out=pool_rows - 64, err_word=err, stream=stream)
+        gather = B.prepare_dequant_gather(layout, pool, ids, out, err_word=err, stream=stream)
+        ms_s = _timed(store, flush, stream, max(3, reps // 5))
+        ms_g = _timed(gather, flush, stream, reps)
+        assert int(err.item()) == 0
+        sb, gb = 1024 + rb, rb + 4 + 1024
+        res[f"store_ratio1_{name}_1048512rows"] = {
+            "ms": ms_s, "rows_per_s": (pool_rows - 64) / (ms_s / 1e3),
+            "gbs": sb * (pool_rows - 64) / (ms_s / 1e3) / 1e9,
+            "frac": sb * (pool_rows - 64) / (ms_s / 1e3) / 1e9 / peak, "bytes_per_row": sb}
+        res[f"gather_{name}_262144_of_1048576"] = {
+            "ms": ms_g, "rows_per_s": n_ids / (ms_g / 1e3), "gbs": gb * n_ids / (ms_g / 1e3) / 1e9,
+            "frac": gb * n_ids / (ms_g / 1e3) / 1e9 / peak, "frac_of_8000": gb * n_ids / (ms_g / 1e3) / 8e12,
+            "bytes_per_row": gb}
+        del pool
+    res["peak_kind"] = kind
+    return res
 
 
 def decode_verify_steps(B, dev, stream, reps=50):
@@ -365,42 +396,89 @@ def run_ours(args, rank, world):
     store_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     gather_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
 
-    # ---- end to end through host buffers (pinned host -> device -> host)
+    # ---- end to end through host buffers (pinned host -> device -> host).
+    # The batch is split into request chunks whose rows are contiguous; chunk
+    # c's rows travel host -> device while chunk c-1 is stored and gathered,
+    # and gathered rows travel back on a third stream.  Each step still moves
+    # every input row in and every gathered row out.
+    n_req = len(cfg["lengths"])
+    bounds = np.linspace(0, n_req, E2E_CHUNKS + 1).astype(int)
+    first, counts = cfg["ext"][0].astype(np.int64), cfg["ext"][1].astype(np.int64)
     h_rows = torch.from_numpy(cfg["rows"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_ext = torch.from_numpy(cfg["ext"]).pin_memory()
-    h_pt = torch.from_numpy(cfg["page_table"]).pin_memory()
-    h_topk = torch.from_numpy(cfg["topk"]).pin_memory()
-    h_ttr = torch.from_numpy(cfg["token_to_req"]).pin_memory()
+    d_rows = rows.clone()
+    d_out = torch.empty((n_gather, 512), dtype=torch.bfloat16, device=dev)
     h_out = torch.empty((n_gather, 512), dtype=torch.bfloat16).pin_memory()
-    d_rows, d_ext, d_pt, d_topk, d_ttr = (t.clone() for t in (rows, ext, pt, topk, ttr))
-    h2d = sum(t.numel() * t.element_size() for t in (h_rows, h_ext, h_pt, h_topk, h_ttr))
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    chunks, h2d = [], 0
+    for c in range(E2E_CHUNKS):
+        r0, r1 = int(bounds[c]), int(bounds[c + 1])
+        if r1 <= r0:
+            continue
+        row0, row1 = int(first[r0]), int(first[r1 - 1] + counts[r1 - 1])
+        meta = {"ext": np.ascontiguousarray(cfg["ext"][:, r0:r1]),
+                "pt": np.ascontiguousarray(cfg["page_table"][r0:r1]),
+                "topk": np.ascontiguousarray(cfg["topk"][r0:r1]),
+                "ttr": np.arange(r1 - r0, dtype=np.int32)}
+        h_meta = {k2: torch.from_numpy(v).pin_memory() for k2, v in meta.items()}
+        d_meta = {k2: v.to(dev) for k2, v in h_meta.items()}
+        n_out_c = int((counts[r0:r1] // 2).sum())
+        k_tok = cfg["topk"].shape[1]
+        store_c = B.prepare_compress_store(1, 2, d_rows, d_meta["ext"], pool, page_table=d_meta["pt"],
+                                           page_bits=6, rmsnorm_w=w, eps=cfg["eps"],
+                                           freqs_cis=freqs, n_out=n_out_c, err_word=err,
+                                           stream=stream)
+        gather_c = B.prepare_dequant_gather_topk(1, pool, d_meta["topk"], d_meta["ttr"],
+                                                 d_meta["pt"], 6, d_out[r0 * k_tok:r1 * k_tok],
+                                                 err_word=err, stream=stream)
+        h2d += (row1 - row0) * rows.stride(0) * 2 + sum(v.numel() * v.element_size()
+                                                         for v in h_meta.values())
+        chunks.append(dict(rows=(row0, row1), out=(r0 * k_tok, r1 * k_tok), h=h_meta, d=d_meta,
+                           store=store_c, gather=gather_c,
+                           ev_in=torch.cuda.Event(), ev_done=torch.cuda.Event(),
+                           ev_out=torch.cuda.Event()))
     d2h = h_out.numel() * h_out.element_size()
     e2e_steps = max(3, min(args.steps, 30))
 
-    from_host = prepared(d_rows, d_ext, d_pt, d_topk, d_ttr)
-
     def e2e_step():
-        for d, h in ((d_rows, h_rows), (d_ext, h_ext), (d_pt, h_pt), (d_topk, h_topk), (d_ttr, h_ttr)):
-            d.copy_(h, non_blocking=True)
-        out = step(None, from_host)
-        h_out.copy_(out, non_blocking=True)
+        for ch in chunks:                          # inputs in
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ch["ev_done"])     # the previous step is done with them
+                for k2 in ch["h"]:
+                    ch["d"][k2].copy_(ch["h"][k2], non_blocking=True)
+                a, b = ch["rows"]
+                d_rows[a:b].copy_(h_rows[a:b], non_blocking=True)
+                ch["ev_in"].record(s_in)
+        for ch in chunks:                          # store + gather
+            stream.wait_event(ch["ev_in"])
+            stream.wait_event(ch["ev_out"])        # d_out chunk copied out by the last step
+            ch["store"]()
+            ch["gather"]()
+            ch["ev_done"].record(stream)
+        for ch in chunks:                          # gathered rows out
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ch["ev_done"])
+                a, b = ch["out"]
+                h_out[a:b].copy_(d_out[a:b], non_blocking=True)
+                ch["ev_out"].record(s_out)
+        launches[0] += 2 * len(chunks)
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
+    for _ in range(2):
+        e2e_step()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
+    e0.record(s_in)
+    for _ in range(e2e_steps):
+        e2e_step()
+    s_out.wait_event(chunks[-1]["ev_out"])
+    e1.record(s_out)
     torch.cuda.synchronize(dev)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     assert int(err.item()) == 0, "device faults during the timed region"
+    # the host copy of the gathered rows equals the device-resident step's
+    assert torch.equal(h_out.view(torch.int16), kvbuf.storage[:n_gather].cpu().view(torch.int16))
 
     # ---- the gather alone on a cold L2: a 1 Mi-row V41 pool (553 MB), 262,144
     # unique random ids, L2 flushed (a 512 MB write) before every launch
@@ -442,7 +520,7 @@ def run_ours(args, rank, world):
             "dequant_gather_topk_x1_plus_3_hits": {"ms": gather_ms,
                                               "rows_per_s": n_gather / (gather_ms / 1e3),
                                               "gbs": gather_gbs}},
-        "gather_cold_l2": cold,
+        "cold_l2": cold,
         "decode_verify_ring": decode,
         "e2e": {"value": whole_job_rate(n_store + n_gather, world, e2e_ms), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d,

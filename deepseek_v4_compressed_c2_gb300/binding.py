@@ -420,6 +420,22 @@ def prepare_dequant_gather(layout, pool, ids, out, *, pool_rows=None, err_word=N
     return PreparedCall("dsv4kv_dequant_gather", args, (pool, ids, out, err_word))
 
 
+def prepare_dequant_gather_topk(layout, pool, topk, token_to_req, page_table, page_bits, out, *,
+                                is_valid=None, pool_rows=None, err_word=None, stream=None):
+    """dsv4kv_dequant_gather_topk with its arguments marshalled once."""
+    dsv4kv_dequant_gather_topk(layout, pool, topk, token_to_req, page_table, page_bits, out,
+                               is_valid=is_valid, pool_rows=pool_rows, err_word=err_word,
+                               stream=stream)
+    n_tok, k = topk.shape
+    if pool_rows is None:
+        pool_rows = pool.numel() * pool.element_size() // _ROW_BYTES.get(layout, 1)
+    args = (layout, _ptr(pool), pool_rows, _ptr(topk), n_tok, k, _ptr(token_to_req),
+            _ptr(is_valid), _ptr(page_table), page_table.shape[0], page_table.shape[1], page_bits,
+            _ptr(out), None, _ptr(err_word), _stream(stream))
+    return PreparedCall("dsv4kv_dequant_gather_topk", args,
+                        (pool, topk, token_to_req, page_table, is_valid, out, err_word))
+
+
 def prepare_get_with_head_topk(kvbuf, layout, pool, topk, token_to_req, page_table, page_bits, *,
                                is_valid=None, pool_rows=None, err_word=None, stream=None):
     """SparsePrefillKVBuffer.get_with_head_topk with its arguments marshalled
