@@ -70,6 +70,7 @@ def lib():
                                                     ctypes.POINTER(ctypes.c_void_p), P,
                                                     ctypes.POINTER(ctypes.c_int), P, P]),
             "dsv4kv_selftest_bounded_wait": (I, [I, P, P, P]),
+            "dsv4kv_selftest_fp4_quotient": (I, [P, P, LL, P, P, P]),
             "dsv4kv_kvbuf_init": (I, [KB, P, LL]),
             "dsv4kv_kvbuf_begin_forward": (None, [KB]),
             "dsv4kv_kvbuf_get": (I, [KB, LL, ctypes.POINTER(ctypes.c_void_p)]),

@@ -222,6 +222,17 @@ int dsv4kv_selftest_bounded_wait(int polls, int* err_word, int* gave_up, void* s
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+int dsv4kv_selftest_fp4_quotient(const float* x, const unsigned char* scale_codes, long long n,
+                                 float* q_fast, float* q_ieee, void* stream) {
+  if (n < 0) return DSV4KV_EINVAL;
+  if (n == 0) return DSV4KV_OK;
+  if (!x || !scale_codes || !q_fast || !q_ieee || ((uintptr_t)x & 3u) ||
+      ((uintptr_t)q_fast & 3u) || ((uintptr_t)q_ieee & 3u))
+    return DSV4KV_EINVAL;
+  return cuda_status(launch_fp4_quotient_selftest(x, scale_codes, n, q_fast, q_ieee,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
 // ----------------------------------------------------------------- reuse
 int dsv4kv_kvbuf_init(dsv4kv_kvbuf* buf, void* storage_bf16, long long capacity_rows) {
   if (!buf || capacity_rows < 0) return DSV4KV_EINVAL;

@@ -78,6 +78,10 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
 cudaError_t launch_bounded_wait_selftest(uint32_t polls, int* err, int* gave_up,
                                          cudaStream_t stream);
 
+cudaError_t launch_fp4_quotient_selftest(const float* x, const unsigned char* scale_codes,
+                                         long long n, float* q_fast, float* q_ieee,
+                                         cudaStream_t stream);
+
 // SM count and resident blocks per SM for a kernel, for persistent grids.
 int device_sm_count();
 

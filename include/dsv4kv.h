@@ -257,6 +257,16 @@ int dsv4kv_topk_to_slots(const int *topk, int n_tok, int k,
 int dsv4kv_selftest_bounded_wait(int polls, int *err_word, int *gave_up, void *stream);
 
 /*
+ * Self-test of the V41_FP4 quantizer's division (no counterpart on the pages):
+ * for each i, with s = the e4m3 value of scale_codes[i], writes the
+ * quantizer's quotient x[i] / s (reciprocal plus one correction step) to
+ * q_fast[i] and the IEEE division to q_ieee[i]; the two must agree bit for
+ * bit.  x, q_fast, q_ieee: fp32 [n] device; scale_codes: uint8 [n] device.
+ */
+int dsv4kv_selftest_fp4_quotient(const float *x, const unsigned char *scale_codes, long long n,
+                                 float *q_fast, float *q_ieee, void *stream);
+
+/*
  * Source-reuse buffer [BUF]: the shared bf16 buffer the sparse-prefill layers
  * read.  It remembers the source it last dequantized -- (layout, pool,
  * pool_rows, ids pointer, n) -- and a get_with_head for that same source is a

@@ -471,3 +471,37 @@ def test_bounded_wait_reports_a_timeout_instead_of_hanging(B):
     g = gpu_store(B, cfg)
     ref = oracle_store(cfg)
     assert np.array_equal(g["pool"], ref["pool"])
+
+
+def test_fp4_quotient_matches_ieee_division_for_every_scale(B):
+    """The FP4 quantizer divides by the e4m3 scale with a correctly rounded
+    reciprocal and one correction step; it must equal the IEEE division bit
+    for bit, for all 126 positive finite e4m3 divisors, on random fp32
+    dividends over the quantizer's range and on dividends at and next to
+    every e2m1 rounding midpoint times the divisor."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(123)
+    codes = torch.arange(1, 127, dtype=torch.uint8, device="cuda")          # 0x01..0x7E
+    s = torch.from_numpy(np.array([oracle.e4m3_value(c) for c in range(1, 127)], np.float32)).cuda()
+    per = 1 << 17
+    # random dividends: |x| up to 8 s, and tiny ones, both signs
+    u = torch.rand((126, per), generator=g, device="cuda")
+    x_rand = (u * 8 - 4) * s[:, None] * 2
+    x_tiny = (torch.rand((126, per // 8), generator=g, device="cuda") - 0.5) * s[:, None] * 2.0 ** -20
+    # near ties: t * s with the fp32 neighbours, t every e2m1 midpoint and value
+    t = torch.tensor([0.25, 0.5, 0.75, 1, 1.25, 1.5, 1.75, 2, 2.5, 3, 3.5, 4, 5, 6, 7],
+                     device="cuda")
+    base = (t[None, :] * s[:, None]).contiguous()
+    bits = base.view(torch.int32)
+    near = torch.cat([(bits + d).view(torch.float32) for d in range(-8, 9)], dim=1)
+    x = torch.cat([x_rand, x_tiny, near, -near], dim=1).contiguous()
+    sc = codes[:, None].expand_as(x).contiguous()
+    q_fast = torch.empty_like(x)
+    q_ieee = torch.empty_like(x)
+    st = B.lib().dsv4kv_selftest_fp4_quotient(x.data_ptr(), sc.data_ptr(), x.numel(),
+                                              q_fast.data_ptr(), q_ieee.data_ptr(),
+                                              torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    bad = q_fast.view(torch.int32) != q_ieee.view(torch.int32)
+    assert int(bad.sum()) == 0, f"{int(bad.sum())} quotients differ, e.g. {x[bad][:4].tolist()}"
