@@ -24,7 +24,7 @@
 //    source rows (one 4 KB copy for a ratio-2 pair in the fused layout) and
 //    of its RoPE row into a 3-stage shared-memory ring; an mbarrier per stage
 //    counts the bytes in flight;
-//  * eight consumer warps, each owning one row (ratio 2) or two (ratio 1) of
+//  * eight consumer warps, each owning one row (ratio 2) or four (ratio 1) of
 //    the stage: wait for the stage, pull the row into registers, release the
 //    slot, look up the destination (out_loc or the page table) and pool,
 //    normalise, rotate, quantize and store the row.  Lane l holds
@@ -55,7 +55,7 @@ struct __align__(16) RowDesc {
 
 template <int RATIO, bool ROPE>
 struct StoreTile {
-  static constexpr int kRowsPerWarp = RATIO == 2 ? 1 : 2;
+  static constexpr int kRowsPerWarp = RATIO == 2 ? 1 : 4;   // 32 KB stages either way
   static constexpr int kRows = kConsumerWarps * kRowsPerWarp;      // rows per stage
   static constexpr int kInBytes = RATIO == 2 ? 4096 : 1024;        // kv0|s0|kv1|s1, or kv
   static constexpr int kRopeBytes = ROPE ? kRopeDim * 4 : 0;
