@@ -24,7 +24,7 @@
 //    source rows (one 4 KB copy for a ratio-2 pair in the fused layout) and
 //    of its RoPE row into a 3-stage shared-memory ring; an mbarrier per stage
 //    counts the bytes in flight;
-//  * eight consumer warps, each owning one row (ratio 2) or four (ratio 1) of
+//  * eight consumer warps, each owning one row (ratio 2) or 2-4 (ratio 1) of
 //    the stage: wait for the stage, pull the row into registers, release the
 //    slot, look up the destination (out_loc or the page table) and pool,
 //    normalise, rotate, quantize and store the row.  Lane l holds
@@ -53,9 +53,12 @@ struct __align__(16) RowDesc {
   int c;     // compressed index inside the request (the page-table index)
 };
 
-template <int RATIO, bool ROPE>
+// Rows per consumer warp per stage: one ratio-2 pair (4 KB), four ratio-1
+// rows when the row is only stored (32 KB stages either way), two ratio-1
+// rows with RMSNorm or RoPE (four would spill registers).
+template <int RATIO, bool NORM, bool ROPE>
 struct StoreTile {
-  static constexpr int kRowsPerWarp = RATIO == 2 ? 1 : 4;   // 32 KB stages either way
+  static constexpr int kRowsPerWarp = RATIO == 2 ? 1 : (NORM || ROPE ? 2 : 4);
   static constexpr int kRows = kConsumerWarps * kRowsPerWarp;      // rows per stage
   static constexpr int kInBytes = RATIO == 2 ? 4096 : 1024;        // kv0|s0|kv1|s1, or kv
   static constexpr int kRopeBytes = ROPE ? kRopeDim * 4 : 0;
@@ -209,7 +212,7 @@ __device__ __forceinline__ void load_row(const uint8_t* slot, int lane, RowIn<RA
   }
   if constexpr (ROPE) {
     if (lane >= 24) {
-      const float4* f = reinterpret_cast<const float4*>(slot + StoreTile<RATIO, ROPE>::kInBytes);
+      const float4* f = reinterpret_cast<const float4*>(slot + (RATIO == 2 ? 4096 : 1024));
       in.fr[0] = f[2 * (lane - 24)];
       in.fr[1] = f[2 * (lane - 24) + 1];
     }
@@ -373,7 +376,7 @@ __device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s
 template <int L, int RATIO, bool NORM, bool ROPE>
 __global__ void __launch_bounds__(kStoreThreads, 2)
 compress_store_kernel(const StoreParams p) {
-  using TL = StoreTile<RATIO, ROPE>;
+  using TL = StoreTile<RATIO, NORM, ROPE>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* s_stage = smem;
   RowDesc* s_desc = reinterpret_cast<RowDesc*>(smem + kStages * TL::kStageBytes);
@@ -497,7 +500,7 @@ compress_store_kernel(const StoreParams p) {
 
 template <int L, int RATIO, bool NORM, bool ROPE>
 static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
-  using TL = StoreTile<RATIO, ROPE>;
+  using TL = StoreTile<RATIO, NORM, ROPE>;
   auto kern = compress_store_kernel<L, RATIO, NORM, ROPE>;
   const size_t smem = (size_t)TL::kFixedSmem + sizeof(long long) * (size_t)(p.n_slots + 1)
                     + 2 * sizeof(int) * (size_t)p.n_slots;
