@@ -79,18 +79,28 @@ __device__ __forceinline__ long long rows_of_slot(int n, int p0) {
   return (((long long)p0 + n) >> 1) - ((long long)p0 >> 1);
 }
 
-// base[i] = sum_{r < i} rows_of_slot(r) for i in [0, n_slots]
+// The in-CTA plan: first[i], start[i] and base[i] = sum_{r < i} rows_of_slot(r)
+// for i in [0, n_slots] (base[n_slots] = total).  The global reads are one
+// coalesced pass with independent loads; the prefix then runs on shared
+// memory only (each thread scans a chunk, warps and the block combine).
 template <int RATIO>
-__device__ void block_scan_counts(const int* __restrict__ ext, const int* __restrict__ start_pos,
-                                  int n_slots, long long* base) {
+__device__ void block_plan(const int* __restrict__ ext, const int* __restrict__ start_pos,
+                           int n_slots, long long* base, int* first, int* start) {
   __shared__ long long s_warp[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nt = blockDim.x, nwarps = nt >> 5;
+  for (int i = tid; i < n_slots; i += nt) {
+    const int n = ext[n_slots + i];
+    const int p0 = start_pos ? start_pos[i] : 0;
+    first[i] = ext[i];
+    start[i] = p0;
+    base[i] = rows_of_slot<RATIO>(n, p0);
+  }
+  __syncthreads();
   const int per = (n_slots + nt - 1) / nt;
   const int beg = min(tid * per, n_slots), end = min(beg + per, n_slots);
   long long local = 0;
-  for (int i = beg; i < end; ++i)
-    local += rows_of_slot<RATIO>(ext[n_slots + i], start_pos ? start_pos[i] : 0);
+  for (int i = beg; i < end; ++i) local += base[i];
   long long v = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -110,9 +120,10 @@ __device__ void block_scan_counts(const int* __restrict__ ext, const int* __rest
   }
   __syncthreads();
   long long excl = v - local + (warp > 0 ? s_warp[warp - 1] : 0);
-  for (int i = beg; i < end; ++i) {
+  for (int i = beg; i < end; ++i) {   // in place: this thread's chunk only
+    const long long c = base[i];
     base[i] = excl;
-    excl += rows_of_slot<RATIO>(ext[n_slots + i], start_pos ? start_pos[i] : 0);
+    excl += c;
   }
   if (tid == nt - 1) base[n_slots] = excl;
 }
@@ -396,11 +407,7 @@ compress_store_kernel(const StoreParams p) {
     *s_abort = 0;
     mbar_fence_init();
   }
-  block_scan_counts<RATIO>(p.ext, p.start_pos, p.n_slots, s_base);
-  for (int i = threadIdx.x; i < p.n_slots; i += blockDim.x) {
-    s_first[i] = p.ext[i];
-    s_start[i] = p.start_pos ? p.start_pos[i] : 0;
-  }
+  block_plan<RATIO>(p.ext, p.start_pos, p.n_slots, s_base, s_first, s_start);
   __syncthreads();
   const long long total = s_base[p.n_slots];
   const long long n_tiles = ((long long)p.n_out + TL::kRows - 1) / TL::kRows;
