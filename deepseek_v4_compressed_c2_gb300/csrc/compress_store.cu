@@ -240,20 +240,24 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
     zero_row_outputs(p, k, lane);
     return;
   }
-  float x[16];
-  unpack_bf16x8(in.kv0[0], x);
-  unpack_bf16x8(in.kv0[1], x + 8);
+  // the lane's 16 values as 8 fp32 pairs: pairs 0..3 = dims 8l.., 4..7 =
+  // dims 256+8l..; every pair comes from one bf16 word
+  uint64_t x2[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) x2[q] = f2_from_bf16x2(word_of(in.kv0[q >> 2], q & 3));
   if constexpr (RATIO == 2) {
     // softmax over the pair: weight of the first = 1 / (1 + exp(s1 - s0));
     // x = k1 + (k0 - k1) * w0 (an ex2 overflow gives w0 = 0, i.e. x = k1)
-    float k1[16], a[16], b[16];
-    unpack_bf16x8(in.kv1[0], k1); unpack_bf16x8(in.kv1[1], k1 + 8);
-    unpack_bf16x8(in.s0[0], a);   unpack_bf16x8(in.s0[1], a + 8);
-    unpack_bf16x8(in.s1[0], b);   unpack_bf16x8(in.s1[1], b + 8);
+    const uint64_t log2e = f2(1.4426950408889634f, 1.4426950408889634f), one = f2(1.f, 1.f);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float w0 = rcp_approx(1.f + ex2_approx((b[i] - a[i]) * 1.4426950408889634f));
-      x[i] = fmaf(x[i] - k1[i], w0, k1[i]);
+    for (int q = 0; q < 8; ++q) {
+      const uint64_t k1 = f2_from_bf16x2(word_of(in.kv1[q >> 2], q & 3));
+      const uint64_t a = f2_from_bf16x2(word_of(in.s0[q >> 2], q & 3));
+      const uint64_t b = f2_from_bf16x2(word_of(in.s1[q >> 2], q & 3));
+      float t0, t1, d0, d1;
+      f2_split(f2_mul(f2_sub(b, a), log2e), t0, t1);
+      f2_split(f2_add(f2(ex2_approx(t0), ex2_approx(t1)), one), d0, d1);
+      x2[q] = f2_fma(f2_sub(x2[q], k1), f2(rcp_approx(d0), rcp_approx(d1)), k1);
     }
   }
   // RMSNorm: x_n = (x * w) * inv with inv = rsqrt(mean(x^2) + eps).  The
@@ -262,46 +266,54 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
   // quantizing the explicit x_n (see store_row_v41_scaled).
   float inv = 1.f;
   if constexpr (NORM) {
-    float ss[4] = {0.f, 0.f, 0.f, 0.f};
+    uint64_t acc[2] = {0ull, 0ull};     // partial sums of dims = 0,1 and 2,3 (mod 4)
 #pragma unroll
-    for (int i = 0; i < 16; ++i) ss[i & 3] = fmaf(x[i], x[i], ss[i & 3]);
-    float t = (ss[0] + ss[1]) + (ss[2] + ss[3]);
+    for (int q = 0; q < 8; ++q) acc[q & 1] = f2_fma(x2[q], x2[q], acc[q & 1]);
+    float s0, s1, s2, s3;
+    f2_split(acc[0], s0, s1);
+    f2_split(acc[1], s2, s3);
+    float t = (s0 + s1) + (s2 + s3);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFullMask, t, o);
     inv = rsqrtf(fmaf(t, 1.f / kDim, p.eps));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] *= w[i];
+    for (int q = 0; q < 8; ++q) x2[q] = f2_mul(x2[q], f2(w[2 * q], w[2 * q + 1]));
   }
+  const uint64_t inv2 = f2(inv, inv);
   if (p.latent_out) {  // post-norm, pre-RoPE
     float xn[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) xn[i] = x[i] * inv;
+    for (int q = 0; q < 8; ++q) f2_split(f2_mul(x2[q], inv2), xn[2 * q], xn[2 * q + 1]);
     uint4* o = reinterpret_cast<uint4*>(p.latent_out + k * kDim);
     o[lane] = pack_bf16x8(xn);
     o[32 + lane] = pack_bf16x8(xn + 8);
   }
   if constexpr (ROPE) {
-    // lanes 24..31 hold dims 448+8(l-24) .. +7 in x[8..15]: 4 complex pairs
+    // lanes 24..31 hold dims 448+8(l-24) .. +7 in pairs 4..7: 4 complex
+    // pairs (a, b) rotated by (c, s): (a c - b s, a s + b c)
     if (lane >= 24) {
       const float f[8] = {in.fr[0].x, in.fr[0].y, in.fr[0].z, in.fr[0].w,
                           in.fr[1].x, in.fr[1].y, in.fr[1].z, in.fr[1].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float c = f[2 * q], s = f[2 * q + 1];
-        const float a = x[8 + 2 * q], b = x[9 + 2 * q];
-        x[8 + 2 * q] = fmaf(a, c, -b * s);
-        x[9 + 2 * q] = fmaf(a, s, b * c);
+        const float c = f[2 * q], sn = f[2 * q + 1];
+        float a, b;
+        f2_split(x2[4 + q], a, b);
+        const uint64_t bsc = f2_mul(f2(b, b), f2(-sn, c));          // (-b s, b c)
+        x2[4 + q] = f2_fma(f2(a, a), f2(c, sn), bsc);
       }
     }
   }
+  float x[16];
   const bool store = slot > 0 && slot < p.pool_rows;
   if (slot != 0 && !store && lane == 0 && p.err) atomicAdd(p.err, 1);   // destination fault
   if (p.prequant_out || L != kV41 || !NORM) {
-    // explicit pre-quant row (debug output, FP4, or no norm: inv == 1)
+    // explicit pre-quant row (debug output, FP4, V4, or no norm: inv == 1)
     if constexpr (NORM) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] *= inv;
+      for (int q = 0; q < 8; ++q) x2[q] = f2_mul(x2[q], inv2);
     }
+    f2_unpack16(x2, x);
     if (p.prequant_out) {
       float4* o = reinterpret_cast<float4*>(p.prequant_out + k * kDim);
       o[2 * lane] = make_float4(x[0], x[1], x[2], x[3]);
@@ -311,6 +323,7 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
     }
     if (store) store_row_split<L>(x, PagedKV<L>{p.pool, p.page_bits}.row(slot), lane);
   } else if (store) {
+    f2_unpack16(x2, x);
     store_row_v41_scaled(x, inv, PagedKV<kV41>{p.pool, p.page_bits}.row(slot), lane);
   }
 }
