@@ -505,3 +505,40 @@ def test_fp4_quotient_matches_ieee_division_for_every_scale(B):
     torch.cuda.synchronize()
     bad = q_fast.view(torch.int32) != q_ieee.view(torch.int32)
     assert int(bad.sum()) == 0, f"{int(bad.sum())} quotients differ, e.g. {x[bad][:4].tolist()}"
+
+
+@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4, oracle.V4])
+def test_guard_regions_around_pool_output_and_ring_stay_untouched(B, layout):
+    """The pool, the gathered output and the ring sit inside larger buffers
+    whose guard regions are sentinel-filled; no call writes outside its
+    buffers (slots and ids include the first and last rows and out-of-range
+    values)."""
+    rb = oracle.row_bytes(layout)
+    G = 1 << 16                                           # guard bytes each side
+    cfg = dict(W.decode_verify(seed=21, n_req=48, n_new=5, ring_size=4, max_prefix=256),
+               layout=layout)
+    pool_bytes = cfg["pool_rows"] * rb
+    big = torch.full((pool_bytes + 2 * G,), 0x5C, dtype=torch.uint8, device="cuda")
+    pool = big[G:G + pool_bytes]
+    ring_big = torch.full((cfg["ring"].size + 2 * G,), 0x1234, dtype=torch.int16, device="cuda")
+    ring = ring_big[G:G + cfg["ring"].size].view(torch.bfloat16).view(cfg["ring"].shape)
+    ring.copy_(dev_bf16(cfg["ring"]))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # slots: the plan's, plus the pool's last row and out-of-range values
+    p = oracle.plan(2, cfg["ext"], cfg["page_table"], cfg["page_bits"], start_pos=cfg["start_pos"])
+    out_loc = p["slot"].astype(np.int32).copy()
+    out_loc[:3] = [cfg["pool_rows"] - 1, cfg["pool_rows"], -1]
+    B.dsv4kv_compress_store(layout, 2, dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
+                            page_table=dev(cfg["page_table"]), page_bits=cfg["page_bits"],
+                            rmsnorm_w=dev_bf16(cfg["norm_w"]), eps=cfg["eps"],
+                            freqs_cis=dev(cfg["freqs"]), out_loc=dev(out_loc),
+                            err_word=err, start_pos=dev(cfg["start_pos"]), ring=ring)
+    ids = np.array([0, cfg["pool_rows"] - 1, cfg["pool_rows"], -5, 1 << 30, 7], np.int32)
+    out_big = torch.full(((len(ids) + 2) * 512,), 0x3A3A, dtype=torch.int16, device="cuda")
+    out = out_big[512:512 + len(ids) * 512].view(torch.bfloat16).view(len(ids), 512)
+    B.dsv4kv_dequant_gather(layout, pool, dev(ids), out, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 2 + 2                       # two bad slots, two bad ids
+    assert bool((big[:G] == 0x5C).all()) and bool((big[G + pool_bytes:] == 0x5C).all())
+    assert bool((ring_big[:G] == 0x1234).all()) and bool((ring_big[G + cfg["ring"].size:] == 0x1234).all())
+    assert bool((out_big[:512] == 0x3A3A).all()) and bool((out_big[512 + len(ids) * 512:] == 0x3A3A).all())
