@@ -42,9 +42,13 @@ constexpr int kConsumerWarps = 8;
 constexpr int kStages = 3;
 constexpr int kStoreThreads = (kConsumerWarps + 1) * 32;
 
-// kRowRing: the pair's first token is in the ring; the per-request ring phase
-// computes that row (after the tiles), not the tile consumers.
-enum RowState : int { kRowNone = 0, kRowPad = 1, kRowBad = 2, kRowOk = 3, kRowRing = 4 };
+// kRowOkRing: the pair's first token is in the ring and the producer copies
+// the ring entry into the stage like any row.  kRowRing: the same, but the
+// request's step is long enough (n >= 2R) for its ring update to reuse that
+// entry, so the per-request ring phase computes the row (read before write,
+// in one warp) and the tiles skip it.
+enum RowState : int { kRowNone = 0, kRowPad = 1, kRowBad = 2, kRowOk = 3, kRowRing = 4,
+                      kRowOkRing = 5 };
 
 struct __align__(16) RowDesc {
   int state;
@@ -79,13 +83,13 @@ __device__ __forceinline__ long long rows_of_slot(int n, int p0) {
   return (((long long)p0 + n) >> 1) - ((long long)p0 >> 1);
 }
 
-// The in-CTA plan: first[i], start[i] and base[i] = sum_{r < i} rows_of_slot(r)
+// The in-CTA plan: first[i], start[i], count[i] and base[i] = sum_{r < i} rows_of_slot(r)
 // for i in [0, n_slots] (base[n_slots] = total).  The global reads are one
 // coalesced pass with independent loads; the prefix then runs on shared
 // memory only (each thread scans a chunk, warps and the block combine).
 template <int RATIO>
 __device__ void block_plan(const int* __restrict__ ext, const int* __restrict__ start_pos,
-                           int n_slots, long long* base, int* first, int* start) {
+                           int n_slots, long long* base, int* first, int* start, int* count) {
   __shared__ long long s_warp[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nt = blockDim.x, nwarps = nt >> 5;
@@ -94,6 +98,7 @@ __device__ void block_plan(const int* __restrict__ ext, const int* __restrict__ 
     const int p0 = start_pos ? start_pos[i] : 0;
     first[i] = ext[i];
     start[i] = p0;
+    count[i] = n;
     base[i] = rows_of_slot<RATIO>(n, p0);
   }
   __syncthreads();
@@ -136,7 +141,8 @@ __device__ void block_plan(const int* __restrict__ ext, const int* __restrict__ 
 template <int RATIO, bool ROPE>
 __device__ __forceinline__ RowDesc plan_row(const StoreParams& p, long long k, long long total,
                                             const long long* s_base, const int* s_first,
-                                            const int* s_start, long long& src) {
+                                            const int* s_start, const int* s_count,
+                                            long long& src) {
   RowDesc d;
   d.state = kRowNone; d.pos = 0; d.r = 0; d.c = 0;
   src = 0;
@@ -155,7 +161,11 @@ __device__ __forceinline__ RowDesc plan_row(const StoreParams& p, long long k, l
   d.pos = (int)pos;
   src = (long long)s_first[lo] + (pos - p0);
   if (pos < p0) {                                  // first token in the ring
-    d.state = kRowRing;
+    if (p.ring == nullptr) { d.state = kRowBad; return d; }
+    if (s_count[lo] >= 2LL * p.ring_size) { d.state = kRowRing; return d; }
+    const long long first = s_first[lo];
+    const bool ok = first >= 0 && first + 1 <= p.n_rows && pos >= 0 && (!ROPE || pos < p.max_pos);
+    d.state = ok ? kRowOkRing : kRowBad;
     return d;
   }
   const bool ok = src >= 0 && src + RATIO <= p.n_rows && pos >= 0 && (!ROPE || pos < p.max_pos);
@@ -235,7 +245,7 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
                                             long long slot, const RowIn<RATIO, ROPE>& in,
                                             const float (&w)[16], int lane) {
   if (d.state == kRowNone || d.state == kRowRing) return;
-  if (d.state != kRowOk) {
+  if (d.state != kRowOk && d.state != kRowOkRing) {
     if (d.state == kRowBad && lane == 0 && p.err) atomicAdd(p.err, 1);
     zero_row_outputs(p, k, lane);
     return;
@@ -329,12 +339,15 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
 }
 
 // Per-request ring work (ratio 2), one warp per request slot, in program
-// order: (1) the pair whose first token precedes p0 -- token p0 - 1 from the
-// ring entry ((p0 - 1) / 2) % R, token p0 from the first new row -- then
-// (2) the ring update: each even-position new token among the last 2R
-// positions of the step goes to entry (q / 2) % R.  A lane writes exactly the
-// 16-byte words it read, so the read of (1) precedes any write of the same
-// entry; no other warp touches this request's ring.
+// order: (1) for a request whose step has n >= 2R new tokens, the pair whose
+// first token precedes p0 -- token p0 - 1 from the ring entry
+// ((p0 - 1) / 2) % R, token p0 from the first new row -- then (2) the ring
+// update: each even-position new token among the last 2R positions of the
+// step goes to entry (q / 2) % R.  A lane writes exactly the 16-byte words it
+// read, so the read of (1) precedes any write of the same entry.  With
+// n < 2R the entries written are (p0+1)/2 .. (p0+n-1)/2, all different from
+// the read entry (p0-1)/2 modulo R, so the tile path may read that entry
+// concurrently.  No other warp writes this request's ring.
 template <int L, bool NORM, bool ROPE>
 __device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s_base,
                                         const int* s_first, const int* s_start,
@@ -348,10 +361,12 @@ __device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s
     const long long first = s_first[r];
     if (n <= 0) continue;
     const long long k = s_base[r];
-    if ((p0 & 1) && k < p.n_out) {
+    // the ring row goes through the tiles unless the ring update of this
+    // step may reuse its entry (n >= 2R); without a ring it is a tile fault
+    if ((p0 & 1) && k < p.n_out && p.ring != nullptr && n >= 2LL * p.ring_size) {
       RowDesc d;
       d.r = (int)r; d.c = (int)(p0 >> 1); d.pos = (int)(p0 - 1);
-      const bool ok = p.ring != nullptr && p0 >= 1 && first >= 0 && first + 1 <= p.n_rows &&
+      const bool ok = p0 >= 1 && first >= 0 && first + 1 <= p.n_rows &&
                       (!ROPE || d.pos < p.max_pos);
       d.state = ok ? kRowOk : kRowBad;
       RowIn<2, ROPE> in;
@@ -410,6 +425,7 @@ compress_store_kernel(const StoreParams p) {
   long long* s_base = reinterpret_cast<long long*>(smem + TL::kFixedSmem);
   int* s_first = reinterpret_cast<int*>(s_base + p.n_slots + 1);
   int* s_start = s_first + p.n_slots;
+  int* s_count = s_start + p.n_slots;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -420,7 +436,7 @@ compress_store_kernel(const StoreParams p) {
     *s_abort = 0;
     mbar_fence_init();
   }
-  block_plan<RATIO>(p.ext, p.start_pos, p.n_slots, s_base, s_first, s_start);
+  block_plan<RATIO>(p.ext, p.start_pos, p.n_slots, s_base, s_first, s_start, s_count);
   __syncthreads();
   const long long total = s_base[p.n_slots];
   const long long n_tiles = ((long long)p.n_out + TL::kRows - 1) / TL::kRows;
@@ -441,20 +457,34 @@ compress_store_kernel(const StoreParams p) {
       d.state = kRowNone;
       long long src = 0;
       if (lane < TL::kRows) {
-        d = plan_row<RATIO, ROPE>(p, tile * TL::kRows + lane, total, s_base, s_first, s_start, src);
+        d = plan_row<RATIO, ROPE>(p, tile * TL::kRows + lane, total, s_base, s_first, s_start,
+                                  s_count, src);
         s_desc[s * TL::kRows + lane] = d;
       }
-      uint32_t bytes = d.state == kRowOk ? (uint32_t)TL::kSlotBytes : 0u;
+      const bool copy = d.state == kRowOk || d.state == kRowOkRing;
+      uint32_t bytes = copy ? (uint32_t)TL::kSlotBytes : 0u;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(kFullMask, bytes, o);
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&s_full[s], bytes);
       __syncwarp();
-      if (d.state == kRowOk) {
+      if (copy) {
         uint8_t* dst = s_stage + s * TL::kStageBytes + lane * TL::kSlotBytes;
-        const __nv_bfloat16* r0 = p.rows + src * p.row_stride;
+        const __nv_bfloat16* r0 = p.rows + (d.state == kRowOkRing ? 0 : src) * p.row_stride;
         if constexpr (RATIO == 2) {
-          if (fused_pair) {
+          if (d.state == kRowOkRing) {
+            // token p0 - 1 from the ring (kv | score, 2 KB), token p0 = row src + 1
+            const __nv_bfloat16* e =
+                p.ring + ((long long)d.r * p.ring_size + (d.c % p.ring_size)) * (2 * kDim);
+            const __nv_bfloat16* r1 = p.rows + (src + 1) * p.row_stride;
+            bulk_g2s(dst, e, 2048, &s_full[s], pol);
+            if (fused_pair) {
+              bulk_g2s(dst + 2048, r1, 2048, &s_full[s], pol);
+            } else {
+              bulk_g2s(dst + 2048, r1, 1024, &s_full[s], pol);
+              bulk_g2s(dst + 3072, score_base + (src + 1) * sstride, 1024, &s_full[s], pol);
+            }
+          } else if (fused_pair) {
             bulk_g2s(dst, r0, 4096, &s_full[s], pol);             // kv0|s0|kv1|s1
           } else {
             const __nv_bfloat16* c0 = score_base + src * sstride;
@@ -499,9 +529,9 @@ compress_store_kernel(const StoreParams p) {
       for (int q = 0; q < TL::kRowsPerWarp; ++q) {
         const int t = warp * TL::kRowsPerWarp + q;
         d[q] = s_desc[s * TL::kRows + t];
-        slot[q] = d[q].state == kRowOk ? dest_slot(p, tile * TL::kRows + t, d[q]) : 0;
-        if (d[q].state == kRowOk)
-          load_row<RATIO, ROPE>(s_stage + s * TL::kStageBytes + t * TL::kSlotBytes, lane, in[q]);
+        const bool ok = d[q].state == kRowOk || d[q].state == kRowOkRing;
+        slot[q] = ok ? dest_slot(p, tile * TL::kRows + t, d[q]) : 0;
+        if (ok) load_row<RATIO, ROPE>(s_stage + s * TL::kStageBytes + t * TL::kSlotBytes, lane, in[q]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[s]);
@@ -523,14 +553,14 @@ static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
   using TL = StoreTile<RATIO, NORM, ROPE>;
   auto kern = compress_store_kernel<L, RATIO, NORM, ROPE>;
   const size_t smem = (size_t)TL::kFixedSmem + sizeof(long long) * (size_t)(p.n_slots + 1)
-                    + 2 * sizeof(int) * (size_t)p.n_slots;
+                    + 3 * sizeof(int) * (size_t)p.n_slots;
   static int attr_set_for_device[64] = {0};  // the largest size any call can need, once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !attr_set_for_device[dev]) {
     const size_t max_smem = (size_t)TL::kFixedSmem + sizeof(long long) * (kMaxSlots + 1)
-                          + 2 * sizeof(int) * kMaxSlots;
+                          + 3 * sizeof(int) * kMaxSlots;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set_for_device[dev] = 1;
