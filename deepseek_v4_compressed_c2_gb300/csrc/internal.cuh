@@ -82,7 +82,7 @@ cudaError_t launch_fp4_quotient_selftest(const float* x, const unsigned char* sc
                                          long long n, float* q_fast, float* q_ieee,
                                          cudaStream_t stream);
 
-// SM count and resident blocks per SM for a kernel, for persistent grids.
+// Multiprocessor count of the current device (cached), for persistent grids.
 int device_sm_count();
 
 }  // namespace dsv4kv
