@@ -275,8 +275,12 @@ def cold_gather(B, dev, stream, reps):
 
 def decode_verify_steps(B, dev, stream, reps=50):
     """The ring form of the compressor on decode-shaped steps (one new token
-    per request; 1 + 3 draft tokens per request), timed per launch.  These
-    are small, latency-bound launches (working set in L2)."""
+    per request; 1 + 3 draft tokens per request).  These are small,
+    latency-bound launches (working set in L2).  The serving loop runs them
+    inside a CUDA graph whose offsets are refreshed in place, so the device
+    time per launch is taken from a captured graph of `reps` launches; the
+    eager figure (one prepared C-ABI call per launch from Python) is kept
+    beside it and includes the host's launch cost."""
     import torch
     from deepseek_v4_compressed_c2_gb300 import workloads as W
     res = {}
@@ -287,25 +291,39 @@ def decode_verify_steps(B, dev, stream, reps=50):
         ring = bf(cfg["ring"])
         err = torch.zeros(1, dtype=torch.int32, device=dev)
         rows = bf(cfg["rows"])
-        args_ = dict(page_table=torch.from_numpy(cfg["page_table"]).to(dev), page_bits=6,
-                     rmsnorm_w=bf(cfg["norm_w"]), eps=cfg["eps"],
-                     freqs_cis=torch.from_numpy(cfg["freqs"]).to(dev), n_out=cfg["n_out"],
-                     err_word=err, stream=stream,
-                     start_pos=torch.from_numpy(cfg["start_pos"]).to(dev), ring=ring)
         ext = torch.from_numpy(cfg["ext"]).to(dev)
         with torch.cuda.stream(stream):
+            call = B.prepare_compress_store(
+                1, 2, rows, ext, pool, page_table=torch.from_numpy(cfg["page_table"]).to(dev),
+                page_bits=6, rmsnorm_w=bf(cfg["norm_w"]), eps=cfg["eps"],
+                freqs_cis=torch.from_numpy(cfg["freqs"]).to(dev), n_out=cfg["n_out"],
+                err_word=err, stream=stream, start_pos=torch.from_numpy(cfg["start_pos"]).to(dev),
+                ring=ring)
             for _ in range(5):
-                B.dsv4kv_compress_store(1, 2, rows, ext, pool, **args_)
+                call()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for _ in range(reps):
-                B.dsv4kv_compress_store(1, 2, rows, ext, pool, **args_)
+                call()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        eager_us = a.elapsed_time(b) * 1e3 / reps
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(reps):
+                call()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+            a.record(stream)
+            graph.replay()
             b.record(stream)
         torch.cuda.synchronize(dev)
         assert int(err.item()) == 0
         us = a.elapsed_time(b) * 1e3 / reps
-        res[name] = {"us_per_launch": us, "rows": cfg["n_out"], "tokens": n_req * n_new,
-                     "rows_per_s": cfg["n_out"] / (us / 1e6)}
+        res[name] = {"us_per_launch": us, "eager_us_per_launch": eager_us, "rows": cfg["n_out"],
+                     "tokens": n_req * n_new, "rows_per_s": cfg["n_out"] / (us / 1e6)}
+        del graph
     return res
 
 

@@ -375,28 +375,37 @@ class PreparedCall:
 def prepare_compress_store(layout, ratio, rows, extend_offsets, pool, *, score=None,
                            page_table=None, page_bits=0, rmsnorm_w=None, eps=1e-6,
                            freqs_cis=None, out_loc=None, n_out=None, pool_rows=None,
-                           latent_out=None, prequant_out=None, err_word=None, stream=None):
-    """dsv4kv_compress_store with its arguments marshalled once."""
+                           latent_out=None, prequant_out=None, err_word=None, stream=None,
+                           start_pos=None, ring=None):
+    """dsv4kv_compress_store (or, with start_pos / ring, the _ring entry) with
+    its arguments marshalled once.  The checked first call below runs the
+    launch once (a ring step advances the ring)."""
     if n_out is None:
         n_out = out_loc.numel()
     if pool_rows is None:
         pool_rows = pool.numel() * pool.element_size() // _ROW_BYTES.get(layout, 1)
-    args = (layout, ratio, _ptr(rows), rows.shape[0], rows.stride(0), _ptr(score),
+    head = (layout, ratio, _ptr(rows), rows.shape[0], rows.stride(0), _ptr(score),
             0 if score is None else score.stride(0), _ptr(extend_offsets),
-            extend_offsets.shape[1], _ptr(page_table),
-            0 if page_table is None else page_table.shape[1], page_bits, _ptr(rmsnorm_w), eps,
-            _ptr(freqs_cis), 0 if freqs_cis is None else freqs_cis.shape[0], _ptr(out_loc),
-            n_out, _ptr(pool), pool_rows, _ptr(latent_out), _ptr(prequant_out), _ptr(err_word),
-            _stream(stream))
+            extend_offsets.shape[1])
+    tail = (_ptr(page_table), 0 if page_table is None else page_table.shape[1], page_bits,
+            _ptr(rmsnorm_w), eps, _ptr(freqs_cis), 0 if freqs_cis is None else freqs_cis.shape[0],
+            _ptr(out_loc), n_out, _ptr(pool), pool_rows, _ptr(latent_out), _ptr(prequant_out),
+            _ptr(err_word), _stream(stream))
+    use_ring = start_pos is not None or ring is not None
+    if use_ring:
+        name = "dsv4kv_compress_store_ring"
+        args = head + (_ptr(start_pos), _ptr(ring), 0 if ring is None else ring.shape[1]) + tail
+    else:
+        name, args = "dsv4kv_compress_store", head + tail
     # one checked call validates shapes through the same path as the plain binding
     dsv4kv_compress_store(layout, ratio, rows, extend_offsets, pool, score=score,
                           page_table=page_table, page_bits=page_bits, rmsnorm_w=rmsnorm_w,
                           eps=eps, freqs_cis=freqs_cis, out_loc=out_loc, n_out=n_out,
                           pool_rows=pool_rows, latent_out=latent_out, prequant_out=prequant_out,
-                          err_word=err_word, stream=stream)
-    return PreparedCall("dsv4kv_compress_store", args,
+                          err_word=err_word, stream=stream, start_pos=start_pos, ring=ring)
+    return PreparedCall(name, args,
                         (rows, extend_offsets, pool, score, page_table, rmsnorm_w, freqs_cis,
-                         out_loc, latent_out, prequant_out, err_word))
+                         out_loc, latent_out, prequant_out, err_word, start_pos, ring))
 
 
 def prepare_topk_to_slots(topk, token_to_req, page_table, page_bits, slots, lens, *,

@@ -32,6 +32,8 @@
 //    conflict-free and every global store of a row half is one contiguous
 //    warp access.
 //  All waits are bounded (see tma.cuh).
+#include <atomic>
+
 #include "internal.cuh"
 #include "quant.cuh"
 #include "tma.cuh"
@@ -84,61 +86,104 @@ __device__ __forceinline__ long long rows_of_slot(int n, int p0) {
 }
 
 // The in-CTA plan: first[i], start[i], count[i] and base[i] = sum_{r < i} rows_of_slot(r)
-// for i in [0, n_slots] (base[n_slots] = total).  The global reads are one
-// coalesced pass with independent loads; the prefix then runs on shared
-// memory only (each thread scans a chunk, warps and the block combine).
-template <int RATIO>
-__device__ void block_plan(const int* __restrict__ ext, const int* __restrict__ start_pos,
-                           int n_slots, long long* base, int* first, int* start, int* count) {
-  __shared__ long long s_warp[32];
+// for i in [0, n_slots] (base[n_slots] = total).  Pass 1 reads the slot
+// arrays in one coalesced sweep whose loads are all issued before any is
+// used (kPlanBatch slots per thread per sweep) and leaves each slot's row
+// count in base[i].  Pass 2 gives thread t the PER consecutive slots
+// [t * PER, (t + 1) * PER): their counts go to registers in one unrolled
+// burst of shared-memory loads, the thread scans them in registers, one
+// shuffle scan per warp and one pass over the warps' totals add the
+// offsets, and the exclusive prefix is written back in place.
+constexpr int kPlanBatch = 16;
+constexpr int kPlanMaxPer = (kMaxSlots + kStoreThreads - 1) / kStoreThreads;
+
+template <int RATIO, int PER>
+__device__ __forceinline__ void block_plan_per(const int* __restrict__ ext,
+                                               const int* __restrict__ start_pos, int n_slots,
+                                               long long* base, int* first, int* start,
+                                               int* count, long long* s_warp) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nt = blockDim.x, nwarps = nt >> 5;
-  for (int i = tid; i < n_slots; i += nt) {
-    const int n = ext[n_slots + i];
-    const int p0 = start_pos ? start_pos[i] : 0;
-    first[i] = ext[i];
-    start[i] = p0;
-    count[i] = n;
-    base[i] = rows_of_slot<RATIO>(n, p0);
+  for (int i0 = tid; i0 < n_slots; i0 += kPlanBatch * nt) {
+    int f[kPlanBatch], n[kPlanBatch], p0[kPlanBatch];
+#pragma unroll
+    for (int u = 0; u < kPlanBatch; ++u) {
+      const int i = i0 + u * nt;
+      f[u] = 0; n[u] = 0; p0[u] = 0;
+      if (i < n_slots) {
+        f[u] = __ldg(ext + i);
+        n[u] = __ldg(ext + n_slots + i);
+        if (start_pos) p0[u] = __ldg(start_pos + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPlanBatch; ++u) {
+      const int i = i0 + u * nt;
+      if (i < n_slots) {
+        first[i] = f[u];
+        start[i] = p0[u];
+        count[i] = n[u];
+        base[i] = rows_of_slot<RATIO>(n[u], p0[u]);
+      }
+    }
   }
   __syncthreads();
-  const int per = (n_slots + nt - 1) / nt;
-  const int beg = min(tid * per, n_slots), end = min(beg + per, n_slots);
-  long long local = 0;
-  for (int i = beg; i < end; ++i) local += base[i];
-  long long v = local;
+  const int beg = tid * PER;
+  long long v[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) v[u] = beg + u < n_slots ? base[beg + u] : 0;
+  long long run = 0;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const long long c = v[u];
+    v[u] = run;
+    run += c;
+  }
+  long long incl = run;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const long long t = __shfl_up_sync(kFullMask, v, o);
-    if (lane >= o) v += t;
+    const long long t = __shfl_up_sync(kFullMask, incl, o);
+    if (lane >= o) incl += t;
   }
-  if (lane == 31) s_warp[warp] = v;
+  if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    long long wv = lane < nwarps ? s_warp[lane] : 0;
+  long long off = incl - run, total = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    const long long t = s_warp[w];
+    if (w < warp) off += t;
+    total += t;
+  }
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long t = __shfl_up_sync(kFullMask, wv, o);
-      if (lane >= o) wv += t;
-    }
-    s_warp[lane] = wv;
-  }
-  __syncthreads();
-  long long excl = v - local + (warp > 0 ? s_warp[warp - 1] : 0);
-  for (int i = beg; i < end; ++i) {   // in place: this thread's chunk only
-    const long long c = base[i];
-    base[i] = excl;
-    excl += c;
-  }
-  if (tid == nt - 1) base[n_slots] = excl;
+  for (int u = 0; u < PER; ++u)
+    if (beg + u < n_slots) base[beg + u] = off + v[u];
+  if (tid == 0) base[n_slots] = total;
+}
+
+// n_slots <= kMaxSlots (checked by the host) needs at most kPlanMaxPer slots
+// per thread; small plans take a short unrolled form.
+template <int RATIO>
+__device__ __noinline__ void block_plan(const int* __restrict__ ext, const int* __restrict__ start_pos,
+                                        int n_slots, long long* base, int* first, int* start,
+                                        int* count) {
+  static_assert(kPlanMaxPer * kStoreThreads >= kMaxSlots, "the chunks cover every slot");
+  __shared__ long long s_warp[32];
+  const int per = (n_slots + (int)blockDim.x - 1) / (int)blockDim.x;
+  if (per <= 1)
+    block_plan_per<RATIO, 1>(ext, start_pos, n_slots, base, first, start, count, s_warp);
+  else if (per <= 4)
+    block_plan_per<RATIO, 4>(ext, start_pos, n_slots, base, first, start, count, s_warp);
+  else
+    block_plan_per<RATIO, kPlanMaxPer>(ext, start_pos, n_slots, base, first, start, count,
+                                       s_warp);
 }
 
 // The plan for output row k (shared memory only, no global loads): request
 // slot r (last slot whose prefix <= k), row j = k - base[r] of the request,
 // compressed index c = c_lo + j (c_lo = p0 for ratio 1, p0 / 2 for ratio 2),
 // first token at position RATIO*c in source row first_r + RATIO*c - p0, or in
-// the ring when that position precedes p0.
-template <int RATIO, bool ROPE>
+// the ring when that position precedes p0 (only with start positions at
+// ratio 2, RING).
+template <int RATIO, bool ROPE, bool RING>
 __device__ __forceinline__ RowDesc plan_row(const StoreParams& p, long long k, long long total,
                                             const long long* s_base, const int* s_first,
                                             const int* s_start, const int* s_count,
@@ -160,7 +205,7 @@ __device__ __forceinline__ RowDesc plan_row(const StoreParams& p, long long k, l
   d.c = (int)c;
   d.pos = (int)pos;
   src = (long long)s_first[lo] + (pos - p0);
-  if (pos < p0) {                                  // first token in the ring
+  if (RING && pos < p0) {                          // first token in the ring
     if (p.ring == nullptr) { d.state = kRowBad; return d; }
     if (s_count[lo] >= 2LL * p.ring_size) { d.state = kRowRing; return d; }
     const long long first = s_first[lo];
@@ -338,25 +383,34 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
   }
 }
 
-// Per-request ring work (ratio 2), one warp per request slot, in program
-// order: (1) for a request whose step has n >= 2R new tokens, the pair whose
-// first token precedes p0 -- token p0 - 1 from the ring entry
-// ((p0 - 1) / 2) % R, token p0 from the first new row -- then (2) the ring
-// update: each even-position new token among the last 2R positions of the
-// step goes to entry (q / 2) % R.  A lane writes exactly the 16-byte words it
-// read, so the read of (1) precedes any write of the same entry.  With
-// n < 2R the entries written are (p0+1)/2 .. (p0+n-1)/2, all different from
-// the read entry (p0-1)/2 modulo R, so the tile path may read that entry
-// concurrently.  No other warp writes this request's ring.
+// Per-request ring work (ratio 2).  Each warp owns the request slots
+// r = warp id + i * (warps in the grid) and makes two passes over them:
+// (1) for a request whose step has n >= 2R new tokens, the pair whose first
+// token precedes p0 -- token p0 - 1 from the ring entry ((p0 - 1) / 2) % R,
+// token p0 from the first new row; (2) the ring update: each even-position
+// new token among the last 2R positions of the step goes to entry
+// (q / 2) % R.  A lane writes exactly the 16-byte words it read, and pass (1)
+// ends before pass (2) starts, so every read of (1) precedes any write of the
+// same entry.  With n < 2R the entries written are (p0+1)/2 .. (p0+n-1)/2,
+// all different from the read entry (p0-1)/2 modulo R, so the tile path may
+// read that entry at any time.  No other warp writes this request's ring,
+// and no tile reads an entry that this phase writes, so the consumers run it
+// before their tile loop, while the producer's first copies are in flight.
 template <int L, bool NORM, bool ROPE>
 __device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s_base,
                                         const int* s_first, const int* s_start,
-                                        const float (&w)[16], int warp, int lane) {
+                                        const int* s_count, int warp, int lane) {
+  float w[16];
+  if constexpr (NORM) {
+    const uint4* wp = reinterpret_cast<const uint4*>(p.norm_w);
+    unpack_bf16x8(__ldg(wp + lane), w);
+    unpack_bf16x8(__ldg(wp + 32 + lane), w + 8);
+  }
   const __nv_bfloat16* score_base = p.score ? p.score : p.rows + kDim;
   const long long sstride = p.score ? p.score_stride : p.row_stride;
   for (long long r = (long long)blockIdx.x * kConsumerWarps + warp; r < p.n_slots;
        r += (long long)gridDim.x * kConsumerWarps) {
-    const int n = p.ext[p.n_slots + r];
+    const int n = s_count[r];
     const long long p0 = s_start[r];
     const long long first = s_first[r];
     if (n <= 0) continue;
@@ -391,28 +445,109 @@ __device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s
       }
       process_row<L, 2, NORM, ROPE>(p, k, d, slot, in, w, lane);
     }
-    if (p.ring != nullptr) {
-      long long q = p0 + n - 2LL * p.ring_size;
-      if (q < p0) q = p0;
-      for (; q < p0 + n; ++q) {
-        if (q & 1) continue;
-        const long long row = first + (q - p0);
-        if (row < 0 || row >= p.n_rows) {
-          if (lane == 0 && p.err) atomicAdd(p.err, 1);
-          continue;
+  }
+  if (p.ring == nullptr) return;
+  __syncwarp();
+  // (2) the ring update.  The warp takes its requests kRingBatch at a time and
+  // their t-th ring tokens together, so up to kRingBatch copies are in flight
+  // per round trip; all the entries of one round are distinct.
+  constexpr int kRingBatch = 4;
+  const long long stride = (long long)gridDim.x * kConsumerWarps;
+  for (long long r0 = (long long)blockIdx.x * kConsumerWarps + warp; r0 < p.n_slots;
+       r0 += kRingBatch * stride) {
+    long long qlo[kRingBatch], qhi[kRingBatch];
+    long long tokens = 0;
+#pragma unroll
+    for (int j = 0; j < kRingBatch; ++j) {
+      const long long r = r0 + j * stride;
+      qlo[j] = 0;
+      qhi[j] = 0;
+      if (r < p.n_slots && s_count[r] > 0) {
+        const long long p0 = s_start[r], n = s_count[r];
+        long long q = p0 + n - 2LL * p.ring_size;
+        if (q < p0) q = p0;
+        qlo[j] = q + (q & 1);      // the first even position
+        qhi[j] = p0 + n;
+        const long long t = qhi[j] > qlo[j] ? (qhi[j] - qlo[j] + 1) >> 1 : 0;
+        tokens = t > tokens ? t : tokens;
+      }
+    }
+    for (long long t = 0; t < tokens; ++t) {
+      uint4 v[kRingBatch][4];
+      bool ok[kRingBatch];
+#pragma unroll
+      for (int j = 0; j < kRingBatch; ++j) {
+        const long long r = r0 + j * stride;
+        const long long q = qlo[j] + 2 * t;
+        ok[j] = false;
+        if (q < qhi[j]) {
+          const long long row = s_first[r] + (q - s_start[r]);
+          if (row < 0 || row >= p.n_rows) {
+            if (lane == 0 && p.err) atomicAdd(p.err, 1);
+          } else {
+            ok[j] = true;
+            const uint4* kv = reinterpret_cast<const uint4*>(p.rows + row * p.row_stride);
+            const uint4* sc = reinterpret_cast<const uint4*>(score_base + row * sstride);
+            v[j][0] = kv[lane]; v[j][1] = kv[32 + lane]; v[j][2] = sc[lane]; v[j][3] = sc[32 + lane];
+          }
         }
+      }
+#pragma unroll
+      for (int j = 0; j < kRingBatch; ++j) {
+        if (!ok[j]) continue;
+        const long long r = r0 + j * stride;
+        const long long q = qlo[j] + 2 * t;
         uint4* e = reinterpret_cast<uint4*>(
             p.ring + ((r * p.ring_size) + ((q >> 1) % p.ring_size)) * (2 * kDim));
-        const uint4* kv = reinterpret_cast<const uint4*>(p.rows + row * p.row_stride);
-        const uint4* sc = reinterpret_cast<const uint4*>(score_base + row * sstride);
-        const uint4 a = kv[lane], b = kv[32 + lane], c = sc[lane], dd = sc[32 + lane];
-        e[lane] = a; e[32 + lane] = b; e[64 + lane] = c; e[96 + lane] = dd;
+        e[lane] = v[j][0]; e[32 + lane] = v[j][1]; e[64 + lane] = v[j][2]; e[96 + lane] = v[j][3];
       }
     }
   }
 }
 
+// The consumer warps' tile loop: wait for a stage, pull the rows into
+// registers, release the stage, then finish each row (process_row).
 template <int L, int RATIO, bool NORM, bool ROPE>
+__device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_t* s_stage,
+                                              const RowDesc* s_desc, uint64_t* s_full,
+                                              uint64_t* s_empty, volatile int* abort,
+                                              long long n_tiles, int warp, int lane) {
+  using TL = StoreTile<RATIO, NORM, ROPE>;
+  float w[16];
+  if constexpr (NORM) {
+    const uint4* wp = reinterpret_cast<const uint4*>(p.norm_w);
+    unpack_bf16x8(__ldg(wp + lane), w);
+    unpack_bf16x8(__ldg(wp + 32 + lane), w + 8);
+  }
+  long long it = 0;
+  for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+    const int s = (int)(it % kStages);
+    const uint32_t use = (uint32_t)(it / kStages);
+    if (!mbar_wait(&s_full[s], use & 1u, abort, p.err)) break;
+    RowDesc d[TL::kRowsPerWarp];
+    RowIn<RATIO, ROPE> in[TL::kRowsPerWarp];
+    long long slot[TL::kRowsPerWarp];
+#pragma unroll
+    for (int q = 0; q < TL::kRowsPerWarp; ++q) {
+      const int t = warp * TL::kRowsPerWarp + q;
+      d[q] = s_desc[s * TL::kRows + t];
+      const bool ok = d[q].state == kRowOk || d[q].state == kRowOkRing;
+      slot[q] = ok ? dest_slot(p, tile * TL::kRows + t, d[q]) : 0;
+      if (ok) load_row<RATIO, ROPE>(s_stage + s * TL::kStageBytes + t * TL::kSlotBytes, lane, in[q]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_empty[s]);
+#pragma unroll
+    for (int q = 0; q < TL::kRowsPerWarp; ++q) {
+      const long long k = tile * TL::kRows + warp * TL::kRowsPerWarp + q;
+      process_row<L, RATIO, NORM, ROPE>(p, k, d[q], slot[q], in[q], w, lane);
+    }
+  }
+}
+
+// RING: ratio 2 with start positions and/or the pair-state ring.  The
+// launches without either take RING = false, whose kernel has no ring code.
+template <int L, int RATIO, bool NORM, bool ROPE, bool RING>
 __global__ void __launch_bounds__(kStoreThreads, 2)
 compress_store_kernel(const StoreParams p) {
   using TL = StoreTile<RATIO, NORM, ROPE>;
@@ -457,7 +592,7 @@ compress_store_kernel(const StoreParams p) {
       d.state = kRowNone;
       long long src = 0;
       if (lane < TL::kRows) {
-        d = plan_row<RATIO, ROPE>(p, tile * TL::kRows + lane, total, s_base, s_first, s_start,
+        d = plan_row<RATIO, ROPE, RING>(p, tile * TL::kRows + lane, total, s_base, s_first, s_start,
                                   s_count, src);
         s_desc[s * TL::kRows + lane] = d;
       }
@@ -511,47 +646,17 @@ compress_store_kernel(const StoreParams p) {
     }
   } else {
     // ------------------------------------------------------------ consumers
-    float w[16];
-    if constexpr (NORM) {
-      const uint4* wp = reinterpret_cast<const uint4*>(p.norm_w);
-      unpack_bf16x8(__ldg(wp + lane), w);
-      unpack_bf16x8(__ldg(wp + 32 + lane), w + 8);
-    }
-    long long it = 0;
-    for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
-      const int s = (int)(it % kStages);
-      const uint32_t use = (uint32_t)(it / kStages);
-      if (!mbar_wait(&s_full[s], use & 1u, abort, p.err)) break;
-      RowDesc d[TL::kRowsPerWarp];
-      RowIn<RATIO, ROPE> in[TL::kRowsPerWarp];
-      long long slot[TL::kRowsPerWarp];
-#pragma unroll
-      for (int q = 0; q < TL::kRowsPerWarp; ++q) {
-        const int t = warp * TL::kRowsPerWarp + q;
-        d[q] = s_desc[s * TL::kRows + t];
-        const bool ok = d[q].state == kRowOk || d[q].state == kRowOkRing;
-        slot[q] = ok ? dest_slot(p, tile * TL::kRows + t, d[q]) : 0;
-        if (ok) load_row<RATIO, ROPE>(s_stage + s * TL::kStageBytes + t * TL::kSlotBytes, lane, in[q]);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[s]);
-#pragma unroll
-      for (int q = 0; q < TL::kRowsPerWarp; ++q) {
-        const long long k = tile * TL::kRows + warp * TL::kRowsPerWarp + q;
-        process_row<L, RATIO, NORM, ROPE>(p, k, d[q], slot[q], in[q], w, lane);
-      }
-    }
-    if constexpr (RATIO == 2) {
-      if (p.start_pos != nullptr || p.ring != nullptr)
-        ring_phase<L, NORM, ROPE>(p, s_base, s_first, s_start, w, warp, lane);
-    }
+    if constexpr (RATIO == 2 && RING)
+      ring_phase<L, NORM, ROPE>(p, s_base, s_first, s_start, s_count, warp, lane);
+    consume_tiles<L, RATIO, NORM, ROPE>(p, s_stage, s_desc, s_full, s_empty, abort, n_tiles, warp,
+                                        lane);
   }
 }
 
-template <int L, int RATIO, bool NORM, bool ROPE>
+template <int L, int RATIO, bool NORM, bool ROPE, bool RING>
 static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
   using TL = StoreTile<RATIO, NORM, ROPE>;
-  auto kern = compress_store_kernel<L, RATIO, NORM, ROPE>;
+  auto kern = compress_store_kernel<L, RATIO, NORM, ROPE, RING>;
   const size_t smem = (size_t)TL::kFixedSmem + sizeof(long long) * (size_t)(p.n_slots + 1)
                     + 3 * sizeof(int) * (size_t)p.n_slots;
   static int attr_set_for_device[64] = {0};  // the largest size any call can need, once per device
@@ -565,9 +670,20 @@ static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set_for_device[dev] = 1;
   }
+  // resident CTAs per SM at this shared-memory size, cached per device as
+  // (smem << 8 | per_sm): the query costs more host time than the launch
+  static std::atomic<unsigned long long> occupancy[64];
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStoreThreads, smem);
-  if (e != cudaSuccess) return e;
+  const unsigned long long seen = dev < 64 ? occupancy[dev].load(std::memory_order_relaxed) : 0ull;
+  if (seen != 0 && (seen >> 8) == (unsigned long long)smem) {
+    per_sm = (int)(seen & 0xFF);
+  } else {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStoreThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && per_sm > 0 && per_sm < 256)
+      occupancy[dev].store(((unsigned long long)smem << 8) | (unsigned long long)per_sm,
+                           std::memory_order_relaxed);
+  }
   const long long tiles = ((long long)p.n_out + TL::kRows - 1) / TL::kRows;
   const long long cap = (long long)device_sm_count() * (per_sm > 0 ? per_sm : 1);
   const int grid = (int)(tiles < cap ? tiles : cap);
@@ -575,20 +691,26 @@ static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int L, int RATIO>
+template <int L, int RATIO, bool RING>
 static cudaError_t launch_norm_rope(const StoreParams& p, cudaStream_t s) {
   const bool norm = p.norm_w != nullptr, rope = p.freqs != nullptr;
-  if (norm && rope) return launch_variant<L, RATIO, true, true>(p, s);
-  if (norm) return launch_variant<L, RATIO, true, false>(p, s);
-  if (rope) return launch_variant<L, RATIO, false, true>(p, s);
-  return launch_variant<L, RATIO, false, false>(p, s);
+  if (norm && rope) return launch_variant<L, RATIO, true, true, RING>(p, s);
+  if (norm) return launch_variant<L, RATIO, true, false, RING>(p, s);
+  if (rope) return launch_variant<L, RATIO, false, true, RING>(p, s);
+  return launch_variant<L, RATIO, false, false, RING>(p, s);
+}
+
+template <int L>
+static cudaError_t launch_ratio(const StoreParams& p, int ratio, cudaStream_t s) {
+  if (ratio == 1) return launch_norm_rope<L, 1, false>(p, s);
+  if (p.start_pos != nullptr || p.ring != nullptr) return launch_norm_rope<L, 2, true>(p, s);
+  return launch_norm_rope<L, 2, false>(p, s);
 }
 
 cudaError_t launch_compress_store(const StoreParams& p, int layout, int ratio, cudaStream_t s) {
-  if (layout == kV41) return ratio == 1 ? launch_norm_rope<kV41, 1>(p, s) : launch_norm_rope<kV41, 2>(p, s);
-  if (layout == kV41Fp4)
-    return ratio == 1 ? launch_norm_rope<kV41Fp4, 1>(p, s) : launch_norm_rope<kV41Fp4, 2>(p, s);
-  return ratio == 1 ? launch_norm_rope<kV4, 1>(p, s) : launch_norm_rope<kV4, 2>(p, s);
+  if (layout == kV41) return launch_ratio<kV41>(p, ratio, s);
+  if (layout == kV41Fp4) return launch_ratio<kV41Fp4>(p, ratio, s);
+  return launch_ratio<kV4>(p, ratio, s);
 }
 
 }  // namespace dsv4kv

@@ -15,6 +15,8 @@
 // output row is written as two fully coalesced 512-byte warp stores.  Lane l
 // owns the 8-dim chunks l and l + 32, i.e. output bytes [16l, 16l+16) and
 // [512 + 16l, ...), so every store instruction covers one contiguous half row.
+#include <atomic>
+
 #include "internal.cuh"
 #include "quant.cuh"
 
@@ -198,9 +200,17 @@ template <int L, bool TOPK>
 static cudaError_t launch_layout(const uint8_t* pool, long long pool_rows, const GatherSrc& g,
                                  long long n, __nv_bfloat16* out, int* err, cudaStream_t s) {
   auto kern = dequant_gather_kernel<L, TOPK>;
-  int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGatherThreads, 0);
+  // resident CTAs per SM, queried once per device (no dynamic shared memory)
+  static std::atomic<int> occupancy[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  int per_sm = dev < 64 ? occupancy[dev].load(std::memory_order_relaxed) : 0;
+  if (per_sm <= 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGatherThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) occupancy[dev].store(per_sm, std::memory_order_relaxed);
+  }
   const long long rows_per_block = (long long)kGatherWarps * kRowsPerWarp;
   const long long want = (n + rows_per_block - 1) / rows_per_block;
   const long long cap = (long long)device_sm_count() * (per_sm > 0 ? per_sm : 1);
