@@ -20,17 +20,18 @@
 //  * one producer warp: one lane per row of the tile finds the row's request
 //    (binary search over the prefix, shared memory only), writes a 16-byte
 //    descriptor (state, position, request, row) and issues cp.async.bulk
-//    copies of the row's
-//    source rows (one 4 KB copy for a ratio-2 pair in the fused layout) and
-//    of its RoPE row into a 3-stage shared-memory ring; an mbarrier per stage
-//    counts the bytes in flight;
+//    copies of the row's source rows (one 4 KB copy for a ratio-2 pair in
+//    the fused layout) and of its RoPE row into a 3-stage shared-memory
+//    ring, an mbarrier per stage counting the bytes in flight;
 //  * eight consumer warps, each owning one row (ratio 2) or 2-4 (ratio 1) of
 //    the stage: wait for the stage, pull the row into registers, release the
-//    slot, look up the destination (out_loc or the page table) and pool,
-//    normalise, rotate, quantize and store the row.  Lane l holds
-//    dims 8l..8l+7 and 256+8l..263+8l, so every shared-memory read is
+//    slot, look up the destination (out_loc or the page table), then pool,
+//    normalise, rotate, quantize and store the row.  Lane l
+//    holds dims 8l..8l+7 and 256+8l..263+8l, so every shared-memory read is
 //    conflict-free and every global store of a row half is one contiguous
-//    warp access.
+//    warp access;
+//  * with start positions or the pair-state ring (decode, verify, chunked
+//    prefill) the consumers first run the per-request ring phase.
 //  All waits are bounded (see tma.cuh).
 #include <atomic>
 
@@ -70,10 +71,12 @@ struct StoreTile {
   static constexpr int kRopeBytes = ROPE ? kRopeDim * 4 : 0;
   static constexpr int kSlotBytes = kInBytes + kRopeBytes;
   static constexpr int kStageBytes = kRows * kSlotBytes;
+  // stages | descriptors | full, empty and plan barriers | abort flag (+pad)
   static constexpr int kFixedSmem = kStages * kStageBytes + kStages * kRows * (int)sizeof(RowDesc)
-                                  + 2 * kStages * 8 + 16;
+                                  + 2 * kStages * 8 + 8 + 8;
   static_assert(kRows <= 32, "one producer lane per row");
-  static_assert(kSlotBytes % 16 == 0 && kStageBytes % 128 == 0, "bulk-copy alignment");
+  static_assert(kSlotBytes % 16 == 0 && kStageBytes % 128 == 0 && kFixedSmem % 16 == 0,
+                "bulk-copy alignment");
 };
 
 // Compressed rows a request slot produces: RATIO 1: its n new tokens;
@@ -86,56 +89,38 @@ __device__ __forceinline__ long long rows_of_slot(int n, int p0) {
 }
 
 // The in-CTA plan: first[i], start[i], count[i] and base[i] = sum_{r < i} rows_of_slot(r)
-// for i in [0, n_slots] (base[n_slots] = total).  Pass 1 reads the slot
-// arrays in one coalesced sweep whose loads are all issued before any is
-// used (kPlanBatch slots per thread per sweep) and leaves each slot's row
-// count in base[i].  Pass 2 gives thread t the PER consecutive slots
-// [t * PER, (t + 1) * PER): their counts go to registers in one unrolled
-// burst of shared-memory loads, the thread scans them in registers, one
-// shuffle scan per warp and one pass over the warps' totals add the
-// offsets, and the exclusive prefix is written back in place.
+// for i in [0, n_slots] (base[n_slots] = total).
+//  * The slot arrays come into shared memory as bulk copies (one per array,
+//    completing on the plan barrier) when they are 16-byte aligned and
+//    n_slots % 4 == 0; otherwise in one coalesced sweep of plain loads, all
+//    issued before any is used (kPlanBatch slots per thread per sweep).
+//  * Thread t then owns the PER consecutive slots [t * PER, (t + 1) * PER):
+//    their row counts go to registers in one unrolled burst of
+//    shared-memory loads, the thread scans them, one shuffle scan per warp
+//    and one pass over the warps' totals add the offsets, and the exclusive
+//    prefix is written to base.
 constexpr int kPlanBatch = 16;
 constexpr int kPlanMaxPer = (kMaxSlots + kStoreThreads - 1) / kStoreThreads;
 
 template <int RATIO, int PER>
-__device__ __forceinline__ void block_plan_per(const int* __restrict__ ext,
-                                               const int* __restrict__ start_pos, int n_slots,
-                                               long long* base, int* first, int* start,
-                                               int* count, long long* s_warp) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nt = blockDim.x, nwarps = nt >> 5;
-  for (int i0 = tid; i0 < n_slots; i0 += kPlanBatch * nt) {
-    int f[kPlanBatch], n[kPlanBatch], p0[kPlanBatch];
+__device__ __forceinline__ void plan_scan(int n_slots, long long* base, const int* start,
+                                          const int* count, long long* s_warp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int beg = tid * PER, last = n_slots - 1;   // n_slots >= 1
+  // loads at clamped (in-bounds) indices, issued together; slots past the
+  // end count zero rows
+  int cnt[PER], st[PER];
 #pragma unroll
-    for (int u = 0; u < kPlanBatch; ++u) {
-      const int i = i0 + u * nt;
-      f[u] = 0; n[u] = 0; p0[u] = 0;
-      if (i < n_slots) {
-        f[u] = __ldg(ext + i);
-        n[u] = __ldg(ext + n_slots + i);
-        if (start_pos) p0[u] = __ldg(start_pos + i);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kPlanBatch; ++u) {
-      const int i = i0 + u * nt;
-      if (i < n_slots) {
-        first[i] = f[u];
-        start[i] = p0[u];
-        count[i] = n[u];
-        base[i] = rows_of_slot<RATIO>(n[u], p0[u]);
-      }
-    }
+  for (int u = 0; u < PER; ++u) {
+    const int i = min(beg + u, last);
+    cnt[u] = ld_shared_s32(count + i);
+    st[u] = ld_shared_s32(start + i);
   }
-  __syncthreads();
-  const int beg = tid * PER;
   long long v[PER];
-#pragma unroll
-  for (int u = 0; u < PER; ++u) v[u] = beg + u < n_slots ? base[beg + u] : 0;
   long long run = 0;
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
-    const long long c = v[u];
+    const long long c = beg + u <= last ? rows_of_slot<RATIO>(cnt[u], st[u]) : 0;
     v[u] = run;
     run += c;
   }
@@ -155,26 +140,79 @@ __device__ __forceinline__ void block_plan_per(const int* __restrict__ ext,
   }
 #pragma unroll
   for (int u = 0; u < PER; ++u)
-    if (beg + u < n_slots) base[beg + u] = off + v[u];
-  if (tid == 0) base[n_slots] = total;
+    if (beg + u <= last) st_shared_s64(base + beg + u, off + v[u]);
+  if (tid == 0) st_shared_s64(base + n_slots, total);
 }
 
-// n_slots <= kMaxSlots (checked by the host) needs at most kPlanMaxPer slots
-// per thread; small plans take a short unrolled form.
+// Returns false (the same on every thread) when the plan's copies timed out;
+// the CTA then does nothing more.  The barrier inits by thread 0 precede the
+// call.
 template <int RATIO>
-__device__ __noinline__ void block_plan(const int* __restrict__ ext, const int* __restrict__ start_pos,
-                                        int n_slots, long long* base, int* first, int* start,
-                                        int* count) {
+__device__ __noinline__ bool block_plan(const int* __restrict__ ext,
+                                        const int* __restrict__ start_pos, int n_slots,
+                                        long long* base, int* first, int* start, int* count,
+                                        uint64_t* bar, volatile int* abort, int* err) {
   static_assert(kPlanMaxPer * kStoreThreads >= kMaxSlots, "the chunks cover every slot");
   __shared__ long long s_warp[32];
-  const int per = (n_slots + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const bool bulk = n_slots > 0 && (n_slots & 3) == 0 &&
+                    (reinterpret_cast<uintptr_t>(ext) & 15) == 0 &&
+                    (start_pos == nullptr || (reinterpret_cast<uintptr_t>(start_pos) & 15) == 0);
+  if (bulk) {
+    if (tid == 0) {
+      const uint32_t b = 4u * (uint32_t)n_slots;
+      const uint64_t pol = policy_evict_last();
+      mbar_arrive_expect_tx(bar, start_pos ? 3 * b : 2 * b);
+      bulk_g2s(first, ext, b, bar, pol);
+      bulk_g2s(count, ext + n_slots, b, bar, pol);
+      if (start_pos) bulk_g2s(start, start_pos, b, bar, pol);
+    }
+    if (start_pos == nullptr)
+      for (int i = tid; i < n_slots; i += nt) start[i] = 0;
+    __syncthreads();   // every thread sees the initialised barrier before polling it
+    if (!mbar_wait(bar, 0, abort, err) && tid == 0) {
+      // the copies still land in this CTA's shared memory: wait for them again
+      for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(bar, 0); ++i) {
+      }
+    }
+  } else {
+    for (int i0 = tid; i0 < n_slots; i0 += kPlanBatch * nt) {
+      int f[kPlanBatch], n[kPlanBatch], p0[kPlanBatch];
+#pragma unroll
+      for (int u = 0; u < kPlanBatch; ++u) {
+        const int i = i0 + u * nt;
+        f[u] = 0; n[u] = 0; p0[u] = 0;
+        if (i < n_slots) {
+          f[u] = __ldg(ext + i);
+          n[u] = __ldg(ext + n_slots + i);
+          if (start_pos) p0[u] = __ldg(start_pos + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kPlanBatch; ++u) {
+        const int i = i0 + u * nt;
+        if (i < n_slots) {
+          first[i] = f[u];
+          start[i] = p0[u];
+          count[i] = n[u];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (*abort) return false;
+  if (n_slots == 0) {
+    if (tid == 0) base[0] = 0;
+    return true;
+  }
+  const int per = (n_slots + nt - 1) / nt;
   if (per <= 1)
-    block_plan_per<RATIO, 1>(ext, start_pos, n_slots, base, first, start, count, s_warp);
+    plan_scan<RATIO, 1>(n_slots, base, start, count, s_warp);
   else if (per <= 4)
-    block_plan_per<RATIO, 4>(ext, start_pos, n_slots, base, first, start, count, s_warp);
+    plan_scan<RATIO, 4>(n_slots, base, start, count, s_warp);
   else
-    block_plan_per<RATIO, kPlanMaxPer>(ext, start_pos, n_slots, base, first, start, count,
-                                       s_warp);
+    plan_scan<RATIO, kPlanMaxPer>(n_slots, base, start, count, s_warp);
+  return true;
 }
 
 // The plan for output row k (shared memory only, no global loads): request
@@ -400,106 +438,113 @@ template <int L, bool NORM, bool ROPE>
 __device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s_base,
                                         const int* s_first, const int* s_start,
                                         const int* s_count, int warp, int lane) {
-  float w[16];
-  if constexpr (NORM) {
-    const uint4* wp = reinterpret_cast<const uint4*>(p.norm_w);
-    unpack_bf16x8(__ldg(wp + lane), w);
-    unpack_bf16x8(__ldg(wp + 32 + lane), w + 8);
-  }
   const __nv_bfloat16* score_base = p.score ? p.score : p.rows + kDim;
   const long long sstride = p.score ? p.score_stride : p.row_stride;
-  for (long long r = (long long)blockIdx.x * kConsumerWarps + warp; r < p.n_slots;
-       r += (long long)gridDim.x * kConsumerWarps) {
-    const int n = s_count[r];
-    const long long p0 = s_start[r];
-    const long long first = s_first[r];
-    if (n <= 0) continue;
-    const long long k = s_base[r];
-    // the ring row goes through the tiles unless the ring update of this
-    // step may reuse its entry (n >= 2R); without a ring it is a tile fault
-    if ((p0 & 1) && k < p.n_out && p.ring != nullptr && n >= 2LL * p.ring_size) {
-      RowDesc d;
-      d.r = (int)r; d.c = (int)(p0 >> 1); d.pos = (int)(p0 - 1);
-      const bool ok = p0 >= 1 && first >= 0 && first + 1 <= p.n_rows &&
-                      (!ROPE || d.pos < p.max_pos);
-      d.state = ok ? kRowOk : kRowBad;
-      RowIn<2, ROPE> in;
-      long long slot = 0;
-      if (ok) {
-        const uint4* e = reinterpret_cast<const uint4*>(
-            p.ring + ((r * p.ring_size) + (d.c % p.ring_size)) * (2 * kDim));
-        const uint4* kv = reinterpret_cast<const uint4*>(p.rows + first * p.row_stride);
-        const uint4* sc = reinterpret_cast<const uint4*>(score_base + first * sstride);
-        in.kv0[0] = e[lane];       in.kv0[1] = e[32 + lane];
-        in.s0[0] = e[64 + lane];   in.s0[1] = e[96 + lane];
-        in.kv1[0] = kv[lane];      in.kv1[1] = kv[32 + lane];
-        in.s1[0] = sc[lane];       in.s1[1] = sc[32 + lane];
-        if constexpr (ROPE) {
-          if (lane >= 24) {
-            const float4* f = reinterpret_cast<const float4*>(p.freqs + (long long)d.pos * kRopeDim);
-            in.fr[0] = f[2 * (lane - 24)];
-            in.fr[1] = f[2 * (lane - 24) + 1];
-          }
-        }
-        slot = dest_slot(p, k, d);
-      }
-      process_row<L, 2, NORM, ROPE>(p, k, d, slot, in, w, lane);
+  const long long stride = (long long)gridDim.x * kConsumerWarps;
+  const int R = p.ring_size;
+  // (1) ring rows of the requests with n >= 2R new tokens
+  for (long long r = (long long)blockIdx.x * kConsumerWarps + warp; r < p.n_slots; r += stride) {
+    const int n = ld_shared_s32(s_count + r);
+    const long long p0 = ld_shared_s32(s_start + r);
+    if (n <= 0 || !(p0 & 1) || p.ring == nullptr || n < 2LL * R) continue;
+    const long long k = ld_shared_s64(s_base + r);
+    if (k >= p.n_out) continue;
+    const long long first = ld_shared_s32(s_first + r);
+    float w[16];
+    if constexpr (NORM) {
+      const uint4* wp = reinterpret_cast<const uint4*>(p.norm_w);
+      unpack_bf16x8(__ldg(wp + lane), w);
+      unpack_bf16x8(__ldg(wp + 32 + lane), w + 8);
     }
+    RowDesc d;
+    d.r = (int)r; d.c = (int)(p0 >> 1); d.pos = (int)(p0 - 1);
+    const bool ok = p0 >= 1 && first >= 0 && first + 1 <= p.n_rows && (!ROPE || d.pos < p.max_pos);
+    d.state = ok ? kRowOk : kRowBad;
+    RowIn<2, ROPE> in;
+    long long slot = 0;
+    if (ok) {
+      const uint4* e = reinterpret_cast<const uint4*>(
+          p.ring + ((r * R) + (d.c % R)) * (2 * kDim));
+      const uint4* kv = reinterpret_cast<const uint4*>(p.rows + first * p.row_stride);
+      const uint4* sc = reinterpret_cast<const uint4*>(score_base + first * sstride);
+      in.kv0[0] = e[lane];       in.kv0[1] = e[32 + lane];
+      in.s0[0] = e[64 + lane];   in.s0[1] = e[96 + lane];
+      in.kv1[0] = kv[lane];      in.kv1[1] = kv[32 + lane];
+      in.s1[0] = sc[lane];       in.s1[1] = sc[32 + lane];
+      if constexpr (ROPE) {
+        if (lane >= 24) {
+          const float4* f = reinterpret_cast<const float4*>(p.freqs + (long long)d.pos * kRopeDim);
+          in.fr[0] = f[2 * (lane - 24)];
+          in.fr[1] = f[2 * (lane - 24) + 1];
+        }
+      }
+      slot = dest_slot(p, k, d);
+    }
+    process_row<L, 2, NORM, ROPE>(p, k, d, slot, in, w, lane);
   }
   if (p.ring == nullptr) return;
   __syncwarp();
-  // (2) the ring update.  The warp takes its requests kRingBatch at a time and
-  // their t-th ring tokens together, so up to kRingBatch copies are in flight
-  // per round trip; all the entries of one round are distinct.
-  constexpr int kRingBatch = 4;
-  const long long stride = (long long)gridDim.x * kConsumerWarps;
+  // (2) the ring update.  The warp takes its requests kRingGroup at a time;
+  // lane l stands for token tl = l % kRingLanes (+ multiples of kRingLanes)
+  // of request l / kRingLanes and works out its source row and ring entry.
+  // A ballot lists the lanes whose token is valid, and the warp copies those
+  // tokens kRingCopies at a time (the 2 KB kv | score row, 16 bytes per lane
+  // per load).  All the entries of a group are distinct.  A token at a
+  // negative position, or whose source row is out of range, is a fault.
+  constexpr int kRingGroup = 4, kRingLanes = 32 / kRingGroup, kRingCopies = 2;
+  const int gj = lane / kRingLanes, tl = lane % kRingLanes;
   for (long long r0 = (long long)blockIdx.x * kConsumerWarps + warp; r0 < p.n_slots;
-       r0 += kRingBatch * stride) {
-    long long qlo[kRingBatch], qhi[kRingBatch];
-    long long tokens = 0;
-#pragma unroll
-    for (int j = 0; j < kRingBatch; ++j) {
-      const long long r = r0 + j * stride;
-      qlo[j] = 0;
-      qhi[j] = 0;
-      if (r < p.n_slots && s_count[r] > 0) {
-        const long long p0 = s_start[r], n = s_count[r];
-        long long q = p0 + n - 2LL * p.ring_size;
-        if (q < p0) q = p0;
-        qlo[j] = q + (q & 1);      // the first even position
-        qhi[j] = p0 + n;
-        const long long t = qhi[j] > qlo[j] ? (qhi[j] - qlo[j] + 1) >> 1 : 0;
-        tokens = t > tokens ? t : tokens;
+       r0 += kRingGroup * stride) {
+    const long long r = r0 + gj * stride;
+    long long qlo = 0, src = 0;
+    int ntok = 0;
+    if (r < p.n_slots) {
+      const int n = ld_shared_s32(s_count + r);
+      const long long p0 = ld_shared_s32(s_start + r);
+      long long q = p0 + n - 2LL * R;
+      if (q < p0) q = p0;
+      q += q & 1;                                   // the first even position
+      if (n > 0 && p0 + n > q) {
+        qlo = q;
+        ntok = (int)((p0 + n - q + 1) >> 1);        // <= R
+        src = ld_shared_s32(s_first + r) + (q - p0);
       }
     }
-    for (long long t = 0; t < tokens; ++t) {
-      uint4 v[kRingBatch][4];
-      bool ok[kRingBatch];
+    const int max_tok = __reduce_max_sync(kFullMask, (unsigned)ntok);
+    for (int t0 = 0; t0 < max_tok; t0 += kRingLanes) {
+      const int t = t0 + tl;
+      const long long q = qlo + 2LL * t, row = src + 2LL * t;
+      const bool has = t < ntok;
+      const bool bad = has && (q < 0 || row < 0 || row >= p.n_rows);
+      const unsigned n_bad = __popc(__ballot_sync(kFullMask, bad));
+      if (lane == 0 && n_bad && p.err) atomicAdd(p.err, (int)n_bad);
+      unsigned todo = __ballot_sync(kFullMask, has && !bad);
+      const long long dst = has && !bad ? (r * R + (unsigned)(q >> 1) % (unsigned)R) * (2 * kDim) : 0;
+      while (todo) {
+        long long rows_[kRingCopies], dsts_[kRingCopies];
+        bool use[kRingCopies];
 #pragma unroll
-      for (int j = 0; j < kRingBatch; ++j) {
-        const long long r = r0 + j * stride;
-        const long long q = qlo[j] + 2 * t;
-        ok[j] = false;
-        if (q < qhi[j]) {
-          const long long row = s_first[r] + (q - s_start[r]);
-          if (row < 0 || row >= p.n_rows) {
-            if (lane == 0 && p.err) atomicAdd(p.err, 1);
-          } else {
-            ok[j] = true;
-            const uint4* kv = reinterpret_cast<const uint4*>(p.rows + row * p.row_stride);
-            const uint4* sc = reinterpret_cast<const uint4*>(score_base + row * sstride);
-            v[j][0] = kv[lane]; v[j][1] = kv[32 + lane]; v[j][2] = sc[lane]; v[j][3] = sc[32 + lane];
-          }
+        for (int c = 0; c < kRingCopies; ++c) {
+          use[c] = todo != 0;
+          const int l = use[c] ? __ffs(todo) - 1 : 0;
+          if (use[c]) todo &= todo - 1;
+          rows_[c] = __shfl_sync(kFullMask, row, l);
+          dsts_[c] = __shfl_sync(kFullMask, dst, l);
         }
-      }
+        uint4 v[kRingCopies][4];
 #pragma unroll
-      for (int j = 0; j < kRingBatch; ++j) {
-        if (!ok[j]) continue;
-        const long long r = r0 + j * stride;
-        const long long q = qlo[j] + 2 * t;
-        uint4* e = reinterpret_cast<uint4*>(
-            p.ring + ((r * p.ring_size) + ((q >> 1) % p.ring_size)) * (2 * kDim));
-        e[lane] = v[j][0]; e[32 + lane] = v[j][1]; e[64 + lane] = v[j][2]; e[96 + lane] = v[j][3];
+        for (int c = 0; c < kRingCopies; ++c) {
+          if (!use[c]) continue;
+          const uint4* kv = reinterpret_cast<const uint4*>(p.rows + rows_[c] * p.row_stride);
+          const uint4* sc = reinterpret_cast<const uint4*>(score_base + rows_[c] * sstride);
+          v[c][0] = kv[lane]; v[c][1] = kv[32 + lane]; v[c][2] = sc[lane]; v[c][3] = sc[32 + lane];
+        }
+#pragma unroll
+        for (int c = 0; c < kRingCopies; ++c) {
+          if (!use[c]) continue;
+          uint4* e = reinterpret_cast<uint4*>(p.ring + dsts_[c]);
+          e[lane] = v[c][0]; e[32 + lane] = v[c][1]; e[64 + lane] = v[c][2]; e[96 + lane] = v[c][3];
+        }
       }
     }
   }
@@ -556,9 +601,12 @@ compress_store_kernel(const StoreParams p) {
   RowDesc* s_desc = reinterpret_cast<RowDesc*>(smem + kStages * TL::kStageBytes);
   uint64_t* s_full = reinterpret_cast<uint64_t*>(s_desc + kStages * TL::kRows);
   uint64_t* s_empty = s_full + kStages;
-  int* s_abort = reinterpret_cast<int*>(s_empty + kStages);
+  uint64_t* s_plan = s_empty + kStages;
+  int* s_abort = reinterpret_cast<int*>(s_plan + 1);
+  // the plan: base (an even count of 8-byte entries, >= n_slots + 1) | first
+  // | start | count, each array 16-byte aligned when n_slots % 4 == 0
   long long* s_base = reinterpret_cast<long long*>(smem + TL::kFixedSmem);
-  int* s_first = reinterpret_cast<int*>(s_base + p.n_slots + 1);
+  int* s_first = reinterpret_cast<int*>(s_base + ((p.n_slots + 2) & ~1));
   int* s_start = s_first + p.n_slots;
   int* s_count = s_start + p.n_slots;
 
@@ -568,14 +616,17 @@ compress_store_kernel(const StoreParams p) {
       mbar_init(&s_full[s], 1);
       mbar_init(&s_empty[s], kConsumerWarps);
     }
+    mbar_init(s_plan, 1);
     *s_abort = 0;
     mbar_fence_init();
   }
-  block_plan<RATIO>(p.ext, p.start_pos, p.n_slots, s_base, s_first, s_start, s_count);
+  volatile int* abort = s_abort;
+  if (!block_plan<RATIO>(p.ext, p.start_pos, p.n_slots, s_base, s_first, s_start, s_count, s_plan,
+                         abort, p.err))
+    return;
   __syncthreads();
   const long long total = s_base[p.n_slots];
   const long long n_tiles = ((long long)p.n_out + TL::kRows - 1) / TL::kRows;
-  volatile int* abort = s_abort;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -593,7 +644,7 @@ compress_store_kernel(const StoreParams p) {
       long long src = 0;
       if (lane < TL::kRows) {
         d = plan_row<RATIO, ROPE, RING>(p, tile * TL::kRows + lane, total, s_base, s_first, s_start,
-                                  s_count, src);
+                                        s_count, src);
         s_desc[s * TL::kRows + lane] = d;
       }
       const bool copy = d.state == kRowOk || d.state == kRowOkRing;
@@ -657,14 +708,14 @@ template <int L, int RATIO, bool NORM, bool ROPE, bool RING>
 static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
   using TL = StoreTile<RATIO, NORM, ROPE>;
   auto kern = compress_store_kernel<L, RATIO, NORM, ROPE, RING>;
-  const size_t smem = (size_t)TL::kFixedSmem + sizeof(long long) * (size_t)(p.n_slots + 1)
+  const size_t smem = (size_t)TL::kFixedSmem + sizeof(long long) * (size_t)((p.n_slots + 2) & ~1)
                     + 3 * sizeof(int) * (size_t)p.n_slots;
   static int attr_set_for_device[64] = {0};  // the largest size any call can need, once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !attr_set_for_device[dev]) {
-    const size_t max_smem = (size_t)TL::kFixedSmem + sizeof(long long) * (kMaxSlots + 1)
+    const size_t max_smem = (size_t)TL::kFixedSmem + sizeof(long long) * ((kMaxSlots + 2) & ~1)
                           + 3 * sizeof(int) * kMaxSlots;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
     if (e != cudaSuccess) return e;

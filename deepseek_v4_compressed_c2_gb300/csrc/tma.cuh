@@ -61,10 +61,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   return mbar_wait_bounded(bar, parity, abort, err, kSpinLimit);
 }
 
+// Shared-memory accesses through generic pointers that the compiler cannot
+// prove to be shared (e.g. inside a function that is not inlined).
+__device__ __forceinline__ int ld_shared_s32(const int* p) {
+  int v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ long long ld_shared_s64(const long long* p) {
+  long long v;
+  asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_s64(long long* p, long long v) {
+  asm volatile("st.shared.b64 [%0], %1;" :: "r"(smem_u32(p)), "l"(v) : "memory");
+}
+
 // L2 policy for data read exactly once
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// L2 policy for data that every CTA of the grid reads
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 

@@ -444,7 +444,8 @@ int64_t orc_compress_store(
             if (first_new < 0 || last_new >= n_rows) bad = 1;
             if (src[k] < 0 && !ring) bad = 1;
         }
-        if (freqs && (pos[k] < 0 || pos[k] >= max_pos)) bad = 1;
+        if (pos[k] < 0) bad = 1;   /* no token precedes position 0 */
+        if (freqs && pos[k] >= max_pos) bad = 1;
         slot = out_loc ? (int64_t)out_loc[k] : pslot[k];
         if (bad) { /* a row that cannot be computed: zero outputs, one fault */
             ++faults;
@@ -516,7 +517,8 @@ int64_t orc_compress_store(
     }
     /* the ring keeps each request's last ring_size even-position new tokens
      * (kv | score of position q at entry (q / 2) % ring_size), written after
-     * every row of the step has read it */
+     * every row of the step has read it; a token at a negative position has
+     * no entry and, like a source row out of range, counts one fault */
     if (ring && !which) {
         int r;
         for (r = 0; r < n_slots; ++r) {
@@ -529,7 +531,7 @@ int64_t orc_compress_store(
                 uint16_t *e;
                 int d;
                 if (q & 1) continue;
-                if (row < 0 || row >= n_rows) { ++faults; continue; }
+                if (q < 0 || row < 0 || row >= n_rows) { ++faults; continue; }
                 e = ring + ((int64_t)r * ring_size + ((q >> 1) % ring_size)) * (2 * ORC_D);
                 for (d = 0; d < ORC_D; ++d) {
                     e[d] = rows[row * row_stride + d];

@@ -102,3 +102,38 @@ def test_ring_row_without_ring_is_a_counted_fault(B):
                             n_out=cfg["n_out"], err_word=err, start_pos=dev(cfg["start_pos"]))
     torch.cuda.synchronize()
     assert int(err.item()) == int((cfg["start_pos"] % 2 == 1).sum()) == cfg["n_out"]
+
+
+@pytest.mark.parametrize("rope", [False, True])
+def test_negative_start_positions_fault_like_the_oracle(B, rope):
+    rng = np.random.default_rng(21)
+    n_req, R = 6, 3
+    p0 = np.array([-5, -1, -2, 3, -7, 0], np.int32)
+    n = np.array([9, 4, 1, 5, 2, 6], np.int32)
+    first = np.concatenate([[0], np.cumsum(n)[:-1]]).astype(np.int32)
+    rows = W.bf16_from_f32(rng.standard_normal((int(n.sum()), 1024)).astype(np.float32))
+    ring0 = W.bf16_from_f32(rng.standard_normal((n_req, R, 1024)).astype(np.float32))
+    w = W.bf16_from_f32(rng.uniform(0.5, 1.5, 512).astype(np.float32))
+    pt = (rng.permutation(n_req) + 1).astype(np.int32).reshape(n_req, 1)
+    ext = np.stack([first, n]).astype(np.int32)
+    fr = W.rope_table(64) if rope else None
+    n_out = int(sum(((a + b) >> 1) - (a >> 1) for a, b in zip(p0.tolist(), n.tolist())))
+    pool_rows = (n_req + 1) << 6
+    pool = torch.full((pool_rows * 528,), 0xA5, dtype=torch.uint8, device="cuda")
+    ring = dev_bf16(ring0)
+    pre = torch.zeros((n_out, 512), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsv4kv_compress_store(oracle.V41, 2, dev_bf16(rows), dev(ext), pool, page_table=dev(pt),
+                            page_bits=6, rmsnorm_w=dev_bf16(w), eps=1e-6,
+                            freqs_cis=None if fr is None else dev(fr), n_out=n_out,
+                            prequant_out=pre, err_word=err, start_pos=dev(p0), ring=ring)
+    torch.cuda.synchronize()
+    ref_ring = ring0.copy()
+    ref_pool = np.full(pool_rows * 528, 0xA5, np.uint8)
+    pre_h = pre.cpu().numpy()
+    ref = oracle.compress_store(oracle.V41, 2, rows, ext, page_table=pt, page_bits=6, norm_w=w,
+                                eps=1e-6, freqs=fr, n_out=n_out, start_pos=p0, pool=ref_pool,
+                                pool_rows=pool_rows, ring=ref_ring, prequant_in=pre_h)
+    assert ref["faults"] > 0 and int(err.item()) == ref["faults"]
+    assert np.array_equal(host_u16(ring).reshape(ref_ring.shape), ref_ring)
+    assert np.array_equal(pool.cpu().numpy(), ref_pool)

@@ -116,3 +116,27 @@ def test_ring_row_without_a_ring_is_a_fault_and_ring_keeps_last_even_tokens():
     assert np.array_equal(ring[0, 5 % 3], rows[10])
     assert np.array_equal(ring[0, 6 % 3], rows[12])
     assert np.array_equal(ring[0, 7 % 3], rows[14])
+
+
+def test_negative_positions_are_faults_and_the_rest_matches_a_fresh_start():
+    """A start position before 0 (out of contract) must not index the ring
+    or the pool out of range: rows and ring tokens at negative positions
+    count one fault each, the rest equals the same tokens started at 0."""
+    rows, w, fr, pt, pr = _setup(9, 20)
+    for freqs in (None, fr):
+        pool = np.zeros(pr * 528, np.uint8)
+        ring = np.full((1, 3, 1024), 0x3F80, np.uint16)
+        res = oracle.compress_store(oracle.V41, 2, rows[0:9].copy(), np.array([[0], [9]], np.int32),
+                                    page_table=pt, page_bits=3, norm_w=w, freqs=freqs,
+                                    start_pos=np.array([-5], np.int32), pool=pool, pool_rows=pr,
+                                    ring=ring)
+        # positions -5..3: rows c = -3, -2, -1 (pos < 0) and ring token -2 are faults
+        assert res["faults"] == 4 and res["total"] == 5
+        assert np.array_equal(ring[0, 0], rows[5]) and np.array_equal(ring[0, 1], rows[7])
+        assert (ring[0, 2] == 0x3F80).all()
+        fresh = np.zeros(pr * 528, np.uint8)
+        oracle.compress_store(oracle.V41, 2, rows[5:9].copy(), np.array([[0], [4]], np.int32),
+                              page_table=pt, page_bits=3, norm_w=w, freqs=freqs,
+                              start_pos=np.array([0], np.int32), pool=fresh, pool_rows=pr,
+                              ring=np.zeros((1, 3, 1024), np.uint16))
+        assert np.array_equal(pool, fresh)
