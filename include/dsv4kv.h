@@ -159,7 +159,10 @@ int dsv4kv_compress_store(int layout, int ratio,
  *
  *   start_pos   NULL (every slot starts at 0) or int32 [n_slots]: position
  *               p0 of slot r's first new token; new token t (t < count_r) is
- *               at position p0 + t in source row first_r + t.
+ *               at position p0 + t in source row first_r + t.  Positions
+ *               start at 0: a row, or a ring token, at a negative position
+ *               counts one fault in err_word and is neither stored nor
+ *               written to the ring.
  *   Rows: compressed row c pools the tokens at positions ratio*c ..
  *         ratio*c + ratio - 1 and is produced by the step that holds its
  *         last token: ratio 1: c in [p0, p0 + n); ratio 2: c in
