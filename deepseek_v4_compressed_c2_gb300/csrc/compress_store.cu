@@ -41,9 +41,20 @@
 
 namespace dsv4kv {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kStages = 3;
-constexpr int kStoreThreads = (kConsumerWarps + 1) * 32;
+// Two launch shapes.  Streaming (large batches): 8 consumer warps, 3 stages,
+// two CTAs per SM, so each SM keeps 48 rows' inputs in flight.  Latency
+// (ring-form steps small enough for one row per consumer warp: decode and
+// speculative verify): 16 consumer warps, 2 stages, one CTA per SM, so a step
+// of up to 16 rows per SM finishes after one row's latency per warp.
+enum StoreShapeId : int { kShapeStream = 0, kShapeLatency = 1 };
+
+template <int SHAPE>
+struct StoreShape {
+  static constexpr int kWarps = SHAPE == kShapeLatency ? 16 : 8;     // consumer warps
+  static constexpr int kStages = SHAPE == kShapeLatency ? 2 : 3;
+  static constexpr int kMinBlocks = SHAPE == kShapeLatency ? 1 : 2;  // CTAs per SM
+  static constexpr int kThreads = (kWarps + 1) * 32;
+};
 
 // kRowOkRing: the pair's first token is in the ring and the producer copies
 // the ring entry into the stage like any row.  kRowRing: the same, but the
@@ -63,17 +74,22 @@ struct __align__(16) RowDesc {
 // Rows per consumer warp per stage: one ratio-2 pair (4 KB), four ratio-1
 // rows when the row is only stored (32 KB stages either way), two ratio-1
 // rows with RMSNorm or RoPE (four would spill registers).
-template <int RATIO, bool NORM, bool ROPE>
+template <int RATIO, bool NORM, bool ROPE, int SHAPE>
 struct StoreTile {
+  static constexpr int kWarps = StoreShape<SHAPE>::kWarps;
+  static constexpr int kStages = StoreShape<SHAPE>::kStages;
+  static constexpr int kThreads = StoreShape<SHAPE>::kThreads;
   static constexpr int kRowsPerWarp = RATIO == 2 ? 1 : (NORM || ROPE ? 2 : 4);
-  static constexpr int kRows = kConsumerWarps * kRowsPerWarp;      // rows per stage
+  static constexpr int kRows = kWarps * kRowsPerWarp;              // rows per stage
   static constexpr int kInBytes = RATIO == 2 ? 4096 : 1024;        // kv0|s0|kv1|s1, or kv
   static constexpr int kRopeBytes = ROPE ? kRopeDim * 4 : 0;
   static constexpr int kSlotBytes = kInBytes + kRopeBytes;
   static constexpr int kStageBytes = kRows * kSlotBytes;
-  // stages | descriptors | full, empty and plan barriers | abort flag (+pad)
+  // stages | descriptors | full barriers (one per stage and consumer warp),
+  // empty barriers (one per stage), the plan barrier | abort flag (+pad)
+  static constexpr int kBarriers = kStages * kWarps + kStages + 1;
   static constexpr int kFixedSmem = kStages * kStageBytes + kStages * kRows * (int)sizeof(RowDesc)
-                                  + 2 * kStages * 8 + 8 + 8;
+                                  + ((kBarriers * 8 + 8 + 15) & ~15);
   static_assert(kRows <= 32, "one producer lane per row");
   static_assert(kSlotBytes % 16 == 0 && kStageBytes % 128 == 0 && kFixedSmem % 16 == 0,
                 "bulk-copy alignment");
@@ -100,7 +116,6 @@ __device__ __forceinline__ long long rows_of_slot(int n, int p0) {
 //    and one pass over the warps' totals add the offsets, and the exclusive
 //    prefix is written to base.
 constexpr int kPlanBatch = 16;
-constexpr int kPlanMaxPer = (kMaxSlots + kStoreThreads - 1) / kStoreThreads;
 
 template <int RATIO, int PER>
 __device__ __forceinline__ void plan_scan(int n_slots, long long* base, const int* start,
@@ -132,12 +147,16 @@ __device__ __forceinline__ void plan_scan(int n_slots, long long* base, const in
   }
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
-  long long off = incl - run, total = 0;
-  for (int w = 0; w < nwarps; ++w) {
-    const long long t = s_warp[w];
-    if (w < warp) off += t;
-    total += t;
+  // every warp scans the warps' totals across its lanes (nwarps <= 32)
+  const long long wt = lane < nwarps ? s_warp[lane] : 0;
+  long long wincl = wt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long t = __shfl_up_sync(kFullMask, wincl, o);
+    if (lane >= o) wincl += t;
   }
+  const long long total = __shfl_sync(kFullMask, wincl, 31);
+  const long long off = incl - run + __shfl_sync(kFullMask, wincl - wt, warp);
 #pragma unroll
   for (int u = 0; u < PER; ++u)
     if (beg + u <= last) st_shared_s64(base + beg + u, off + v[u]);
@@ -147,12 +166,15 @@ __device__ __forceinline__ void plan_scan(int n_slots, long long* base, const in
 // Returns false (the same on every thread) when the plan's copies timed out;
 // the CTA then does nothing more.  The barrier inits by thread 0 precede the
 // call.
-template <int RATIO>
+template <int RATIO, int THREADS>
 __device__ __noinline__ bool block_plan(const int* __restrict__ ext,
                                         const int* __restrict__ start_pos, int n_slots,
                                         long long* base, int* first, int* start, int* count,
                                         uint64_t* bar, volatile int* abort, int* err) {
-  static_assert(kPlanMaxPer * kStoreThreads >= kMaxSlots, "the chunks cover every slot");
+  // chunk lengths are odd: thread t's slots start at word PER * t, and an odd
+  // stride keeps a warp's 4-byte loads and 8-byte stores free of bank
+  // conflicts
+  constexpr int kPlanMaxPer = ((kMaxSlots + THREADS - 1) / THREADS) | 1;
   __shared__ long long s_warp[32];
   const int tid = threadIdx.x, nt = blockDim.x;
   const bool bulk = n_slots > 0 && (n_slots & 3) == 0 &&
@@ -208,8 +230,8 @@ __device__ __noinline__ bool block_plan(const int* __restrict__ ext,
   const int per = (n_slots + nt - 1) / nt;
   if (per <= 1)
     plan_scan<RATIO, 1>(n_slots, base, start, count, s_warp);
-  else if (per <= 4)
-    plan_scan<RATIO, 4>(n_slots, base, start, count, s_warp);
+  else if (per <= 5)
+    plan_scan<RATIO, 5>(n_slots, base, start, count, s_warp);
   else
     plan_scan<RATIO, kPlanMaxPer>(n_slots, base, start, count, s_warp);
   return true;
@@ -434,16 +456,16 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
 // read that entry at any time.  No other warp writes this request's ring,
 // and no tile reads an entry that this phase writes, so the consumers run it
 // before their tile loop, while the producer's first copies are in flight.
-template <int L, bool NORM, bool ROPE>
+template <int L, bool NORM, bool ROPE, int WARPS>
 __device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s_base,
                                         const int* s_first, const int* s_start,
                                         const int* s_count, int warp, int lane) {
   const __nv_bfloat16* score_base = p.score ? p.score : p.rows + kDim;
   const long long sstride = p.score ? p.score_stride : p.row_stride;
-  const long long stride = (long long)gridDim.x * kConsumerWarps;
+  const long long stride = (long long)gridDim.x * WARPS;
   const int R = p.ring_size;
   // (1) ring rows of the requests with n >= 2R new tokens
-  for (long long r = (long long)blockIdx.x * kConsumerWarps + warp; r < p.n_slots; r += stride) {
+  for (long long r = (long long)blockIdx.x * WARPS + warp; r < p.n_slots; r += stride) {
     const int n = ld_shared_s32(s_count + r);
     const long long p0 = ld_shared_s32(s_start + r);
     if (n <= 0 || !(p0 & 1) || p.ring == nullptr || n < 2LL * R) continue;
@@ -493,7 +515,7 @@ __device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s
   // negative position, or whose source row is out of range, is a fault.
   constexpr int kRingGroup = 4, kRingLanes = 32 / kRingGroup, kRingCopies = 2;
   const int gj = lane / kRingLanes, tl = lane % kRingLanes;
-  for (long long r0 = (long long)blockIdx.x * kConsumerWarps + warp; r0 < p.n_slots;
+  for (long long r0 = (long long)blockIdx.x * WARPS + warp; r0 < p.n_slots;
        r0 += kRingGroup * stride) {
     const long long r = r0 + gj * stride;
     long long qlo = 0, src = 0;
@@ -552,12 +574,12 @@ __device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s
 
 // The consumer warps' tile loop: wait for a stage, pull the rows into
 // registers, release the stage, then finish each row (process_row).
-template <int L, int RATIO, bool NORM, bool ROPE>
+template <int L, int RATIO, bool NORM, bool ROPE, int SHAPE>
 __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_t* s_stage,
                                               const RowDesc* s_desc, uint64_t* s_full,
                                               uint64_t* s_empty, volatile int* abort,
                                               long long n_tiles, int warp, int lane) {
-  using TL = StoreTile<RATIO, NORM, ROPE>;
+  using TL = StoreTile<RATIO, NORM, ROPE, SHAPE>;
   float w[16];
   if constexpr (NORM) {
     const uint4* wp = reinterpret_cast<const uint4*>(p.norm_w);
@@ -566,9 +588,9 @@ __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_
   }
   long long it = 0;
   for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
-    const int s = (int)(it % kStages);
-    const uint32_t use = (uint32_t)(it / kStages);
-    if (!mbar_wait(&s_full[s], use & 1u, abort, p.err)) break;
+    const int s = (int)(it % TL::kStages);
+    const uint32_t use = (uint32_t)(it / TL::kStages);
+    if (!mbar_wait(&s_full[s * TL::kWarps + warp], use & 1u, abort, p.err)) break;
     RowDesc d[TL::kRowsPerWarp];
     RowIn<RATIO, ROPE> in[TL::kRowsPerWarp];
     long long slot[TL::kRowsPerWarp];
@@ -592,15 +614,16 @@ __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_
 
 // RING: ratio 2 with start positions and/or the pair-state ring.  The
 // launches without either take RING = false, whose kernel has no ring code.
-template <int L, int RATIO, bool NORM, bool ROPE, bool RING>
-__global__ void __launch_bounds__(kStoreThreads, 2)
+template <int L, int RATIO, bool NORM, bool ROPE, bool RING, int SHAPE>
+__global__ void __launch_bounds__(StoreShape<SHAPE>::kThreads, StoreShape<SHAPE>::kMinBlocks)
 compress_store_kernel(const StoreParams p) {
-  using TL = StoreTile<RATIO, NORM, ROPE>;
+  using TL = StoreTile<RATIO, NORM, ROPE, SHAPE>;
+  constexpr int kStages = TL::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* s_stage = smem;
   RowDesc* s_desc = reinterpret_cast<RowDesc*>(smem + kStages * TL::kStageBytes);
   uint64_t* s_full = reinterpret_cast<uint64_t*>(s_desc + kStages * TL::kRows);
-  uint64_t* s_empty = s_full + kStages;
+  uint64_t* s_empty = s_full + kStages * TL::kWarps;
   uint64_t* s_plan = s_empty + kStages;
   int* s_abort = reinterpret_cast<int*>(s_plan + 1);
   // the plan: base (an even count of 8-byte entries, >= n_slots + 1) | first
@@ -613,22 +636,22 @@ compress_store_kernel(const StoreParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], kConsumerWarps);
+      for (int w = 0; w < TL::kWarps; ++w) mbar_init(&s_full[s * TL::kWarps + w], 1);
+      mbar_init(&s_empty[s], TL::kWarps);
     }
     mbar_init(s_plan, 1);
     *s_abort = 0;
     mbar_fence_init();
   }
   volatile int* abort = s_abort;
-  if (!block_plan<RATIO>(p.ext, p.start_pos, p.n_slots, s_base, s_first, s_start, s_count, s_plan,
+  if (!block_plan<RATIO, TL::kThreads>(p.ext, p.start_pos, p.n_slots, s_base, s_first, s_start, s_count, s_plan,
                          abort, p.err))
     return;
   __syncthreads();
   const long long total = s_base[p.n_slots];
   const long long n_tiles = ((long long)p.n_out + TL::kRows - 1) / TL::kRows;
 
-  if (warp == kConsumerWarps) {
+  if (warp == TL::kWarps) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
     const __nv_bfloat16* score_base = p.score ? p.score : p.rows + kDim;
@@ -647,12 +670,15 @@ compress_store_kernel(const StoreParams p) {
                                         s_count, src);
         s_desc[s * TL::kRows + lane] = d;
       }
+      // each consumer warp's rows complete on that warp's own barrier: the
+      // first lane of the warp's rows arms it with their bytes
       const bool copy = d.state == kRowOk || d.state == kRowOkRing;
+      uint64_t* bar = &s_full[s * TL::kWarps + min(lane, TL::kRows - 1) / TL::kRowsPerWarp];
       uint32_t bytes = copy ? (uint32_t)TL::kSlotBytes : 0u;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(kFullMask, bytes, o);
+      for (int o = 1; o < TL::kRowsPerWarp; o <<= 1) bytes += __shfl_xor_sync(kFullMask, bytes, o);
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&s_full[s], bytes);
+      if (lane < TL::kRows && lane % TL::kRowsPerWarp == 0) mbar_arrive_expect_tx(bar, bytes);
       __syncwarp();
       if (copy) {
         uint8_t* dst = s_stage + s * TL::kStageBytes + lane * TL::kSlotBytes;
@@ -663,51 +689,52 @@ compress_store_kernel(const StoreParams p) {
             const __nv_bfloat16* e =
                 p.ring + ((long long)d.r * p.ring_size + (d.c % p.ring_size)) * (2 * kDim);
             const __nv_bfloat16* r1 = p.rows + (src + 1) * p.row_stride;
-            bulk_g2s(dst, e, 2048, &s_full[s], pol);
+            bulk_g2s(dst, e, 2048, bar, pol);
             if (fused_pair) {
-              bulk_g2s(dst + 2048, r1, 2048, &s_full[s], pol);
+              bulk_g2s(dst + 2048, r1, 2048, bar, pol);
             } else {
-              bulk_g2s(dst + 2048, r1, 1024, &s_full[s], pol);
-              bulk_g2s(dst + 3072, score_base + (src + 1) * sstride, 1024, &s_full[s], pol);
+              bulk_g2s(dst + 2048, r1, 1024, bar, pol);
+              bulk_g2s(dst + 3072, score_base + (src + 1) * sstride, 1024, bar, pol);
             }
           } else if (fused_pair) {
-            bulk_g2s(dst, r0, 4096, &s_full[s], pol);             // kv0|s0|kv1|s1
+            bulk_g2s(dst, r0, 4096, bar, pol);             // kv0|s0|kv1|s1
           } else {
             const __nv_bfloat16* c0 = score_base + src * sstride;
-            bulk_g2s(dst, r0, 1024, &s_full[s], pol);
-            bulk_g2s(dst + 1024, c0, 1024, &s_full[s], pol);
-            bulk_g2s(dst + 2048, r0 + p.row_stride, 1024, &s_full[s], pol);
-            bulk_g2s(dst + 3072, c0 + sstride, 1024, &s_full[s], pol);
+            bulk_g2s(dst, r0, 1024, bar, pol);
+            bulk_g2s(dst + 1024, c0, 1024, bar, pol);
+            bulk_g2s(dst + 2048, r0 + p.row_stride, 1024, bar, pol);
+            bulk_g2s(dst + 3072, c0 + sstride, 1024, bar, pol);
           }
         } else {
-          bulk_g2s(dst, r0, 1024, &s_full[s], pol);
+          bulk_g2s(dst, r0, 1024, bar, pol);
         }
         if constexpr (ROPE)
           bulk_g2s(dst + TL::kInBytes, p.freqs + (long long)d.pos * kRopeDim, kRopeDim * 4,
-                   &s_full[s], pol);
+                   bar, pol);
       }
     }
     // every issued copy has landed before the CTA may exit (bounded)
-    if (lane == 0) {
+    if (lane < TL::kWarps) {
       for (int s = 0; s < kStages && s < it; ++s) {
         const uint32_t last_use = (uint32_t)((it - 1 - s) / kStages);
-        for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(&s_full[s], last_use & 1u); ++i) {
+        uint64_t* bar = &s_full[s * TL::kWarps + lane];
+        for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(bar, last_use & 1u); ++i) {
         }
       }
     }
   } else {
     // ------------------------------------------------------------ consumers
     if constexpr (RATIO == 2 && RING)
-      ring_phase<L, NORM, ROPE>(p, s_base, s_first, s_start, s_count, warp, lane);
-    consume_tiles<L, RATIO, NORM, ROPE>(p, s_stage, s_desc, s_full, s_empty, abort, n_tiles, warp,
-                                        lane);
+      ring_phase<L, NORM, ROPE, TL::kWarps>(p, s_base, s_first, s_start, s_count, warp, lane);
+    consume_tiles<L, RATIO, NORM, ROPE, SHAPE>(p, s_stage, s_desc, s_full, s_empty, abort, n_tiles,
+                                               warp, lane);
   }
 }
 
-template <int L, int RATIO, bool NORM, bool ROPE, bool RING>
+template <int L, int RATIO, bool NORM, bool ROPE, bool RING, int SHAPE>
 static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
-  using TL = StoreTile<RATIO, NORM, ROPE>;
-  auto kern = compress_store_kernel<L, RATIO, NORM, ROPE, RING>;
+  using TL = StoreTile<RATIO, NORM, ROPE, SHAPE>;
+  auto kern = compress_store_kernel<L, RATIO, NORM, ROPE, RING, SHAPE>;
   const size_t smem = (size_t)TL::kFixedSmem + sizeof(long long) * (size_t)((p.n_slots + 2) & ~1)
                     + 3 * sizeof(int) * (size_t)p.n_slots;
   static int attr_set_for_device[64] = {0};  // the largest size any call can need, once per device
@@ -729,7 +756,7 @@ static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
   if (seen != 0 && (seen >> 8) == (unsigned long long)smem) {
     per_sm = (int)(seen & 0xFF);
   } else {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStoreThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, TL::kThreads, smem);
     if (e != cudaSuccess) return e;
     if (dev < 64 && per_sm > 0 && per_sm < 256)
       occupancy[dev].store(((unsigned long long)smem << 8) | (unsigned long long)per_sm,
@@ -738,24 +765,34 @@ static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
   const long long tiles = ((long long)p.n_out + TL::kRows - 1) / TL::kRows;
   const long long cap = (long long)device_sm_count() * (per_sm > 0 ? per_sm : 1);
   const int grid = (int)(tiles < cap ? tiles : cap);
-  kern<<<grid, kStoreThreads, smem, stream>>>(p);
+  kern<<<grid, TL::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int L, int RATIO, bool RING>
+template <int L, int RATIO, bool RING, int SHAPE>
 static cudaError_t launch_norm_rope(const StoreParams& p, cudaStream_t s) {
   const bool norm = p.norm_w != nullptr, rope = p.freqs != nullptr;
-  if (norm && rope) return launch_variant<L, RATIO, true, true, RING>(p, s);
-  if (norm) return launch_variant<L, RATIO, true, false, RING>(p, s);
-  if (rope) return launch_variant<L, RATIO, false, true, RING>(p, s);
-  return launch_variant<L, RATIO, false, false, RING>(p, s);
+  if (norm && rope) return launch_variant<L, RATIO, true, true, RING, SHAPE>(p, s);
+  if (norm) return launch_variant<L, RATIO, true, false, RING, SHAPE>(p, s);
+  if (rope) return launch_variant<L, RATIO, false, true, RING, SHAPE>(p, s);
+  return launch_variant<L, RATIO, false, false, RING, SHAPE>(p, s);
 }
 
+// The ring form takes the latency shape for steps of more than 8 and at
+// most 16 output rows per SM: the streaming shape (one 8-warp CTA per SM
+// when the plan is large) would give warps two rows in sequence, the latency
+// shape gives every row a consumer warp of its own.  Smaller steps spread
+// over more SMs in the streaming shape.
 template <int L>
 static cudaError_t launch_ratio(const StoreParams& p, int ratio, cudaStream_t s) {
-  if (ratio == 1) return launch_norm_rope<L, 1, false>(p, s);
-  if (p.start_pos != nullptr || p.ring != nullptr) return launch_norm_rope<L, 2, true>(p, s);
-  return launch_norm_rope<L, 2, false>(p, s);
+  if (ratio == 1) return launch_norm_rope<L, 1, false, kShapeStream>(p, s);
+  if (p.start_pos == nullptr && p.ring == nullptr)
+    return launch_norm_rope<L, 2, false, kShapeStream>(p, s);
+  const long long sms = device_sm_count();
+  if ((long long)p.n_out > sms * StoreShape<kShapeStream>::kWarps &&
+      (long long)p.n_out <= sms * StoreShape<kShapeLatency>::kWarps)
+    return launch_norm_rope<L, 2, true, kShapeLatency>(p, s);
+  return launch_norm_rope<L, 2, true, kShapeStream>(p, s);
 }
 
 cudaError_t launch_compress_store(const StoreParams& p, int layout, int ratio, cudaStream_t s) {

@@ -33,11 +33,15 @@ def gpu_step(B, cfg, pool, ring, *, want_pre=True):
     return None if pre is None else pre.cpu().numpy(), int(err.item())
 
 
-@pytest.mark.parametrize("n_new,layout", [(1, oracle.V41), (4, oracle.V41), (4, oracle.V41_FP4),
-                                           (7, oracle.V41)])
-def test_decode_verify_step_matches_oracle(B, n_new, layout):
-    cfg = dict(W.decode_verify(seed=11 + n_new, n_new=n_new, ring_size=4, max_prefix=1024),
-               layout=layout)
+# n_req 512: the latency launch shape (one output row per consumer warp);
+# n_req 2048 x 5 tokens (~5000 rows, more than 16 rows per SM): the
+# streaming shape of the ring form
+@pytest.mark.parametrize("n_new,layout,n_req", [(1, oracle.V41, 512), (4, oracle.V41, 512),
+                                                (4, oracle.V41_FP4, 512), (7, oracle.V41, 512),
+                                                (5, oracle.V41, 2048)])
+def test_decode_verify_step_matches_oracle(B, n_new, layout, n_req):
+    cfg = dict(W.decode_verify(seed=11 + n_new, n_req=n_req, n_new=n_new, ring_size=4,
+                               max_prefix=1024), layout=layout)
     rb = oracle.row_bytes(layout)
     pool = torch.full((cfg["pool_rows"] * rb,), 0xA5, dtype=torch.uint8, device="cuda")
     ring = dev_bf16(cfg["ring"])
