@@ -40,18 +40,37 @@ cudaError_t launch_bounded_wait_selftest(uint32_t polls, int* err, int* gave_up,
 // scale_codes[i].
 __global__ void fp4_quotient_selftest_kernel(const float* x, const unsigned char* scale_codes,
                                              long long n, float* q_fast, float* q_ieee) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const float s = e4m3_to_f32(scale_codes[i]);
-    q_fast[i] = div_by_recip(x[i], s, __frcp_rn(s));
-    q_ieee[i] = __fdiv_rn(x[i], s);
+  // elements 2j and 2j + 1 go through the paired form used by the FP4 store
+  // (each with its own divisor and the quantizer's reciprocal table); the
+  // loop bound is per warp, so every lane reaches the table's shuffle
+  const int lane = threadIdx.x & 31;
+  const uint32_t table = fp4_recip_table(lane);
+  const long long pairs = (n + 1) / 2;
+  for (long long j0 = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); j0 < pairs;
+       j0 += (long long)gridDim.x * blockDim.x) {
+    const long long i = 2 * (j0 + lane);
+    const bool has0 = i < n, has1 = i + 1 < n;
+    const uint32_t c0 = has0 ? scale_codes[i] : 1u, c1 = has1 ? scale_codes[i + 1] : 1u;
+    const float y0 = e4m3_recip(c0, table), y1 = e4m3_recip(c1, table);
+    const float s0 = e4m3_to_f32(c0), s1 = e4m3_to_f32(c1);
+    float a, b;
+    f2_split(div2_by_recip(f2(has0 ? x[i] : 0.f, has1 ? x[i + 1] : 0.f), f2(-s0, -s1), f2(y0, y1)),
+             a, b);
+    if (has0) {
+      q_fast[i] = a;
+      q_ieee[i] = __fdiv_rn(x[i], s0);
+    }
+    if (has1) {
+      q_fast[i + 1] = b;
+      q_ieee[i + 1] = __fdiv_rn(x[i + 1], s1);
+    }
   }
 }
 
 cudaError_t launch_fp4_quotient_selftest(const float* x, const unsigned char* scale_codes,
                                          long long n, float* q_fast, float* q_ieee,
                                          cudaStream_t stream) {
-  const long long want = (n + 255) / 256;
+  const long long want = ((n + 1) / 2 + 255) / 256;
   const int grid = (int)(want < 4096 ? want : 4096);
   fp4_quotient_selftest_kernel<<<grid, 256, 0, stream>>>(x, scale_codes, n, q_fast, q_ieee);
   return cudaGetLastError();

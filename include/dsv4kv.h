@@ -262,9 +262,11 @@ int dsv4kv_selftest_bounded_wait(int polls, int *err_word, int *gave_up, void *s
 /*
  * Self-test of the V41_FP4 quantizer's division (no counterpart on the pages):
  * for each i, with s = the e4m3 value of scale_codes[i], writes the
- * quantizer's quotient x[i] / s (reciprocal plus one correction step) to
- * q_fast[i] and the IEEE division to q_ieee[i]; the two must agree bit for
- * bit.  x, q_fast, q_ieee: fp32 [n] device; scale_codes: uint8 [n] device.
+ * quantizer's quotient x[i] / s (reciprocal plus one correction step, in
+ * the paired fp32 form the quantizer uses: elements 2j and 2j + 1 together)
+ * to q_fast[i] and the IEEE division to q_ieee[i]; the two must agree bit
+ * for bit.  x, q_fast, q_ieee: fp32 [n] device; scale_codes: uint8 [n]
+ * device.
  */
 int dsv4kv_selftest_fp4_quotient(const float *x, const unsigned char *scale_codes, long long n,
                                  float *q_fast, float *q_ieee, void *stream);
