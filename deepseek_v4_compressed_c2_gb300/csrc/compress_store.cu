@@ -323,9 +323,13 @@ struct RowIn {
   float4 fr[2];
 };
 
+// Stage layout: the rows' inputs back to back (kInBytes each), then their
+// RoPE rows (kRopeBytes each), so consecutive source rows can arrive in one
+// copy.
 template <int RATIO, bool ROPE>
-__device__ __forceinline__ void load_row(const uint8_t* slot, int lane, RowIn<RATIO, ROPE>& in) {
-  const uint4* b = reinterpret_cast<const uint4*>(slot);   // 64 uint4 per 1 KB block
+__device__ __forceinline__ void load_row(const uint8_t* in_row, const uint8_t* rope_row, int lane,
+                                         RowIn<RATIO, ROPE>& in) {
+  const uint4* b = reinterpret_cast<const uint4*>(in_row);   // 64 uint4 per 1 KB block
   in.kv0[0] = b[lane];
   in.kv0[1] = b[32 + lane];
   if constexpr (RATIO == 2) {
@@ -338,7 +342,7 @@ __device__ __forceinline__ void load_row(const uint8_t* slot, int lane, RowIn<RA
   }
   if constexpr (ROPE) {
     if (lane >= 24) {
-      const float4* f = reinterpret_cast<const float4*>(slot + (RATIO == 2 ? 4096 : 1024));
+      const float4* f = reinterpret_cast<const float4*>(rope_row);
       in.fr[0] = f[2 * (lane - 24)];
       in.fr[1] = f[2 * (lane - 24) + 1];
     }
@@ -603,7 +607,10 @@ __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_
       d[q] = s_desc[s * TL::kRows + t];
       const bool ok = d[q].state == kRowOk || d[q].state == kRowOkRing;
       slot[q] = ok ? dest_slot(p, tile * TL::kRows + t, d[q]) : 0;
-      if (ok) load_row<RATIO, ROPE>(s_stage + s * TL::kStageBytes + t * TL::kSlotBytes, lane, in[q]);
+      const uint8_t* stage = s_stage + s * TL::kStageBytes;
+      if (ok)
+        load_row<RATIO, ROPE>(stage + t * TL::kInBytes,
+                              stage + TL::kRows * TL::kInBytes + t * TL::kRopeBytes, lane, in[q]);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&s_empty[s]);
@@ -674,8 +681,19 @@ compress_store_kernel(const StoreParams p) {
         s_desc[s * TL::kRows + lane] = d;
       }
       // each consumer warp's rows complete on that warp's own barrier: the
-      // first lane of the warp's rows arms it with their bytes
+      // first lane of the warp's rows (the group leader) arms it with their
+      // bytes.  Ratio 1: a group of consecutive packed source rows comes in
+      // one copy issued by the leader.
       const bool copy = d.state == kRowOk || d.state == kRowOkRing;
+      const int leader = lane & ~(TL::kRowsPerWarp - 1);
+      bool merged = false;
+      if constexpr (RATIO == 1 && TL::kRowsPerWarp > 1) {
+        const long long src_l = __shfl_sync(kFullMask, src, leader);
+        const bool next = lane < TL::kRows && d.state == kRowOk && src == src_l + (lane - leader);
+        const unsigned all = __ballot_sync(kFullMask, next);
+        const unsigned group = ((1u << TL::kRowsPerWarp) - 1u) << leader;
+        merged = p.row_stride == kDim && (all & group) == group;
+      }
       uint64_t* bar = &s_full[s * TL::kWarps + min(lane, TL::kRows - 1) / TL::kRowsPerWarp];
       uint32_t bytes = copy ? (uint32_t)TL::kSlotBytes : 0u;
 #pragma unroll
@@ -684,7 +702,8 @@ compress_store_kernel(const StoreParams p) {
       if (lane < TL::kRows && lane % TL::kRowsPerWarp == 0) mbar_arrive_expect_tx(bar, bytes);
       __syncwarp();
       if (copy) {
-        uint8_t* dst = s_stage + s * TL::kStageBytes + lane * TL::kSlotBytes;
+        uint8_t* stage = s_stage + s * TL::kStageBytes;
+        uint8_t* dst = stage + lane * TL::kInBytes;
         const __nv_bfloat16* r0 = p.rows + (d.state == kRowOkRing ? 0 : src) * p.row_stride;
         if constexpr (RATIO == 2) {
           if (d.state == kRowOkRing) {
@@ -708,12 +727,14 @@ compress_store_kernel(const StoreParams p) {
             bulk_g2s(dst + 2048, r0 + p.row_stride, 1024, bar, pol);
             bulk_g2s(dst + 3072, c0 + sstride, 1024, bar, pol);
           }
-        } else {
+        } else if (!merged) {
           bulk_g2s(dst, r0, 1024, bar, pol);
+        } else if (lane == leader) {
+          bulk_g2s(dst, r0, 1024 * TL::kRowsPerWarp, bar, pol);
         }
         if constexpr (ROPE)
-          bulk_g2s(dst + TL::kInBytes, p.freqs + (long long)d.pos * kRopeDim, kRopeDim * 4,
-                   bar, pol);
+          bulk_g2s(stage + TL::kRows * TL::kInBytes + lane * TL::kRopeBytes,
+                   p.freqs + (long long)d.pos * kRopeDim, kRopeDim * 4, bar, pol);
       }
     }
     // every issued copy has landed before the CTA may exit (bounded)
