@@ -33,12 +33,14 @@ def gpu_step(B, cfg, pool, ring, *, want_pre=True):
     return None if pre is None else pre.cpu().numpy(), int(err.item())
 
 
-# n_req 512: the latency launch shape (one output row per consumer warp);
-# n_req 2048 x 5 tokens (~5000 rows, more than 16 rows per SM): the
-# streaming shape of the ring form
+# The ring form's launch shape follows the rows per SM: 512 x 1 and 512 x 4
+# (<= 8 rows per SM) and 2048 x 5 (~5000 rows, > 16 per SM) take the
+# streaming shape, 512 x 7 and 4096 x 1 (8-16 per SM) the latency shape;
+# 4096 request slots is the largest plan (222 KB of shared memory there).
 @pytest.mark.parametrize("n_new,layout,n_req", [(1, oracle.V41, 512), (4, oracle.V41, 512),
                                                 (4, oracle.V41_FP4, 512), (7, oracle.V41, 512),
-                                                (5, oracle.V41, 2048)])
+                                                (7, oracle.V41_FP4, 512), (7, oracle.V4, 512),
+                                                (5, oracle.V41, 2048), (1, oracle.V41, 4096)])
 def test_decode_verify_step_matches_oracle(B, n_new, layout, n_req):
     cfg = dict(W.decode_verify(seed=11 + n_new, n_req=n_req, n_new=n_new, ring_size=4,
                                max_prefix=1024), layout=layout)
