@@ -112,8 +112,8 @@ __device__ __forceinline__ long long rows_of_slot(int n, int p0) {
 //    issued before any is used (kPlanBatch slots per thread per sweep).
 //  * Thread t then owns the PER consecutive slots [t * PER, (t + 1) * PER):
 //    their row counts go to registers in one unrolled burst of
-//    shared-memory loads, the thread scans them, one shuffle scan per warp
-//    and one pass over the warps' totals add the offsets, and the exclusive
+//    shared-memory loads, the thread scans them, a shuffle scan per warp and
+//    a second one over the warps' totals add the offsets, and the exclusive
 //    prefix is written to base.
 constexpr int kPlanBatch = 16;
 

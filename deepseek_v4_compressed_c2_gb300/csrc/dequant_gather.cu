@@ -19,6 +19,7 @@
 
 #include "internal.cuh"
 #include "quant.cuh"
+#include "tma.cuh"
 
 namespace dsv4kv {
 
@@ -196,6 +197,265 @@ dequant_gather_kernel(const uint8_t* __restrict__ pool, long long pool_rows, con
   }
 }
 
+// ------------------------------------------------------------------ TMA form
+// V41 and V41_FP4 rows are whole multiples of 16 bytes, so each gathered row
+// can arrive by one cp.async.bulk copy.  Persistent CTAs of one producer warp
+// and kTmaWarps consumer warps walk tiles of kTmaRows rows
+// (tile = blockIdx.x + i * gridDim.x):
+//  * the producer's lane l owns row l of a tile: it resolves the row's slot
+//    (TOPK: the request-local id and the token's request are loaded two tiles
+//    ahead, the page-table entry one tile ahead, so each tile waits on one
+//    dependent load), counts faults and lens, publishes the slot in shared
+//    memory and issues the row's copy into a kTmaStages-deep stage ring; each
+//    consumer warp's rows complete on that warp's own mbarrier;
+//  * consumer warp w owns rows 4w..4w+3 of every tile: it waits for them,
+//    pulls codes and scales from shared memory into registers, releases the
+//    stage and writes each bf16 row as two contiguous 512-byte warp stores.
+// The rows in flight (two CTAs x 4 stages x 32 rows per SM) do not depend on
+// registers, unlike the load-to-register form, whose warps wait on each
+// group's loads before converting it.
+constexpr int kTmaWarps = 8;
+constexpr int kTmaThreads = (kTmaWarps + 1) * 32;
+constexpr int kTmaRows = 32;                            // one per producer lane
+constexpr int kTmaRowsPerWarp = kTmaRows / kTmaWarps;   // 4
+constexpr int kTmaStages = 4;
+
+template <int L>
+struct GatherTile {
+  static constexpr int kRB = LayoutTraits<L>::kRowBytes;
+  static constexpr int kStageBytes = kTmaRows * kRB;
+  static constexpr int kSlotOff = kTmaStages * kStageBytes;            // int slot per staged row
+  static constexpr int kBarOff = kSlotOff + kTmaStages * kTmaRows * 4;
+  static constexpr int kBarriers = kTmaStages * kTmaWarps + kTmaStages;  // full (stage x warp), empty
+  static constexpr int kSmem = kBarOff + kBarriers * 8 + 16;             // + abort flag
+  static_assert(kRB % 16 == 0 && kStageBytes % 16 == 0 && kBarOff % 8 == 0, "bulk-copy alignment");
+};
+
+// A TOPK row's inputs to the page-table step: its request-local id, the
+// token's request, and whether the token is valid.
+struct TopkRaw {
+  int id;
+  int r;
+  bool live;   // row exists, token valid
+};
+
+__device__ __forceinline__ TopkRaw topk_raw(const GatherSrc& g, long long i, long long n) {
+  TopkRaw a{-1, -1, false};
+  if (i >= n) return a;
+  const long long t = i / g.k;
+  a.r = __ldg(g.token_to_req + t);
+  a.id = __ldg(g.topk + i);
+  a.live = !g.is_valid || g.is_valid[t] != 0;
+  return a;
+}
+
+// Lane l resolves row base + l (-1: zero row), with topk_row_slot's faults;
+// TOPK also counts lens.  Called by the whole producer warp.
+template <bool TOPK>
+__device__ __forceinline__ int tma_row_slot(const GatherSrc& g, long long base, long long n,
+                                            const TopkRaw& a, int lane, int* err) {
+  const long long i = base + lane;
+  int slot = -1;
+  if constexpr (!TOPK) {
+    if (i < n) slot = __ldg(g.ids + i);
+  } else {
+    const bool mine = i < n;
+    if (mine) {
+      if (a.r < 0 || a.r >= g.n_req) {
+        if (i % g.k == 0 && err) atomicAdd(err, 1);
+      } else if (a.live && a.id >= 0) {
+        const int lp = a.id >> g.page_bits;
+        if (lp >= g.max_pages) {
+          if (err) atomicAdd(err, 1);
+        } else {
+          const unsigned phys = (unsigned)__ldg(g.page_table + (long long)a.r * g.max_pages + lp);
+          slot = (int)((phys << g.page_bits) | ((unsigned)a.id & ((1u << g.page_bits) - 1u)));
+        }
+      }
+    }
+    if (g.lens) {
+      // count valid slots per token, one atomic per token present in the tile
+      const long long t = mine ? i / g.k : -1;
+      const long long t0 = __shfl_sync(kFullMask, t, 0);
+      const unsigned same = __ballot_sync(kFullMask, mine && t == t0);
+      const unsigned valid = __ballot_sync(kFullMask, mine && slot >= 0);
+      if (lane == 0 && (same & valid)) atomicAdd(g.lens + t0, __popc(same & valid));
+      if (mine && t != t0 && slot >= 0) atomicAdd(g.lens + t, 1);
+    }
+  }
+  return slot;
+}
+
+template <int L, bool TOPK>
+__global__ void __launch_bounds__(kTmaThreads, 2)
+dequant_gather_tma_kernel(const uint8_t* __restrict__ pool, long long pool_rows, const GatherSrc g,
+                          long long n, __nv_bfloat16* __restrict__ out, int* err) {
+  using GT = GatherTile<L>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  int* s_slot = reinterpret_cast<int*>(smem + GT::kSlotOff);
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(smem + GT::kBarOff);
+  uint64_t* s_empty = s_full + kTmaStages * kTmaWarps;
+  int* s_abort = reinterpret_cast<int*>(s_empty + kTmaStages);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kTmaStages * kTmaWarps; ++i) mbar_init(&s_full[i], 1);
+    for (int s = 0; s < kTmaStages; ++s) mbar_init(&s_empty[s], kTmaWarps);
+    *s_abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  volatile int* abort = s_abort;
+  const long long n_tiles = (n + kTmaRows - 1) / kTmaRows;
+  const long long step = gridDim.x;
+
+  if (warp == kTmaWarps) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = policy_evict_first();
+    long long tile = blockIdx.x;
+    TopkRaw raw_next{-1, -1, false};
+    int slot = -1;
+    if constexpr (TOPK) {
+      slot = tma_row_slot<TOPK>(g, tile * kTmaRows, n,
+                                topk_raw(g, tile * kTmaRows + lane, n), lane, err);
+      raw_next = topk_raw(g, (tile + step) * kTmaRows + lane, n);
+    } else {
+      slot = tma_row_slot<TOPK>(g, tile * kTmaRows, n, raw_next, lane, err);
+    }
+    long long it = 0;
+    for (; tile < n_tiles; tile += step, ++it) {
+      TopkRaw raw_after{-1, -1, false};
+      if constexpr (TOPK) raw_after = topk_raw(g, (tile + 2 * step) * kTmaRows + lane, n);
+      const int s = (int)(it % kTmaStages);
+      const uint32_t use = (uint32_t)(it / kTmaStages);
+      if (use > 0 && !mbar_wait(&s_empty[s], (use - 1) & 1u, abort, err)) break;
+      const bool valid = slot >= 0 && slot < pool_rows;
+      if (slot >= pool_rows && err) atomicAdd(err, 1);
+      s_slot[s * kTmaRows + lane] = valid ? slot : -1;
+      uint64_t* bar = &s_full[s * kTmaWarps + lane / kTmaRowsPerWarp];
+      uint32_t bytes = valid ? (uint32_t)GT::kRB : 0u;
+#pragma unroll
+      for (int o = 1; o < kTmaRowsPerWarp; o <<= 1) bytes += __shfl_xor_sync(kFullMask, bytes, o);
+      __syncwarp();
+      if (lane % kTmaRowsPerWarp == 0) mbar_arrive_expect_tx(bar, bytes);
+      __syncwarp();
+      if (valid)
+        bulk_g2s(smem + s * GT::kStageBytes + lane * GT::kRB, pool + (long long)slot * GT::kRB,
+                 GT::kRB, bar, pol);
+      // the next tile's slots, while this tile's copies are in flight
+      slot = tma_row_slot<TOPK>(g, (tile + step) * kTmaRows, n, raw_next, lane, err);
+      raw_next = raw_after;
+    }
+    // every issued copy has landed before the CTA may exit (bounded)
+    if (lane < kTmaWarps) {
+      for (int s = 0; s < kTmaStages && s < it; ++s) {
+        const uint32_t last_use = (uint32_t)((it - 1 - s) / kTmaStages);
+        uint64_t* bar = &s_full[s * kTmaWarps + lane];
+        for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(bar, last_use & 1u); ++i) {
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  long long it = 0;
+  for (long long tile = blockIdx.x; tile < n_tiles; tile += step, ++it) {
+    const int s = (int)(it % kTmaStages);
+    const uint32_t use = (uint32_t)(it / kTmaStages);
+    if (!mbar_wait(&s_full[s * kTmaWarps + warp], use & 1u, abort, err)) break;
+    const uint8_t* stage = smem + s * GT::kStageBytes;
+    int sl[kTmaRowsPerWarp];
+    if constexpr (L == kV41) {
+      uint2 c0[kTmaRowsPerWarp], c1[kTmaRowsPerWarp];
+      uint4 sc[kTmaRowsPerWarp];
+#pragma unroll
+      for (int q = 0; q < kTmaRowsPerWarp; ++q) {
+        const int r = warp * kTmaRowsPerWarp + q;
+        sl[q] = s_slot[s * kTmaRows + r];
+        if (sl[q] >= 0) {
+          const uint8_t* row = stage + r * GT::kRB;
+          c0[q] = *reinterpret_cast<const uint2*>(row + 8 * lane);
+          c1[q] = *reinterpret_cast<const uint2*>(row + 256 + 8 * lane);
+          sc[q] = *reinterpret_cast<const uint4*>(row + LayoutTraits<kV41>::kCodeBytes);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[s]);
+#pragma unroll
+      for (int q = 0; q < kTmaRowsPerWarp; ++q) {
+        const long long i = tile * kTmaRows + warp * kTmaRowsPerWarp + q;
+        if (i >= n) break;
+        uint4* o = reinterpret_cast<uint4*>(out + i * kDim);
+        if (sl[q] < 0) {
+          o[lane] = make_uint4(0, 0, 0, 0);
+          o[32 + lane] = make_uint4(0, 0, 0, 0);
+          continue;
+        }
+        // chunk l: dims 8l..8l+7, group l/4; chunk l+32: group 8 + l/4
+        const int sh = 8 * ((lane >> 2) & 3);
+        const uint32_t e0 = ((lane < 16 ? sc[q].x : sc[q].y) >> sh) & 0xFFu;
+        const uint32_t e1 = ((lane < 16 ? sc[q].z : sc[q].w) >> sh) & 0xFFu;
+        o[lane] = dequant8_v41(c0[q], ue8m0_scale(e0));
+        o[32 + lane] = dequant8_v41(c1[q], ue8m0_scale(e1));
+      }
+    } else {
+      uint32_t c0[kTmaRowsPerWarp], c1[kTmaRowsPerWarp], s0[kTmaRowsPerWarp], s1[kTmaRowsPerWarp];
+#pragma unroll
+      for (int q = 0; q < kTmaRowsPerWarp; ++q) {
+        const int r = warp * kTmaRowsPerWarp + q;
+        sl[q] = s_slot[s * kTmaRows + r];
+        if (sl[q] >= 0) {
+          const uint8_t* row = stage + r * GT::kRB;
+          c0[q] = *reinterpret_cast<const uint32_t*>(row + 4 * lane);
+          c1[q] = *reinterpret_cast<const uint32_t*>(row + 128 + 4 * lane);
+          // chunk l: group l/2; chunk l+32: group 16 + l/2
+          s0[q] = row[LayoutTraits<kV41Fp4>::kCodeBytes + (lane >> 1)];
+          s1[q] = row[LayoutTraits<kV41Fp4>::kCodeBytes + 16 + (lane >> 1)];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[s]);
+#pragma unroll
+      for (int q = 0; q < kTmaRowsPerWarp; ++q) {
+        const long long i = tile * kTmaRows + warp * kTmaRowsPerWarp + q;
+        if (i >= n) break;
+        uint4* o = reinterpret_cast<uint4*>(out + i * kDim);
+        if (sl[q] < 0) {
+          o[lane] = make_uint4(0, 0, 0, 0);
+          o[32 + lane] = make_uint4(0, 0, 0, 0);
+          continue;
+        }
+        o[lane] = dequant8_fp4(c0[q], e4m3_to_f32(s0[q]));
+        o[32 + lane] = dequant8_fp4(c1[q], e4m3_to_f32(s1[q]));
+      }
+    }
+  }
+}
+
+template <int L, bool TOPK>
+static cudaError_t launch_tma(const uint8_t* pool, long long pool_rows, const GatherSrc& g,
+                              long long n, __nv_bfloat16* out, int* err, cudaStream_t s) {
+  using GT = GatherTile<L>;
+  auto kern = dequant_gather_tma_kernel<L, TOPK>;
+  static std::atomic<int> occupancy[64];   // resident CTAs per SM, per device (attribute set then)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int per_sm = dev < 64 ? occupancy[dev].load(std::memory_order_relaxed) : 0;
+  if (per_sm <= 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GT::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTmaThreads, GT::kSmem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && per_sm > 0) occupancy[dev].store(per_sm, std::memory_order_relaxed);
+  }
+  const long long tiles = (n + kTmaRows - 1) / kTmaRows;
+  const long long cap = (long long)device_sm_count() * (per_sm > 0 ? per_sm : 1);
+  const int grid = (int)(tiles < cap ? tiles : cap);
+  kern<<<grid, kTmaThreads, GT::kSmem, s>>>(pool, pool_rows, g, n, out, err);
+  return cudaGetLastError();
+}
+
 template <int L, bool TOPK>
 static cudaError_t launch_layout(const uint8_t* pool, long long pool_rows, const GatherSrc& g,
                                  long long n, __nv_bfloat16* out, int* err, cudaStream_t s) {
@@ -224,9 +484,9 @@ cudaError_t launch_dequant_gather(int layout, const uint8_t* pool, long long poo
                                   cudaStream_t s) {
   GatherSrc g{};
   g.ids = ids;
-  if (layout == kV41) return launch_layout<kV41, false>(pool, pool_rows, g, n, out, err, s);
+  if (layout == kV41) return launch_tma<kV41, false>(pool, pool_rows, g, n, out, err, s);
   if (layout == kV4) return launch_layout<kV4, false>(pool, pool_rows, g, n, out, err, s);
-  return launch_layout<kV41Fp4, false>(pool, pool_rows, g, n, out, err, s);
+  return launch_tma<kV41Fp4, false>(pool, pool_rows, g, n, out, err, s);
 }
 
 cudaError_t launch_dequant_gather_topk(int layout, const uint8_t* pool, long long pool_rows,
@@ -245,9 +505,9 @@ cudaError_t launch_dequant_gather_topk(int layout, const uint8_t* pool, long lon
   g.k = k;
   g.lens = lens;
   const long long n = (long long)n_tok * k;
-  if (layout == kV41) return launch_layout<kV41, true>(pool, pool_rows, g, n, out, err, s);
+  if (layout == kV41) return launch_tma<kV41, true>(pool, pool_rows, g, n, out, err, s);
   if (layout == kV4) return launch_layout<kV4, true>(pool, pool_rows, g, n, out, err, s);
-  return launch_layout<kV41Fp4, true>(pool, pool_rows, g, n, out, err, s);
+  return launch_tma<kV41Fp4, true>(pool, pool_rows, g, n, out, err, s);
 }
 
 }  // namespace dsv4kv
