@@ -384,23 +384,27 @@ def test_pool_bytes_do_not_depend_on_the_debug_outputs(B, layout):
     assert np.array_equal(with_dbg["pool"], without["pool"])
 
 
-@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4, oracle.V4])
-def test_fused_topk_gather_matches_oracle_composition(B, layout):
+@pytest.mark.parametrize("layout,n_tok,k", [(oracle.V41, 37, 515), (oracle.V41_FP4, 37, 515),
+                                            (oracle.V4, 37, 515), (oracle.V41, 101, 5),
+                                            (oracle.V41_FP4, 77, 3)])
+def test_fused_topk_gather_matches_oracle_composition(B, layout, n_tok, k):
     """dsv4kv_dequant_gather_topk == oracle top-k -> slots then gather, with
     lens and every fault kind (bad request, page past the table, slot past the
-    pool), on a pool written by the store."""
+    pool), on a pool written by the store; k = 3 or 5 puts many tokens in one
+    32-row tile of the bulk-copy gather."""
     cfg = dict(W.cfg2_ratio2_small(), layout=layout)
     pool = gpu_store(B, cfg)["pool"]
-    rng = np.random.default_rng(31 + layout)
-    n_tok, k = 37, 515
+    rng = np.random.default_rng(31 + layout + k)
     pt = cfg["page_table"].copy()
     pt[7, 0] = 70                                   # a page past the pool (65 pages)
     topk = rng.integers(-3, 1100, (n_tok, k), dtype=np.int32)
-    topk[2, :7] = 16 * 64 + np.arange(7)            # page index 16 >= max_pages
+    topk[2, :min(k, 7)] = 16 * 64 + np.arange(min(k, 7))   # page index 16 >= max_pages
     ttr = rng.integers(0, 8, n_tok).astype(np.int32)
     ttr[5] = 9                                      # request outside the table
     ttr[6] = 7
+    topk[6, 0] = 5                                  # request 7, page 0 -> past the pool
     valid = (rng.random(n_tok) > 0.15).astype(np.uint8)
+    valid[6] = 1
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     lens = torch.zeros(n_tok, dtype=torch.int32, device="cuda")
     out = B.dsv4kv_dequant_gather_topk(layout, dev(pool), dev(topk), dev(ttr), dev(pt), 6,
