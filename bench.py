@@ -522,6 +522,8 @@ def run_ours(args, rank, world):
     store_gbs = STORE_BYTES_PER_ROW * n_store / (store_ms / 1e3) / 1e9
     gather_gbs = GATHER_BYTES_PER_ROW * n_gather / (gather_ms / 1e3) / 1e9
     traffic = _profiled_traffic("compress_store_long_prefill", STORE_SOURCES)
+    step_bytes = STORE_BYTES_PER_ROW * n_store + GATHER_BYTES_PER_ROW * n_gather
+    step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -537,6 +539,12 @@ def run_ours(args, rank, world):
                      "frac": store_gbs / peak, "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": "compress_store_kernel<V41, ratio 2, norm, rope>",
                      "bytes_per_row": STORE_BYTES_PER_ROW, "frac_of_8000": store_gbs / 8000.0},
+        # the whole step against the same peak: both kernels' algorithmic bytes
+        # over the step time (the gathered rows are written with evict-first
+        # stores, so part of their write-back lands in the next store's time)
+        "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
+                          "frac": step_gbs / peak, "peak_kind": peak_kind,
+                          "bytes_per_step": step_bytes},
         "kernels": {
             "compress_store": {"ms": store_ms, "rows_per_s": n_store / (store_ms / 1e3),
                                "gbs": store_gbs},

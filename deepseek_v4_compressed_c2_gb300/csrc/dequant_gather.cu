@@ -23,6 +23,14 @@
 
 namespace dsv4kv {
 
+// Streaming (evict-first) 16-byte store for the gathered rows: an output of
+// about the L2's size that later kernels read at most once per layer, so it
+// should not displace the pool rows and inputs still to be read.
+__device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
 constexpr int kGatherWarps = 8;
 constexpr int kGatherThreads = kGatherWarps * 32;
 constexpr int kRowsPerWarp = 4;
@@ -116,16 +124,16 @@ dequant_gather_kernel(const uint8_t* __restrict__ pool, long long pool_rows, con
         uint4* o = reinterpret_cast<uint4*>(out + i * kDim);
         if (!valid[t]) {
           if (id[t] >= pool_rows && lane == 0 && err) atomicAdd(err, 1);
-          o[lane] = make_uint4(0, 0, 0, 0);
-          o[32 + lane] = make_uint4(0, 0, 0, 0);
+          st_stream_v4(o + lane, make_uint4(0, 0, 0, 0));
+          st_stream_v4(o + 32 + lane, make_uint4(0, 0, 0, 0));
           continue;
         }
         // chunk l: dims 8l..8l+7, group l/4; chunk l+32: group 8 + l/4
         const int sh = 8 * ((lane >> 2) & 3);
         const uint32_t e0 = ((lane < 16 ? sc[t].x : sc[t].y) >> sh) & 0xFFu;
         const uint32_t e1 = ((lane < 16 ? sc[t].z : sc[t].w) >> sh) & 0xFFu;
-        o[lane] = dequant8_v41(c0[t], ue8m0_scale(e0));
-        o[32 + lane] = dequant8_v41(c1[t], ue8m0_scale(e1));
+        st_stream_v4(o + lane, dequant8_v41(c0[t], ue8m0_scale(e0)));
+        st_stream_v4(o + 32 + lane, dequant8_v41(c1[t], ue8m0_scale(e1)));
       }
     } else if constexpr (L == kV4) {
       // half 0: codes of dims 8l.., group l/8; half 1: lanes 0..23 codes of
@@ -152,18 +160,18 @@ dequant_gather_kernel(const uint8_t* __restrict__ pool, long long pool_rows, con
         uint4* o = reinterpret_cast<uint4*>(out + i * kDim);
         if (!valid[t]) {
           if (id[t] >= pool_rows && lane == 0 && err) atomicAdd(err, 1);
-          o[lane] = make_uint4(0, 0, 0, 0);
-          o[32 + lane] = make_uint4(0, 0, 0, 0);
+          st_stream_v4(o + lane, make_uint4(0, 0, 0, 0));
+          st_stream_v4(o + 32 + lane, make_uint4(0, 0, 0, 0));
           continue;
         }
         const int g0 = lane >> 3, g1 = 4 + (lane >> 3);
         const uint32_t e0 = ((g0 < 4 ? sc[t].x : sc[t].y) >> (8 * (g0 & 3))) & 0xFFu;
-        o[lane] = dequant8_v41(c0[t], ue8m0_scale(e0));
+        st_stream_v4(o + lane, dequant8_v41(c0[t], ue8m0_scale(e0)));
         if (lane < 24) {
           const uint32_t e1 = (sc[t].y >> (8 * (g1 & 3))) & 0xFFu;
-          o[32 + lane] = dequant8_v41(c1[t], ue8m0_scale(e1));
+          st_stream_v4(o + 32 + lane, dequant8_v41(c1[t], ue8m0_scale(e1)));
         } else {
-          o[32 + lane] = make_uint4(c1[t].x, c1[t].y, c2[t].x, c2[t].y);
+          st_stream_v4(o + 32 + lane, make_uint4(c1[t].x, c1[t].y, c2[t].x, c2[t].y));
         }
       }
     } else {
@@ -186,12 +194,12 @@ dequant_gather_kernel(const uint8_t* __restrict__ pool, long long pool_rows, con
         uint4* o = reinterpret_cast<uint4*>(out + i * kDim);
         if (!valid[t]) {
           if (id[t] >= pool_rows && lane == 0 && err) atomicAdd(err, 1);
-          o[lane] = make_uint4(0, 0, 0, 0);
-          o[32 + lane] = make_uint4(0, 0, 0, 0);
+          st_stream_v4(o + lane, make_uint4(0, 0, 0, 0));
+          st_stream_v4(o + 32 + lane, make_uint4(0, 0, 0, 0));
           continue;
         }
-        o[lane] = dequant8_fp4(c0[t], e4m3_to_f32(s0[t]));
-        o[32 + lane] = dequant8_fp4(c1[t], e4m3_to_f32(s1[t]));
+        st_stream_v4(o + lane, dequant8_fp4(c0[t], e4m3_to_f32(s0[t])));
+        st_stream_v4(o + 32 + lane, dequant8_fp4(c1[t], e4m3_to_f32(s1[t])));
       }
     }
   }
@@ -387,16 +395,16 @@ dequant_gather_tma_kernel(const uint8_t* __restrict__ pool, long long pool_rows,
         if (i >= n) break;
         uint4* o = reinterpret_cast<uint4*>(out + i * kDim);
         if (sl[q] < 0) {
-          o[lane] = make_uint4(0, 0, 0, 0);
-          o[32 + lane] = make_uint4(0, 0, 0, 0);
+          st_stream_v4(o + lane, make_uint4(0, 0, 0, 0));
+          st_stream_v4(o + 32 + lane, make_uint4(0, 0, 0, 0));
           continue;
         }
         // chunk l: dims 8l..8l+7, group l/4; chunk l+32: group 8 + l/4
         const int sh = 8 * ((lane >> 2) & 3);
         const uint32_t e0 = ((lane < 16 ? sc[q].x : sc[q].y) >> sh) & 0xFFu;
         const uint32_t e1 = ((lane < 16 ? sc[q].z : sc[q].w) >> sh) & 0xFFu;
-        o[lane] = dequant8_v41(c0[q], ue8m0_scale(e0));
-        o[32 + lane] = dequant8_v41(c1[q], ue8m0_scale(e1));
+        st_stream_v4(o + lane, dequant8_v41(c0[q], ue8m0_scale(e0)));
+        st_stream_v4(o + 32 + lane, dequant8_v41(c1[q], ue8m0_scale(e1)));
       }
     } else {
       uint32_t c0[kTmaRowsPerWarp], c1[kTmaRowsPerWarp], s0[kTmaRowsPerWarp], s1[kTmaRowsPerWarp];
@@ -421,12 +429,12 @@ dequant_gather_tma_kernel(const uint8_t* __restrict__ pool, long long pool_rows,
         if (i >= n) break;
         uint4* o = reinterpret_cast<uint4*>(out + i * kDim);
         if (sl[q] < 0) {
-          o[lane] = make_uint4(0, 0, 0, 0);
-          o[32 + lane] = make_uint4(0, 0, 0, 0);
+          st_stream_v4(o + lane, make_uint4(0, 0, 0, 0));
+          st_stream_v4(o + 32 + lane, make_uint4(0, 0, 0, 0));
           continue;
         }
-        o[lane] = dequant8_fp4(c0[q], e4m3_to_f32(s0[q]));
-        o[32 + lane] = dequant8_fp4(c1[q], e4m3_to_f32(s1[q]));
+        st_stream_v4(o + lane, dequant8_fp4(c0[q], e4m3_to_f32(s0[q])));
+        st_stream_v4(o + 32 + lane, dequant8_fp4(c1[q], e4m3_to_f32(s1[q])));
       }
     }
   }
