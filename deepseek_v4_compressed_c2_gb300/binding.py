@@ -40,7 +40,8 @@ class dsv4kv_kvbuf(ctypes.Structure):
     _fields_ = [("storage", ctypes.c_void_p), ("capacity_rows", ctypes.c_longlong),
                 ("head_valid", ctypes.c_int), ("head_layout", ctypes.c_int),
                 ("head_pool", ctypes.c_void_p), ("head_pool_rows", ctypes.c_longlong),
-                ("head_ids", ctypes.c_void_p), ("head_n", ctypes.c_longlong)]
+                ("head_ids", ctypes.c_void_p), ("head_n", ctypes.c_longlong),
+                ("head_map", ctypes.c_ulonglong)]
 
 
 def lib():

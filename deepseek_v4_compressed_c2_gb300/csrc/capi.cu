@@ -245,6 +245,7 @@ int dsv4kv_kvbuf_init(dsv4kv_kvbuf* buf, void* storage_bf16, long long capacity_
   buf->head_pool_rows = 0;
   buf->head_ids = nullptr;
   buf->head_n = 0;
+  buf->head_map = 0;
   return DSV4KV_OK;
 }
 
@@ -260,12 +261,16 @@ int dsv4kv_kvbuf_get(dsv4kv_kvbuf* buf, long long n, void** rows) {
   return DSV4KV_OK;
 }
 
-int dsv4kv_kvbuf_lookup(dsv4kv_kvbuf* buf, int layout, const void* pool, long long pool_rows,
-                        const int* ids, long long n, int* hit) {
+}  // extern "C"
+
+// The head decision with the mapping fingerprint (0: plain ids).
+static int kvbuf_lookup_map(dsv4kv_kvbuf* buf, int layout, const void* pool, long long pool_rows,
+                            const int* ids, long long n, unsigned long long map, int* hit) {
   if (!buf || !hit || n < 0) return DSV4KV_EINVAL;
   if (n > buf->capacity_rows) return DSV4KV_ERANGE;
   const bool same = buf->head_valid && buf->head_layout == layout && buf->head_pool == pool &&
-                    buf->head_pool_rows == pool_rows && buf->head_ids == ids && buf->head_n == n;
+                    buf->head_pool_rows == pool_rows && buf->head_ids == ids && buf->head_n == n &&
+                    buf->head_map == map;
   if (same) {
     *hit = 1;
     return DSV4KV_OK;
@@ -277,7 +282,34 @@ int dsv4kv_kvbuf_lookup(dsv4kv_kvbuf* buf, int layout, const void* pool, long lo
   buf->head_pool_rows = pool_rows;
   buf->head_ids = ids;
   buf->head_n = n;
+  buf->head_map = map;
   return DSV4KV_OK;
+}
+
+// FNV-1a over the top-k form's mapping arguments; never 0 (0 marks plain ids).
+static unsigned long long topk_map_fingerprint(const int* token_to_req,
+                                               const unsigned char* is_valid,
+                                               const int* page_table, int n_req, int max_pages,
+                                               int page_bits, int k) {
+  const unsigned long long words[7] = {
+      (unsigned long long)(uintptr_t)token_to_req, (unsigned long long)(uintptr_t)is_valid,
+      (unsigned long long)(uintptr_t)page_table, (unsigned long long)(unsigned)n_req,
+      (unsigned long long)(unsigned)max_pages, (unsigned long long)(unsigned)page_bits,
+      (unsigned long long)(unsigned)k};
+  unsigned long long h = 1469598103934665603ull;
+  for (unsigned long long w : words)
+    for (int b = 0; b < 8; ++b) {
+      h ^= (w >> (8 * b)) & 0xFFu;
+      h *= 1099511628211ull;
+    }
+  return h | 1ull;
+}
+
+extern "C" {
+
+int dsv4kv_kvbuf_lookup(dsv4kv_kvbuf* buf, int layout, const void* pool, long long pool_rows,
+                        const int* ids, long long n, int* hit) {
+  return kvbuf_lookup_map(buf, layout, pool, pool_rows, ids, n, 0ull, hit);
 }
 
 int dsv4kv_kvbuf_get_with_head(dsv4kv_kvbuf* buf, int layout, const void* pool,
@@ -306,7 +338,10 @@ int dsv4kv_kvbuf_get_with_head_topk(dsv4kv_kvbuf* buf, int layout, const void* p
   const long long n = (long long)n_tok * k;
   st = check_gather(layout, pool, pool_rows, topk, n, buf->storage);
   if (st != DSV4KV_OK) return st;
-  st = dsv4kv_kvbuf_lookup(buf, layout, pool, pool_rows, topk, n, hit);
+  st = kvbuf_lookup_map(buf, layout, pool, pool_rows, topk, n,
+                        topk_map_fingerprint(token_to_req, is_valid, page_table, n_req, max_pages,
+                                             page_bits, k),
+                        hit);
   if (st != DSV4KV_OK) return st;
   if (rows) *rows = buf->storage;
   if (*hit || n == 0) return DSV4KV_OK;

@@ -293,6 +293,7 @@ typedef struct dsv4kv_kvbuf {
     long long head_pool_rows;
     const int *head_ids;
     long long head_n;
+    unsigned long long head_map;   /* top-k form: fingerprint of the id mapping; 0 for ids */
 } dsv4kv_kvbuf;
 
 /* (Re)initialise: set storage and capacity, forget the head.  Host only. */
@@ -319,9 +320,12 @@ int dsv4kv_kvbuf_get_with_head(dsv4kv_kvbuf *buf, int layout, const void *pool,
                                void **rows, int *hit, int *err_word, void *stream);
 
 /* get_with_head whose gather ids are request-local top-k ids: the head is
- * (layout, pool, pool_rows, topk pointer, n_tok * k); on a miss runs
- * dsv4kv_dequant_gather_topk into the storage (lens as there, written only on
- * a miss), on a hit launches nothing. */
+ * (layout, pool, pool_rows, topk pointer, n_tok * k) plus a fingerprint of
+ * the mapping arguments (token_to_req, is_valid and page_table pointers,
+ * n_req, max_pages, page_bits, k), so the same top-k buffer mapped through
+ * another table is a miss; on a miss runs dsv4kv_dequant_gather_topk into
+ * the storage (lens as there, written only on a miss), on a hit launches
+ * nothing. */
 int dsv4kv_kvbuf_get_with_head_topk(dsv4kv_kvbuf *buf, int layout, const void *pool,
                                     long long pool_rows, const int *topk, int n_tok, int k,
                                     const int *token_to_req, const unsigned char *is_valid,

@@ -168,3 +168,32 @@ def test_ring_and_fused_gather_reject_bad_arguments(B):
     assert g(1, FAKE, 10, FAKE, 4, 8, FAKE, None, FAKE, 2, 2, 6, FAKE + 8, None, None, None) == -1
     assert g(7, FAKE, 10, FAKE, 4, 8, FAKE, None, FAKE, 2, 2, 6, FAKE, None, None, None) == -1
     assert g(1, FAKE, 10, FAKE, 0, 8, FAKE, None, FAKE, 2, 2, 6, FAKE, None, None, None) == 0
+
+
+def test_topk_reuse_head_covers_the_id_mapping(B):
+    """The top-k form's head includes the mapping arguments: the same top-k
+    buffer through another page table, token map, validity mask, page size or
+    k is a miss.  n_tok = 0 rows, so nothing is launched."""
+    L = B.lib()
+    buf = B.dsv4kv_kvbuf()
+    assert L.dsv4kv_kvbuf_init(ctypes.byref(buf), FAKE, 64) == 0
+    rows, hit, lens = ctypes.c_void_p(), ctypes.c_int(), ctypes.c_int()
+    base = [1, FAKE, 1000, FAKE + 256, 0, 8, FAKE + 512, None, FAKE + 1024, 4, 16, 6]
+
+    def call(**kw):
+        a = list(base)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        st = L.dsv4kv_kvbuf_get_with_head_topk(ctypes.byref(buf), *a, ctypes.byref(rows), None,
+                                               ctypes.byref(hit), None, None)
+        assert st == 0
+        return hit.value
+
+    assert call() == 0 and call() == 1                       # same source: hit
+    assert call(a8=FAKE + 2048) == 0 and call(a8=FAKE + 2048) == 1   # other page table
+    assert call(a6=FAKE + 4096) == 0                         # other token -> request map
+    assert call(a7=FAKE + 8192) == 0                         # a validity mask
+    assert call(a11=5) == 0                                  # other page size
+    assert call(a5=7) == 0                                   # other k (n_tok * k still 0)
+    L.dsv4kv_kvbuf_begin_forward(ctypes.byref(buf))
+    assert call() == 0 and call() == 1
