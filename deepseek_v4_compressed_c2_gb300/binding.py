@@ -113,6 +113,16 @@ def _need(t, dtype, name):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _pool_rows(pool, layout, pool_rows):
+    """Rows of the layout the pool tensor holds, or a checked explicit count."""
+    pool_bytes = pool.numel() * pool.element_size()
+    if pool_rows is None:
+        return pool_bytes // _ROW_BYTES.get(layout, 1)
+    if pool_rows * _ROW_BYTES.get(layout, 0) > pool_bytes:
+        raise ValueError("pool_rows exceeds the pool tensor")
+    return pool_rows
+
+
 def dsv4kv_row_bytes(layout: int) -> int:
     rb = lib().dsv4kv_row_bytes(layout)
     _check("dsv4kv_row_bytes", rb if rb < 0 else 0)
@@ -154,11 +164,7 @@ def dsv4kv_compress_store(layout, ratio, rows, extend_offsets, pool, *, score=No
         if out_loc is None:
             raise ValueError("n_out is required when out_loc is None")
         n_out = out_loc.numel()
-    pool_bytes = pool.numel() * pool.element_size()
-    if pool_rows is None:
-        pool_rows = pool_bytes // _ROW_BYTES.get(layout, 1)
-    elif pool_rows * _ROW_BYTES.get(layout, 0) > pool_bytes:
-        raise ValueError("pool_rows exceeds the pool tensor")
+    pool_rows = _pool_rows(pool, layout, pool_rows)
     if out_loc is not None and out_loc.numel() < n_out:
         raise ValueError("out_loc has fewer than n_out entries")
     for name, t in (("latent_out", latent_out), ("prequant_out", prequant_out)):
@@ -203,11 +209,7 @@ def dsv4kv_dequant_gather(layout, pool, ids, out=None, *, pool_rows=None, err_wo
         out = torch.empty((n, DIM), dtype=torch.bfloat16, device=ids.device)
     elif out.numel() < n * DIM or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor of >= n x 512")
-    pool_bytes = pool.numel() * pool.element_size()
-    if pool_rows is None:
-        pool_rows = pool_bytes // _ROW_BYTES.get(layout, 1)
-    elif pool_rows * _ROW_BYTES.get(layout, 0) > pool_bytes:
-        raise ValueError("pool_rows exceeds the pool tensor")
+    pool_rows = _pool_rows(pool, layout, pool_rows)
     st = lib().dsv4kv_dequant_gather(layout, _ptr(pool), pool_rows, _ptr(ids), n, _ptr(out),
                                      _ptr(err_word), _stream(stream))
     _check("dsv4kv_dequant_gather", st)
@@ -217,14 +219,7 @@ def dsv4kv_dequant_gather(layout, pool, ids, out=None, *, pool_rows=None, err_wo
 def dsv4kv_topk_to_slots(topk, token_to_req, page_table, page_bits, *, is_valid=None,
                          slots=None, lens=None, err_word=None, stream=None):
     """Request-local top-k ids -> pool slots (int32 [n_tok, k]) and lens."""
-    _need(topk, torch.int32, "topk")
-    _need(token_to_req, torch.int32, "token_to_req")
-    _need(page_table, torch.int32, "page_table")
-    _need(is_valid, torch.uint8, "is_valid")
-    n_tok, k = topk.shape
-    if not (topk.is_contiguous() and page_table.is_contiguous()) or token_to_req.numel() < n_tok \
-            or (is_valid is not None and is_valid.numel() < n_tok):
-        raise ValueError("topk / page_table must be contiguous; token_to_req, is_valid >= n_tok")
+    n_tok, k = _topk_args(topk, token_to_req, page_table, is_valid)
     if slots is None:
         slots = torch.empty((n_tok, k), dtype=torch.int32, device=topk.device)
     if lens is None:
@@ -264,11 +259,7 @@ def dsv4kv_dequant_gather_topk(layout, pool, topk, token_to_req, page_table, pag
         raise ValueError("out must be a contiguous tensor of >= n_tok * k x 512")
     if lens is not None and lens.numel() < n_tok:
         raise ValueError("lens must hold n_tok counts")
-    pool_bytes = pool.numel() * pool.element_size()
-    if pool_rows is None:
-        pool_rows = pool_bytes // _ROW_BYTES.get(layout, 1)
-    elif pool_rows * _ROW_BYTES.get(layout, 0) > pool_bytes:
-        raise ValueError("pool_rows exceeds the pool tensor")
+    pool_rows = _pool_rows(pool, layout, pool_rows)
     st = lib().dsv4kv_dequant_gather_topk(layout, _ptr(pool), pool_rows, _ptr(topk), n_tok, k,
                                           _ptr(token_to_req), _ptr(is_valid), _ptr(page_table),
                                           page_table.shape[0], page_table.shape[1], page_bits,
@@ -313,11 +304,7 @@ class SparsePrefillKVBuffer:
                                    stream=None):
         """(rows, hit): on a miss the gather-dequant fills the storage."""
         n = ids.numel()
-        pool_bytes = pool.numel() * pool.element_size()
-        if pool_rows is None:
-            pool_rows = pool_bytes // _ROW_BYTES.get(layout, 1)
-        elif pool_rows * _ROW_BYTES.get(layout, 0) > pool_bytes:
-            raise ValueError("pool_rows exceeds the pool tensor")
+        pool_rows = _pool_rows(pool, layout, pool_rows)
         if not ids.is_contiguous():
             raise ValueError("ids must be contiguous")
         p = ctypes.c_void_p()
@@ -336,11 +323,7 @@ class SparsePrefillKVBuffer:
         """(rows, hit) with request-local top-k ids as the gather ids; on a
         miss the fused top-k gather-dequant fills the storage."""
         n_tok, k = _topk_args(topk, token_to_req, page_table, is_valid)
-        pool_bytes = pool.numel() * pool.element_size()
-        if pool_rows is None:
-            pool_rows = pool_bytes // _ROW_BYTES.get(layout, 1)
-        elif pool_rows * _ROW_BYTES.get(layout, 0) > pool_bytes:
-            raise ValueError("pool_rows exceeds the pool tensor")
+        pool_rows = _pool_rows(pool, layout, pool_rows)
         p = ctypes.c_void_p()
         hit = ctypes.c_int(0)
         st = lib().dsv4kv_kvbuf_get_with_head_topk(
