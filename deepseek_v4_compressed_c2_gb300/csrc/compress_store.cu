@@ -653,6 +653,7 @@ compress_store_kernel(const StoreParams p) {
     *s_abort = 0;
     mbar_fence_init();
   }
+  grid_dependency_wait();
   volatile int* abort = s_abort;
   if (!block_plan<RATIO, TL::kThreads>(p.ext, p.start_pos, p.n_slots, s_base, s_first, s_start, s_count, s_plan,
                          abort, p.err))
@@ -746,12 +747,14 @@ compress_store_kernel(const StoreParams p) {
         }
       }
     }
+    allow_dependent_launch();
   } else {
     // ------------------------------------------------------------ consumers
     if constexpr (RATIO == 2 && RING)
       ring_phase<L, NORM, ROPE, TL::kWarps>(p, s_base, s_first, s_start, s_count, warp, lane);
     consume_tiles<L, RATIO, NORM, ROPE, SHAPE>(p, s_stage, s_desc, s_full, s_empty, abort, n_tiles,
                                                warp, lane);
+    allow_dependent_launch();
   }
 }
 
@@ -789,8 +792,7 @@ static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
   const long long tiles = ((long long)p.n_out + TL::kRows - 1) / TL::kRows;
   const long long cap = (long long)device_sm_count() * (per_sm > 0 ? per_sm : 1);
   const int grid = (int)(tiles < cap ? tiles : cap);
-  kern<<<grid, TL::kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, TL::kThreads, smem, stream, p);
 }
 
 template <int L, int RATIO, bool RING, int SHAPE>

@@ -312,6 +312,7 @@ dequant_gather_tma_kernel(const uint8_t* __restrict__ pool, long long pool_rows,
     mbar_fence_init();
   }
   __syncthreads();
+  grid_dependency_wait();
   volatile int* abort = s_abort;
   const long long n_tiles = (n + kTmaRows - 1) / kTmaRows;
   const long long step = gridDim.x;
@@ -362,6 +363,7 @@ dequant_gather_tma_kernel(const uint8_t* __restrict__ pool, long long pool_rows,
         }
       }
     }
+    allow_dependent_launch();
     return;
   }
 
@@ -438,6 +440,7 @@ dequant_gather_tma_kernel(const uint8_t* __restrict__ pool, long long pool_rows,
       }
     }
   }
+  allow_dependent_launch();
 }
 
 template <int L, bool TOPK>
@@ -460,8 +463,7 @@ static cudaError_t launch_tma(const uint8_t* pool, long long pool_rows, const Ga
   const long long tiles = (n + kTmaRows - 1) / kTmaRows;
   const long long cap = (long long)device_sm_count() * (per_sm > 0 ? per_sm : 1);
   const int grid = (int)(tiles < cap ? tiles : cap);
-  kern<<<grid, kTmaThreads, GT::kSmem, s>>>(pool, pool_rows, g, n, out, err);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, kTmaThreads, GT::kSmem, s, pool, pool_rows, g, n, out, err);
 }
 
 template <int L, bool TOPK>

@@ -40,6 +40,25 @@ struct StoreParams {
 
 cudaError_t launch_compress_store(const StoreParams& p, int layout, int ratio, cudaStream_t stream);
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel in the stream finishes; it waits
+// (grid_dependency_wait) before touching global memory.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), int grid, int block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_dequant_gather(int layout, const uint8_t* pool, long long pool_rows,
                                   const int* ids, long long n, __nv_bfloat16* out, int* err,
                                   cudaStream_t stream);

@@ -77,6 +77,20 @@ __device__ __forceinline__ void st_shared_s64(long long* p, long long v) {
   asm volatile("st.shared.b64 [%0], %1;" :: "r"(smem_u32(p)), "l"(v) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization (launch_dependent) may start while the previous kernel in
+// the stream is finishing; every thread waits in grid_dependency_wait before
+// its first global memory access, so what the previous kernel wrote is
+// complete and visible.  allow_dependent_launch lets the next such kernel
+// start once every CTA of this one has called it or exited.  Both are no-ops
+// in a normal launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // L2 policy for data read exactly once
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
