@@ -546,3 +546,50 @@ def test_guard_regions_around_pool_output_and_ring_stay_untouched(B, layout):
     assert bool((big[:G] == 0x5C).all()) and bool((big[G + pool_bytes:] == 0x5C).all())
     assert bool((ring_big[:G] == 0x1234).all()) and bool((ring_big[G + cfg["ring"].size:] == 0x1234).all())
     assert bool((out_big[:512] == 0x3A3A).all()) and bool((out_big[512 + len(ids) * 512:] == 0x3A3A).all())
+
+
+def test_back_to_back_launches_see_the_previous_kernels_writes(B):
+    """The store and the gather are launched to start early (programmatic
+    dependent launch) and must still see what the kernel just before them
+    wrote.  Each round: a torch kernel writes the store's input rows (a row
+    permutation), the store writes the pool, the gather reads the rows just
+    stored, the next round's torch kernel overwrites the inputs -- with no
+    synchronisation anywhere.  The results equal a run synchronised after
+    every launch."""
+    cfg = W.cfg2_ratio2_small()
+    base = dev_bf16(cfg["rows"])
+    ext, pt = dev(cfg["ext"]), dev(cfg["page_table"])
+    w, fr = dev_bf16(cfg["norm_w"]), dev(cfg["freqs"])
+    plan = oracle.plan(2, cfg["ext"], cfg["page_table"], cfg["page_bits"])
+    ids = dev(np.ascontiguousarray(plan["slot"][:plan["total"]]).astype(np.int32))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    rounds = 6
+    perms = [torch.randperm(base.shape[0], generator=g, device="cuda") for _ in range(rounds)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run(sync):
+        rows = torch.empty_like(base)
+        pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device="cuda")
+        outs = [torch.empty((ids.numel(), 512), dtype=torch.bfloat16, device="cuda")
+                for _ in range(rounds)]
+        for r in range(rounds):
+            torch.index_select(base, 0, perms[r], out=rows)
+            if sync:
+                torch.cuda.synchronize()
+            B.dsv4kv_compress_store(1, 2, rows, ext, pool, page_table=pt, page_bits=cfg["page_bits"],
+                                    rmsnorm_w=w, eps=cfg["eps"], freqs_cis=fr,
+                                    n_out=cfg["n_out"], err_word=err)
+            if sync:
+                torch.cuda.synchronize()
+            B.dsv4kv_dequant_gather(1, pool, ids, outs[r], err_word=err)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return [host_u16(o) for o in outs]
+
+    fast, slow = run(False), run(True)
+    assert int(err.item()) == 0
+    for r in range(rounds):
+        assert np.array_equal(fast[r], slow[r]), f"round {r}"
+    assert not np.array_equal(slow[0], slow[1])          # the rounds do differ
