@@ -274,7 +274,7 @@ def cold_gather(B, dev, stream, reps):
     return res
 
 
-def decode_verify_steps(B, dev, stream, reps=50):
+def decode_verify_steps(B, dev, stream, reps=50, max_prefix=4096):
     """The ring form of the compressor on decode-shaped steps (one new token
     per request; 1 + 3 draft tokens per request).  These are small,
     latency-bound launches (working set in L2).  The serving loop runs them
@@ -286,7 +286,8 @@ def decode_verify_steps(B, dev, stream, reps=50):
     from deepseek_v4_compressed_c2_gb300 import workloads as W
     res = {}
     for name, n_req, n_new in (("decode_4096req_1tok", 4096, 1), ("verify_1024req_4tok", 1024, 4)):
-        cfg = W.decode_verify(seed=13, n_req=n_req, n_new=n_new, ring_size=4, max_prefix=4096)
+        cfg = W.decode_verify(seed=13, n_req=n_req, n_new=n_new, ring_size=4,
+                              max_prefix=max_prefix)
         bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
         pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device=dev)
         ring = bf(cfg["ring"])
@@ -508,7 +509,7 @@ def run_ours(args, rank, world):
     cold = None
     if not args.no_cold_gather:
         cold = cold_gather(B, dev, stream, max(5, min(args.steps, 50)))
-        decode = decode_verify_steps(B, dev, stream)
+        decode = decode_verify_steps(B, dev, stream, max_prefix=args.decode_prefix)
     else:
         decode = None
 
@@ -572,12 +573,28 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cold-gather", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="diagnostic: only the decode / verify ring-form launches, one JSON line")
+    ap.add_argument("--decode-prefix", type=int, default=4096,
+                    help="cached prefix bound of the decode / verify requests (sizes their pool)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.decode_only:
+        import torch
+        from deepseek_v4_compressed_c2_gb300 import binding as B
+        B.lib()
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        torch.cuda.set_device(dev)
+        res = decode_verify_steps(B, dev, torch.cuda.Stream(device=dev),
+                                  max_prefix=args.decode_prefix)
+        if rank == 0:
+            print(json.dumps({"decode_verify_ring": res, "decode_prefix": args.decode_prefix}),
+                  flush=True)
         return
     if world > 1:
         import torch
