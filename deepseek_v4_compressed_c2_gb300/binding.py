@@ -70,6 +70,11 @@ def lib():
             "dsv4kv_kvbuf_get_with_head_topk": (I, [KB, I, P, LL, P, I, I, P, P, P, I, I, I,
                                                     ctypes.POINTER(ctypes.c_void_p), P,
                                                     ctypes.POINTER(ctypes.c_int), P, P]),
+            "dsv4kv_kvbuf_get_with_head_all": (I, [KB, I, P, LL, P, I, I, P, P, P, I, I, I,
+                                                   ctypes.POINTER(ctypes.c_void_p), P,
+                                                   ctypes.POINTER(ctypes.c_int), P, P]),
+            "dsv4kv_fill_all_compressed_indices": (I, [P, I, I, P, P]),
+            "dsv4kv_dequant_gather_all": (I, [I, P, LL, P, I, I, P, P, P, I, I, I, P, P, P, P]),
             "dsv4kv_selftest_bounded_wait": (I, [I, P, P, P]),
             "dsv4kv_selftest_fp4_quotient": (I, [P, P, LL, P, P, P]),
             "dsv4kv_kvbuf_init": (I, [KB, P, LL]),
@@ -268,6 +273,60 @@ def dsv4kv_dequant_gather_topk(layout, pool, topk, token_to_req, page_table, pag
     return out
 
 
+def dsv4kv_fill_all_compressed_indices(lens_in, k, out=None, *, stream=None):
+    """Short-context ids: int32 [n_tok, k], row t = 0 .. lens_in[t]-1 then -1."""
+    _need(lens_in, torch.int32, "lens_in")
+    _need(out, torch.int32, "out")
+    n_tok = lens_in.numel()
+    if not lens_in.is_contiguous():
+        raise ValueError("lens_in must be contiguous")
+    if out is None:
+        out = torch.empty((n_tok, k), dtype=torch.int32, device=lens_in.device)
+    elif out.numel() < n_tok * k or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of >= n_tok x k")
+    st = lib().dsv4kv_fill_all_compressed_indices(_ptr(out), n_tok, k, _ptr(lens_in),
+                                                  _stream(stream))
+    _check("dsv4kv_fill_all_compressed_indices", st)
+    return out
+
+
+def _all_args(lens_in, token_to_req, page_table, is_valid):
+    _need(lens_in, torch.int32, "lens_in")
+    _need(token_to_req, torch.int32, "token_to_req")
+    _need(page_table, torch.int32, "page_table")
+    _need(is_valid, torch.uint8, "is_valid")
+    n_tok = lens_in.numel()
+    if not (lens_in.is_contiguous() and page_table.is_contiguous()) \
+            or token_to_req.numel() < n_tok or (is_valid is not None and is_valid.numel() < n_tok):
+        raise ValueError("lens_in / page_table must be contiguous; token_to_req, is_valid >= n_tok")
+    return n_tok
+
+
+def dsv4kv_dequant_gather_all(layout, pool, lens_in, k, token_to_req, page_table, page_bits,
+                              out=None, *, is_valid=None, lens=None, pool_rows=None,
+                              err_word=None, stream=None):
+    """Fused short-context gather: row t*k + j = compressed row j of token t's
+    request when j < lens_in[t], else zeros; returns out [n_tok * k, 512]."""
+    n_tok = _all_args(lens_in, token_to_req, page_table, is_valid)
+    _need(out, torch.bfloat16, "out")
+    _need(lens, torch.int32, "lens")
+    _need(err_word, torch.int32, "err_word")
+    n = n_tok * k
+    if out is None:
+        out = torch.empty((n, DIM), dtype=torch.bfloat16, device=lens_in.device)
+    elif out.numel() < n * DIM or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of >= n_tok * k x 512")
+    if lens is not None and lens.numel() < n_tok:
+        raise ValueError("lens must hold n_tok counts")
+    pool_rows = _pool_rows(pool, layout, pool_rows)
+    st = lib().dsv4kv_dequant_gather_all(layout, _ptr(pool), pool_rows, _ptr(lens_in), n_tok, k,
+                                         _ptr(token_to_req), _ptr(is_valid), _ptr(page_table),
+                                         page_table.shape[0], page_table.shape[1], page_bits,
+                                         _ptr(out), _ptr(lens), _ptr(err_word), _stream(stream))
+    _check("dsv4kv_dequant_gather_all", st)
+    return out
+
+
 class SparsePrefillKVBuffer:
     """The shared bf16 buffer sparse-prefill layers read, with the reuse head
     (sglang PR #45909).  Wraps a caller-owned dsv4kv_kvbuf struct and a
@@ -332,6 +391,24 @@ class SparsePrefillKVBuffer:
             page_table.shape[1], page_bits, ctypes.byref(p), _ptr(lens), ctypes.byref(hit),
             _ptr(err_word), _stream(stream))
         _check("dsv4kv_kvbuf_get_with_head_topk", st)
+        if not hit.value and n_tok * k > 0:
+            self.dequants += 1
+        return self.storage[:n_tok * k], bool(hit.value)
+
+    def dsv4kv_kvbuf_get_with_head_all(self, layout, pool, lens_in, k, token_to_req, page_table,
+                                       page_bits, *, is_valid=None, lens=None, pool_rows=None,
+                                       err_word=None, stream=None):
+        """(rows, hit) with the short-context ids (dsv4kv_dequant_gather_all)."""
+        n_tok = _all_args(lens_in, token_to_req, page_table, is_valid)
+        pool_rows = _pool_rows(pool, layout, pool_rows)
+        p = ctypes.c_void_p()
+        hit = ctypes.c_int(0)
+        st = lib().dsv4kv_kvbuf_get_with_head_all(
+            ctypes.byref(self.buf), layout, _ptr(pool), pool_rows, _ptr(lens_in), n_tok, k,
+            _ptr(token_to_req), _ptr(is_valid), _ptr(page_table), page_table.shape[0],
+            page_table.shape[1], page_bits, ctypes.byref(p), _ptr(lens), ctypes.byref(hit),
+            _ptr(err_word), _stream(stream))
+        _check("dsv4kv_kvbuf_get_with_head_all", st)
         if not hit.value and n_tok * k > 0:
             self.dequants += 1
         return self.storage[:n_tok * k], bool(hit.value)

@@ -191,9 +191,38 @@ int dsv4kv_dequant_gather_topk(int layout, const void* pool, long long pool_rows
   if (st != DSV4KV_OK || n == 0) return st;
   if ((uintptr_t)lens & 3u) return DSV4KV_EINVAL;
   return cuda_status(launch_dequant_gather_topk(
-      layout, static_cast<const uint8_t*>(pool), pool_rows, topk, n_tok, k, token_to_req, is_valid,
-      page_table, n_req, max_pages, page_bits, static_cast<__nv_bfloat16*>(out_bf16), lens,
-      err_word, static_cast<cudaStream_t>(stream)));
+      layout, static_cast<const uint8_t*>(pool), pool_rows, topk, nullptr, n_tok, k, token_to_req,
+      is_valid, page_table, n_req, max_pages, page_bits, static_cast<__nv_bfloat16*>(out_bf16),
+      lens, err_word, static_cast<cudaStream_t>(stream)));
+}
+
+int dsv4kv_dequant_gather_all(int layout, const void* pool, long long pool_rows,
+                              const int* lens_in, int n_tok, int k, const int* token_to_req,
+                              const unsigned char* is_valid, const int* page_table, int n_req,
+                              int max_pages, int page_bits, void* out_bf16, int* lens,
+                              int* err_word, void* stream) {
+  // the top-k checks with lens_in standing where the ids would be
+  int st = check_topk(lens_in, n_tok, k, token_to_req, page_table, n_req, max_pages, page_bits);
+  if (st != DSV4KV_OK) return st;
+  const long long n = (long long)n_tok * k;
+  st = check_gather(layout, pool, pool_rows, lens_in, n, out_bf16);
+  if (st != DSV4KV_OK || n == 0) return st;
+  if ((uintptr_t)lens & 3u) return DSV4KV_EINVAL;
+  return cuda_status(launch_dequant_gather_topk(
+      layout, static_cast<const uint8_t*>(pool), pool_rows, nullptr, lens_in, n_tok, k,
+      token_to_req, is_valid, page_table, n_req, max_pages, page_bits,
+      static_cast<__nv_bfloat16*>(out_bf16), lens, err_word, static_cast<cudaStream_t>(stream)));
+}
+
+int dsv4kv_fill_all_compressed_indices(int* topk_out, int n_tok, int k, const int* lens_in,
+                                       void* stream) {
+  if (n_tok < 0 || k < 0) return DSV4KV_EINVAL;
+  if (k > 65536) return DSV4KV_ERANGE;
+  if (n_tok == 0 || k == 0) return DSV4KV_OK;
+  if (!topk_out || !lens_in || ((uintptr_t)topk_out & 3u) || ((uintptr_t)lens_in & 3u))
+    return DSV4KV_EINVAL;
+  return cuda_status(launch_fill_all_indices(topk_out, n_tok, k, lens_in,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 int dsv4kv_topk_to_slots(const int* topk, int n_tok, int k, const int* token_to_req,
@@ -323,6 +352,33 @@ int dsv4kv_kvbuf_get_with_head(dsv4kv_kvbuf* buf, int layout, const void* pool,
   if (rows) *rows = buf->storage;
   if (*hit || n == 0) return DSV4KV_OK;
   st = dsv4kv_dequant_gather(layout, pool, pool_rows, ids, n, buf->storage, err_word, stream);
+  if (st != DSV4KV_OK) buf->head_valid = 0;
+  return st;
+}
+
+int dsv4kv_kvbuf_get_with_head_all(dsv4kv_kvbuf* buf, int layout, const void* pool,
+                                   long long pool_rows, const int* lens_in, int n_tok, int k,
+                                   const int* token_to_req, const unsigned char* is_valid,
+                                   const int* page_table, int n_req, int max_pages, int page_bits,
+                                   void** rows, int* lens, int* hit, int* err_word, void* stream) {
+  if (!buf || !hit) return DSV4KV_EINVAL;
+  int st = check_topk(lens_in, n_tok, k, token_to_req, page_table, n_req, max_pages, page_bits);
+  if (st != DSV4KV_OK) return st;
+  const long long n = (long long)n_tok * k;
+  st = check_gather(layout, pool, pool_rows, lens_in, n, buf->storage);
+  if (st != DSV4KV_OK) return st;
+  // the short-context form's fingerprint differs from the top-k form's for
+  // the same pointers (its "ids" pointer is the lengths array)
+  const unsigned long long map =
+      topk_map_fingerprint(token_to_req, is_valid, page_table, n_req, max_pages, page_bits, k) ^
+      0x5a5a5a5a5a5a5a5aull;
+  st = kvbuf_lookup_map(buf, layout, pool, pool_rows, lens_in, n, map | 1ull, hit);
+  if (st != DSV4KV_OK) return st;
+  if (rows) *rows = buf->storage;
+  if (*hit || n == 0) return DSV4KV_OK;
+  st = dsv4kv_dequant_gather_all(layout, pool, pool_rows, lens_in, n_tok, k, token_to_req,
+                                 is_valid, page_table, n_req, max_pages, page_bits, buf->storage,
+                                 lens, err_word, stream);
   if (st != DSV4KV_OK) buf->head_valid = 0;
   return st;
 }

@@ -40,7 +40,8 @@ constexpr int kRowsPerWarp = 4;
 // topk_to_slots does (flashinfer_sparse.py, _compressed_topk_to_slots).
 struct GatherSrc {
   const int* ids;                  // [n] slots (plain gather)
-  const int* topk;                 // [n_tok, k] request-local compressed ids
+  const int* topk;                 // [n_tok, k] request-local compressed ids, or nullptr:
+  const int* fill_len;             //   short-context form, ids j < fill_len[t] ([n_tok])
   const int* token_to_req;         // [n_tok]
   const unsigned char* is_valid;   // [n_tok] or nullptr
   const int* page_table;           // [n_req, max_pages]
@@ -55,7 +56,7 @@ __device__ __forceinline__ int topk_row_slot(const GatherSrc& g, long long i, in
   const long long t = i / g.k;
   const int c = (int)(i - t * g.k);
   const int r = __ldg(g.token_to_req + t);
-  const int id = __ldg(g.topk + i);
+  const int id = g.topk ? __ldg(g.topk + i) : (c < __ldg(g.fill_len + t) ? c : -1);
   if (r < 0 || r >= g.n_req) {
     if (c == 0 && err) atomicAdd(err, 1);
     return -1;
@@ -252,7 +253,12 @@ __device__ __forceinline__ TopkRaw topk_raw(const GatherSrc& g, long long i, lon
   if (i >= n) return a;
   const long long t = i / g.k;
   a.r = __ldg(g.token_to_req + t);
-  a.id = __ldg(g.topk + i);
+  if (g.topk) {
+    a.id = __ldg(g.topk + i);
+  } else {
+    const int c = (int)(i - t * g.k);
+    a.id = c < __ldg(g.fill_len + t) ? c : -1;
+  }
   a.live = !g.is_valid || g.is_valid[t] != 0;
   return a;
 }
@@ -500,12 +506,14 @@ cudaError_t launch_dequant_gather(int layout, const uint8_t* pool, long long poo
 }
 
 cudaError_t launch_dequant_gather_topk(int layout, const uint8_t* pool, long long pool_rows,
-                                       const int* topk, int n_tok, int k, const int* token_to_req,
-                                       const unsigned char* is_valid, const int* page_table,
-                                       int n_req, int max_pages, int page_bits,
-                                       __nv_bfloat16* out, int* lens, int* err, cudaStream_t s) {
+                                       const int* topk, const int* fill_len, int n_tok, int k,
+                                       const int* token_to_req, const unsigned char* is_valid,
+                                       const int* page_table, int n_req, int max_pages,
+                                       int page_bits, __nv_bfloat16* out, int* lens, int* err,
+                                       cudaStream_t s) {
   GatherSrc g{};
   g.topk = topk;
+  g.fill_len = fill_len;
   g.token_to_req = token_to_req;
   g.is_valid = is_valid;
   g.page_table = page_table;

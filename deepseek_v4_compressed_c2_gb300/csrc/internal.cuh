@@ -63,11 +63,16 @@ cudaError_t launch_dequant_gather(int layout, const uint8_t* pool, long long poo
                                   const int* ids, long long n, __nv_bfloat16* out, int* err,
                                   cudaStream_t stream);
 
+// topk == nullptr: the short-context form, ids j < fill_len[t] (else -1)
 cudaError_t launch_dequant_gather_topk(int layout, const uint8_t* pool, long long pool_rows,
-                                       const int* topk, int n_tok, int k, const int* token_to_req,
-                                       const unsigned char* is_valid, const int* page_table,
-                                       int n_req, int max_pages, int page_bits,
-                                       __nv_bfloat16* out, int* lens, int* err, cudaStream_t stream);
+                                       const int* topk, const int* fill_len, int n_tok, int k,
+                                       const int* token_to_req, const unsigned char* is_valid,
+                                       const int* page_table, int n_req, int max_pages,
+                                       int page_bits, __nv_bfloat16* out, int* lens, int* err,
+                                       cudaStream_t stream);
+
+cudaError_t launch_fill_all_indices(int* out, int n_tok, int k, const int* lens,
+                                    cudaStream_t stream);
 
 cudaError_t launch_topk_to_slots(const int* topk, int n_tok, int k, const int* token_to_req,
                                  const unsigned char* is_valid, const int* page_table, int n_req,

@@ -89,4 +89,35 @@ cudaError_t launch_topk_to_slots(const int* topk, int n_tok, int k, const int* t
   return cudaGetLastError();
 }
 
+// Short-context ids (sglang PR #39652's test table: fill_all_compressed_indices;
+// flashinfer_sparse.py: the "short-context bypass" of the indexer): every
+// compressed row a token can see is selected, out[t][j] = j for
+// j < min(lens[t], k), -1 after.  One CTA per token row, 4 entries per thread
+// with 16-byte stores when the rows are 16-byte aligned.
+__global__ void __launch_bounds__(kTopkThreads)
+fill_all_indices_kernel(int* __restrict__ out, int n_tok, int k, const int* __restrict__ lens) {
+  const bool vec = (k & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+  for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
+    const int len = __ldg(lens + t);
+    const long long rowoff = (long long)t * k;
+    if (vec) {
+      int4* out4 = reinterpret_cast<int4*>(out + rowoff);
+      for (int c = threadIdx.x; c < (k >> 2); c += blockDim.x) {
+        const int j = 4 * c;
+        out4[c] = make_int4(j < len ? j : -1, j + 1 < len ? j + 1 : -1, j + 2 < len ? j + 2 : -1,
+                            j + 3 < len ? j + 3 : -1);
+      }
+    } else {
+      for (int j = threadIdx.x; j < k; j += blockDim.x) out[rowoff + j] = j < len ? j : -1;
+    }
+  }
+}
+
+cudaError_t launch_fill_all_indices(int* out, int n_tok, int k, const int* lens,
+                                    cudaStream_t stream) {
+  const int grid = n_tok < 65535 * 4 ? n_tok : 65535 * 4;
+  fill_all_indices_kernel<<<grid, kTopkThreads, 0, stream>>>(out, n_tok, k, lens);
+  return cudaGetLastError();
+}
+
 }  // namespace dsv4kv

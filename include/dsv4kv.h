@@ -230,6 +230,31 @@ int dsv4kv_dequant_gather_topk(int layout, const void *pool, long long pool_rows
                                void *out_bf16, int *lens, int *err_word, void *stream);
 
 /*
+ * Short-context ids [KVL test table: fill_all_compressed_indices; TOPK: the
+ * indexer's "short-context bypass", where every compressed row a token can
+ * see is selected]: topk_out[t*k + j] = j for j < lens_in[t], else -1
+ * (lens_in[t] < 0 selects nothing; only the first k are written).  lens_in
+ * is the caller's per-token visible compressed length, e.g. (position + 1) /
+ * ratio in a causal prefill.  topk_out: int32 [n_tok, k] device; lens_in:
+ * int32 [n_tok] device.  DSV4KV_ERANGE if k > 65536.
+ */
+int dsv4kv_fill_all_compressed_indices(int *topk_out, int n_tok, int k, const int *lens_in,
+                                       void *stream);
+
+/*
+ * dsv4kv_dequant_gather_topk with the short-context ids of
+ * dsv4kv_fill_all_compressed_indices made on the fly (no id buffer): row
+ * t*k + j gathers compressed row j of token t's request when j < lens_in[t],
+ * a zero row otherwise.  Same arguments, lens and faults as
+ * dsv4kv_dequant_gather_topk with lens_in in place of topk.
+ */
+int dsv4kv_dequant_gather_all(int layout, const void *pool, long long pool_rows,
+                              const int *lens_in, int n_tok, int k,
+                              const int *token_to_req, const unsigned char *is_valid,
+                              const int *page_table, int n_req, int max_pages, int page_bits,
+                              void *out_bf16, int *lens, int *err_word, void *stream);
+
+/*
  * Request-local top-k compressed ids -> physical pool slots [TOPK,
  * _compressed_topk_to_slots, single-rank branch]:
  *   slots[t][c] = page_table[req][id >> page_bits] << page_bits
@@ -331,6 +356,16 @@ int dsv4kv_kvbuf_get_with_head_topk(dsv4kv_kvbuf *buf, int layout, const void *p
                                     const int *token_to_req, const unsigned char *is_valid,
                                     const int *page_table, int n_req, int max_pages, int page_bits,
                                     void **rows, int *lens, int *hit, int *err_word, void *stream);
+
+/* get_with_head whose ids are the short-context ids (dsv4kv_dequant_gather_all):
+ * the head is (layout, pool, pool_rows, lens_in pointer, n_tok * k) plus the
+ * mapping fingerprint; a miss runs dsv4kv_dequant_gather_all into the
+ * storage, a hit launches nothing. */
+int dsv4kv_kvbuf_get_with_head_all(dsv4kv_kvbuf *buf, int layout, const void *pool,
+                                   long long pool_rows, const int *lens_in, int n_tok, int k,
+                                   const int *token_to_req, const unsigned char *is_valid,
+                                   const int *page_table, int n_req, int max_pages, int page_bits,
+                                   void **rows, int *lens, int *hit, int *err_word, void *stream);
 
 #ifdef __cplusplus
 }

@@ -71,6 +71,7 @@ def _load():
                                        P, I, P, L, P, L, P, L, P, P, P, P, P]),
             "orc_dequant_gather": (L, [I, P, L, P, L, P]),
             "orc_topk_to_slots": (L, [P, L, I, P, P, P, I, I, I, P, P]),
+            "orc_fill_all_indices": (None, [L, I, P, P]),
             "orc_ue8m0_many": (None, [P, L, P]),
             "orc_e4m3_encode_many": (None, [P, L, P]),
             "orc_e2m1_encode_many": (None, [P, L, P]),
@@ -264,6 +265,14 @@ def dequant_gather(layout, pool, pool_rows, ids):
     if faults < 0:
         raise ValueError("orc_dequant_gather: layout not supported")
     return out, int(faults)
+
+
+def fill_all_indices(lens, k):
+    """Short-context ids: int32 [n_tok, k], row t = 0..lens[t]-1 then -1."""
+    lens = _c(lens, np.int32)
+    out = np.zeros((lens.size, k), np.int32)
+    _load().orc_fill_all_indices(lens.size, k, _ptr(lens), _ptr(out))
+    return out
 
 
 def topk_to_slots(topk, token_to_req, page_table, page_bits, is_valid=None):

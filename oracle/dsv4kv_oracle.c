@@ -610,6 +610,21 @@ int64_t orc_topk_to_slots(const int32_t *topk, int64_t n_tok, int k,
     return faults;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Short-context ids [P4 test table: fill_all_compressed_indices; P3         */
+/* "short-context bypass" of the indexer].  Every compressed row a token can  */
+/* see is selected: out[t][j] = j for j < min(lens[t], k), -1 after; lens[t]  */
+/* is the token's visible compressed length (a negative one counts as 0).    */
+/* ------------------------------------------------------------------------ */
+void orc_fill_all_indices(int64_t n_tok, int k, const int32_t *lens, int32_t *out)
+{
+    int64_t t;
+    int j;
+    for (t = 0; t < n_tok; ++t)
+        for (j = 0; j < k; ++j)
+            out[t * k + j] = j < lens[t] ? j : -1;
+}
+
 /* Vectorised helpers for the tests' exhaustive pins. */
 void orc_ue8m0_many(const float *amax, int64_t n, uint8_t *out)
 {

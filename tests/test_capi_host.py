@@ -197,3 +197,30 @@ def test_topk_reuse_head_covers_the_id_mapping(B):
     assert call(a5=7) == 0                                   # other k (n_tok * k still 0)
     L.dsv4kv_kvbuf_begin_forward(ctypes.byref(buf))
     assert call() == 0 and call() == 1
+
+
+def test_short_context_calls_reject_bad_arguments(B):
+    L = B.lib()
+    f = L.dsv4kv_fill_all_compressed_indices
+    assert f(FAKE, 4, 70000, FAKE, None) == -3
+    assert f(FAKE, -1, 8, FAKE, None) == -1
+    assert f(None, 4, 8, FAKE, None) == -1
+    assert f(FAKE, 4, 8, FAKE + 2, None) == -1
+    assert f(None, 0, 8, None, None) == 0                     # nothing to do
+    g = L.dsv4kv_dequant_gather_all
+    assert g(1, FAKE, 10, FAKE, 4, 70000, FAKE, None, FAKE, 2, 2, 6, FAKE, None, None, None) == -3
+    assert g(1, FAKE, 10, None, 4, 8, FAKE, None, FAKE, 2, 2, 6, FAKE, None, None, None) == -1
+    assert g(1, FAKE, 10, FAKE, 4, 8, FAKE, None, FAKE, 2, 2, 17, FAKE, None, None, None) == -1
+    assert g(1, FAKE, 10, FAKE, 4, 8, FAKE, None, FAKE, 2, 2, 6, FAKE + 8, None, None, None) == -1
+    assert g(9, FAKE, 10, FAKE, 4, 8, FAKE, None, FAKE, 2, 2, 6, FAKE, None, None, None) == -1
+    assert g(1, FAKE, 10, FAKE, 0, 8, FAKE, None, FAKE, 2, 2, 6, FAKE, None, None, None) == 0
+    # the reuse head of the short-context form is its own source
+    buf = B.dsv4kv_kvbuf()
+    assert L.dsv4kv_kvbuf_init(ctypes.byref(buf), FAKE, 64) == 0
+    rows, hit = ctypes.c_void_p(), ctypes.c_int()
+    args = (1, FAKE, 1000, FAKE + 256, 0, 8, FAKE + 512, None, FAKE + 1024, 4, 16, 6)
+    for fn, want in ((L.dsv4kv_kvbuf_get_with_head_all, 0), (L.dsv4kv_kvbuf_get_with_head_all, 1),
+                     (L.dsv4kv_kvbuf_get_with_head_topk, 0), (L.dsv4kv_kvbuf_get_with_head_all, 0)):
+        assert fn(ctypes.byref(buf), *args, ctypes.byref(rows), None, ctypes.byref(hit), None,
+                  None) == 0
+        assert hit.value == want

@@ -593,3 +593,37 @@ def test_back_to_back_launches_see_the_previous_kernels_writes(B):
     for r in range(rounds):
         assert np.array_equal(fast[r], slow[r]), f"round {r}"
     assert not np.array_equal(slow[0], slow[1])          # the rounds do differ
+
+
+
+@pytest.mark.parametrize("layout,k", [(oracle.V41, 512), (oracle.V41_FP4, 130), (oracle.V4, 7)])
+def test_short_context_ids_and_fused_gather_match_oracle(B, layout, k):
+    """dsv4kv_fill_all_compressed_indices == the oracle's fill, and
+    dsv4kv_dequant_gather_all == oracle fill -> topk_to_slots -> gather (bit
+    exact, lens, faults), on a pool written by the store."""
+    cfg = dict(W.cfg2_ratio2_small(), layout=layout)
+    pool = gpu_store(B, cfg)["pool"]
+    rng = np.random.default_rng(41 + layout + k)
+    n_tok = 45
+    lens_in = rng.integers(-2, k + 40, n_tok).astype(np.int32)
+    lens_in[:3] = [0, k, 1]
+    pt = cfg["page_table"].copy()
+    pt[7, 0] = 70                                   # a page past the pool (65 pages)
+    ttr = rng.integers(0, 8, n_tok).astype(np.int32)
+    ttr[5] = 9                                      # request outside the table
+    ttr[6], lens_in[6] = 7, 3                       # request 7, page 0 -> past the pool
+    valid = (rng.random(n_tok) > 0.15).astype(np.uint8)
+    valid[6] = 1
+    ids = B.dsv4kv_fill_all_compressed_indices(dev(lens_in), k)
+    torch.cuda.synchronize()
+    want_ids = oracle.fill_all_indices(lens_in, k)
+    assert np.array_equal(ids.cpu().numpy(), want_ids)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lens = torch.zeros(n_tok, dtype=torch.int32, device="cuda")
+    out = B.dsv4kv_dequant_gather_all(layout, dev(pool), dev(lens_in), k, dev(ttr), dev(pt), 6,
+                                      is_valid=dev(valid), lens=lens, err_word=err)
+    ws, wl, f1 = oracle.topk_to_slots(want_ids, ttr, pt, 6, is_valid=valid)
+    want, f2 = oracle.dequant_gather(layout, pool, cfg["pool_rows"], ws.reshape(-1))
+    assert_bf16_equal_nan_aware(host_u16(out), want)
+    assert np.array_equal(lens.cpu().numpy(), wl)
+    assert int(err.item()) == f1 + f2 and f1 > 0 and f2 > 0

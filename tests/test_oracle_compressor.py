@@ -212,6 +212,22 @@ def test_topk_to_slots_oracle():
     assert lens.tolist() == [4, 0] and (slots[1] == -1).all()
 
 
+def test_fill_all_indices_oracle():
+    """Short-context ids, worked by hand: each row counts up to its token's
+    visible length and pads with -1; through topk_to_slots they select every
+    visible compressed row of the request exactly once."""
+    ids = oracle.fill_all_indices(np.array([0, 1, 4, 6, -3], np.int32), 5)
+    assert ids.tolist() == [[-1, -1, -1, -1, -1], [0, -1, -1, -1, -1], [0, 1, 2, 3, -1],
+                            [0, 1, 2, 3, 4], [-1, -1, -1, -1, -1]]
+    pt = np.array([[5, 2, 9], [7, 1, 0]], np.int32)
+    lens_in = np.array([6, 3], np.int32)
+    slots, lens, faults = oracle.topk_to_slots(oracle.fill_all_indices(lens_in, 8),
+                                               np.array([0, 1], np.int32), pt, 2)
+    assert slots[0].tolist() == [20, 21, 22, 23, 8, 9, -1, -1]      # pages 5, 2 of request 0
+    assert slots[1].tolist() == [28, 29, 30, -1, -1, -1, -1, -1]    # page 7 of request 1
+    assert lens.tolist() == [6, 3] and faults == 0
+
+
 def test_row_subset_mode_equals_the_full_run():
     rows, ext, w, freqs = _small_case(13, 2, [40, 17, 0, 66])
     full = oracle.compress_store(oracle.V41, 2, rows, ext, norm_w=w, freqs=freqs,
