@@ -74,6 +74,7 @@ def lib():
                                                    ctypes.POINTER(ctypes.c_void_p), P,
                                                    ctypes.POINTER(ctypes.c_int), P, P]),
             "dsv4kv_fill_all_compressed_indices": (I, [P, I, I, P, P]),
+            "dsv4kv_fake_quant": (I, [I, P, LL, LL, P, P]),
             "dsv4kv_dequant_gather_all": (I, [I, P, LL, P, I, I, P, P, P, I, I, I, P, P, P, P]),
             "dsv4kv_selftest_bounded_wait": (I, [I, P, P, P]),
             "dsv4kv_selftest_fp4_quotient": (I, [P, P, LL, P, P, P]),
@@ -287,6 +288,23 @@ def dsv4kv_fill_all_compressed_indices(lens_in, k, out=None, *, stream=None):
     st = lib().dsv4kv_fill_all_compressed_indices(_ptr(out), n_tok, k, _ptr(lens_in),
                                                   _stream(stream))
     _check("dsv4kv_fill_all_compressed_indices", st)
+    return out
+
+
+def dsv4kv_fake_quant(layout, x, out=None, *, stream=None):
+    """bf16 [n, >=512] rows -> bf16 [n, 512]: quantized with the layout's
+    store_row and dequantized (out may be x when x is [n, 512])."""
+    _need(x, torch.bfloat16, "x")
+    _need(out, torch.bfloat16, "out")
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    n = x.shape[0]
+    if out is None:
+        out = torch.empty((n, DIM), dtype=torch.bfloat16, device=x.device)
+    elif out.numel() < n * DIM or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of >= n x 512")
+    st = lib().dsv4kv_fake_quant(layout, _ptr(x), n, x.stride(0), _ptr(out), _stream(stream))
+    _check("dsv4kv_fake_quant", st)
     return out
 
 

@@ -243,6 +243,19 @@ int dsv4kv_topk_to_slots(const int* topk, int n_tok, int k, const int* token_to_
                                           static_cast<cudaStream_t>(stream)));
 }
 
+int dsv4kv_fake_quant(int layout, const void* in_bf16, long long n, long long in_stride,
+                      void* out_bf16, void* stream) {
+  int st = check_rw_layout(layout);
+  if (st != DSV4KV_OK) return st;
+  if (n < 0 || in_stride < 0) return DSV4KV_EINVAL;
+  if (n == 0) return DSV4KV_OK;
+  if (!in_bf16 || !out_bf16 || !aligned16(in_bf16) || !aligned16(out_bf16)) return DSV4KV_EINVAL;
+  if (in_stride < DSV4KV_DIM || (in_stride % 8) != 0) return DSV4KV_EINVAL;
+  return cuda_status(launch_fake_quant(layout, static_cast<const __nv_bfloat16*>(in_bf16), n,
+                                       in_stride, static_cast<__nv_bfloat16*>(out_bf16),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 int dsv4kv_selftest_bounded_wait(int polls, int* err_word, int* gave_up, void* stream) {
   if (polls < 1 || polls > (1 << 24)) return DSV4KV_ERANGE;
   if (!err_word || !gave_up || ((uintptr_t)err_word & 3u) || ((uintptr_t)gave_up & 3u))

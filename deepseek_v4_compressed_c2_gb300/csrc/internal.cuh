@@ -74,6 +74,9 @@ cudaError_t launch_dequant_gather_topk(int layout, const uint8_t* pool, long lon
 cudaError_t launch_fill_all_indices(int* out, int n_tok, int k, const int* lens,
                                     cudaStream_t stream);
 
+cudaError_t launch_fake_quant(int layout, const __nv_bfloat16* in, long long n,
+                              long long in_stride, __nv_bfloat16* out, cudaStream_t stream);
+
 cudaError_t launch_topk_to_slots(const int* topk, int n_tok, int k, const int* token_to_req,
                                  const unsigned char* is_valid, const int* page_table, int n_req,
                                  int max_pages, int page_bits, int* slots, int* lens, int* err,

@@ -297,6 +297,18 @@ int dsv4kv_selftest_fp4_quotient(const float *x, const unsigned char *scale_code
                                  float *q_fast, float *q_ieee, void *stream);
 
 /*
+ * Fake quantization [KVL test table: fake_quant_compressed_kv,
+ * fake_quant_fp4]: out_bf16[i] = bf16(dequant(store_row(in_bf16[i]))) for
+ * each of n rows, with the layout's own store_row and dequantizer, so the
+ * result equals dsv4kv_compress_store (store-only) followed by
+ * dsv4kv_dequant_gather of that row, bit for bit.  in_bf16: [n, in_stride]
+ * (in_stride >= 512, a multiple of 8 elements), out_bf16: [n, 512]; both
+ * 16-byte aligned; out_bf16 == in_bf16 (in_stride 512) is allowed.
+ */
+int dsv4kv_fake_quant(int layout, const void *in_bf16, long long n, long long in_stride,
+                      void *out_bf16, void *stream);
+
+/*
  * Source-reuse buffer [BUF]: the shared bf16 buffer the sparse-prefill layers
  * read.  It remembers the source it last dequantized -- (layout, pool,
  * pool_rows, ids pointer, n) -- and a get_with_head for that same source is a

@@ -224,3 +224,15 @@ def test_short_context_calls_reject_bad_arguments(B):
         assert fn(ctypes.byref(buf), *args, ctypes.byref(rows), None, ctypes.byref(hit), None,
                   None) == 0
         assert hit.value == want
+
+
+def test_fake_quant_rejects_bad_arguments(B):
+    L = B.lib()
+    f = L.dsv4kv_fake_quant
+    assert f(3, FAKE, 10, 512, FAKE, None) == -1            # layout
+    assert f(1, FAKE, -1, 512, FAKE, None) == -1
+    assert f(1, FAKE + 8, 10, 512, FAKE, None) == -1        # misaligned input
+    assert f(1, FAKE, 10, 512, FAKE + 4, None) == -1        # misaligned output
+    assert f(1, FAKE, 10, 500, FAKE, None) == -1            # stride below 512
+    assert f(1, FAKE, 10, 516, FAKE, None) == -1            # stride not a multiple of 8
+    assert f(1, None, 0, 512, None, None) == 0              # nothing to do

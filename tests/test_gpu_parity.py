@@ -627,3 +627,37 @@ def test_short_context_ids_and_fused_gather_match_oracle(B, layout, k):
     assert_bf16_equal_nan_aware(host_u16(out), want)
     assert np.array_equal(lens.cpu().numpy(), wl)
     assert int(err.item()) == f1 + f2 and f1 > 0 and f2 > 0
+
+
+@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4, oracle.V4])
+def test_fake_quant_matches_oracle_and_store_then_gather(B, layout):
+    """dsv4kv_fake_quant == the oracle's dequant(store_row(x)) bit for bit
+    (rows with outliers, all-zero rows), from a strided input and in place,
+    and == a store-only dsv4kv_compress_store followed by dsv4kv_dequant_gather."""
+    rng = np.random.default_rng(61 + layout)
+    n = 333
+    x32 = rng.standard_normal((n, 512)).astype(np.float32)
+    x32[rng.random((n, 512)) < 0.01] *= 50
+    x32[7] = 0.0
+    x = W.bf16_from_f32(x32)
+    want = oracle.bf16_bits(oracle.dequant_rows(layout, oracle.quantize_rows(layout, oracle.bf16_to_f64(x))))
+    wide = torch.zeros((n, 1024), dtype=torch.bfloat16, device="cuda")
+    wide[:, :512] = dev_bf16(x)
+    out = B.dsv4kv_fake_quant(layout, wide[:, :512])
+    torch.cuda.synchronize()
+    assert np.array_equal(host_u16(out), want)
+    inplace = dev_bf16(x).contiguous()
+    B.dsv4kv_fake_quant(layout, inplace, inplace)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_u16(inplace), want)
+    # the same through the pool: store-only rows 1..n, gathered back
+    rb = oracle.row_bytes(layout)
+    pool = torch.zeros((n + 1) * rb, dtype=torch.uint8, device="cuda")
+    ext = torch.tensor([[0], [n]], dtype=torch.int32, device="cuda")
+    B.dsv4kv_compress_store(layout, 1, dev_bf16(x), ext, pool,
+                            out_loc=torch.arange(1, n + 1, dtype=torch.int32, device="cuda"),
+                            n_out=n)
+    back = B.dsv4kv_dequant_gather(layout, pool, torch.arange(1, n + 1, dtype=torch.int32,
+                                                             device="cuda"))
+    torch.cuda.synchronize()
+    assert np.array_equal(host_u16(back), want)
