@@ -233,10 +233,13 @@ def _timed(fn, flush, stream, reps):
 
 def cold_gather(B, dev, stream, reps):
     """The store-only fill and the gather, each timed alone with a cold L2:
-    1,048,576-row pools (page 0 reserved) in V41 and V41_FP4 layouts, filled
-    by the ratio-1 store from bf16 N(0,1) latents (torch generator, seed 4);
-    262,144 unique row ids (numpy seed 4); a 512 MB buffer written between
-    launches."""
+    1,048,576-row pools (page 0 reserved) in the V41, V41_FP4 and V4 layouts,
+    filled by the ratio-1 store from bf16 N(0,1) latents (torch generator,
+    seed 4); 262,144 unique row ids (numpy seed 4); a 512 MB buffer written
+    between launches.  Also, per layout, the fake quantization of the same
+    1,048,512 latent rows (bf16 in, bf16 out), and on the V41 pool the
+    short-context gather: 128 tokens of one request, each selecting every
+    compressed row it sees (lengths uniform in [1, 2048], numpy seed 5)."""
     import torch
     pool_rows, n_ids = 1 << 20, 1 << 18
     g = torch.Generator(device=dev)
@@ -252,7 +255,8 @@ def cold_gather(B, dev, stream, reps):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     peak, kind = _peaks()
     res = {}
-    for layout, name, rb in ((1, "v41", 528), (2, "fp4", 288)):
+    fq_out = torch.empty((pool_rows - 64, 512), dtype=torch.bfloat16, device=dev)
+    for layout, name, rb in ((1, "v41", 528), (2, "fp4", 288), (0, "v4", 584)):
         pool = torch.zeros(pool_rows * rb, dtype=torch.uint8, device=dev)
         store = B.prepare_compress_store(layout, 1, lat, ext, pool, page_table=pt, page_bits=6,
                                          n_out=pool_rows - 64, err_word=err, stream=stream)
@@ -269,6 +273,29 @@ def cold_gather(B, dev, stream, reps):
             "ms": ms_g, "rows_per_s": n_ids / (ms_g / 1e3), "gbs": gb * n_ids / (ms_g / 1e3) / 1e9,
             "frac": gb * n_ids / (ms_g / 1e3) / 1e9 / peak, "frac_of_8000": gb * n_ids / (ms_g / 1e3) / 8e12,
             "bytes_per_row": gb}
+        ms_f = _timed(lambda: B.dsv4kv_fake_quant(layout, lat, fq_out, stream=stream), flush,
+                      stream, max(3, reps // 5))
+        res[f"fake_quant_{name}_1048512rows"] = {
+            "ms": ms_f, "rows_per_s": (pool_rows - 64) / (ms_f / 1e3),
+            "gbs": 2048 * (pool_rows - 64) / (ms_f / 1e3) / 1e9,
+            "frac": 2048 * (pool_rows - 64) / (ms_f / 1e3) / 1e9 / peak, "bytes_per_row": 2048}
+        if layout == 1:
+            n_tok, k = 128, 2048
+            lens_in = torch.from_numpy(np.random.default_rng(5).integers(1, k + 1, n_tok)
+                                       .astype(np.int32)).to(dev)
+            ttr = torch.zeros(n_tok, dtype=torch.int32, device=dev)
+            ms_a = _timed(lambda: B.dsv4kv_dequant_gather_all(1, pool, lens_in, k, ttr, pt, 6,
+                                                              out[:n_tok * k], err_word=err,
+                                                              stream=stream),
+                          flush, stream, reps)
+            n_rows = int(lens_in.sum().item())
+            res["gather_all_v41_128tok_2048"] = {
+                "ms": ms_a, "rows": n_tok * k, "selected_rows": n_rows,
+                "rows_per_s": n_tok * k / (ms_a / 1e3),
+                "out_gbs": 1024 * n_tok * k / (ms_a / 1e3) / 1e9,
+                "note": "every token of one request re-reads the same <= 2048 compressed rows "
+                        "(L2-resident after the first); bound by the 1 KB/row output"}
+        assert int(err.item()) == 0
         del pool
     res["peak_kind"] = kind
     return res
