@@ -9,6 +9,7 @@
 
 #include "dsv4kv.h"
 #include "internal.cuh"
+#include "launchers.cuh"
 #include "layout.cuh"
 
 namespace dsv4kv {

@@ -36,6 +36,7 @@
 #include <atomic>
 
 #include "internal.cuh"
+#include "launchers.cuh"
 #include "quant.cuh"
 #include "tma.cuh"
 

@@ -18,6 +18,7 @@
 #include <atomic>
 
 #include "internal.cuh"
+#include "launchers.cuh"
 #include "quant.cuh"
 #include "tma.cuh"
 

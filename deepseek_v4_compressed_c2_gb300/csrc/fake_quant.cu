@@ -13,6 +13,7 @@
 // and writes only its own 16-byte chunks (dims 8l..8l+7 and 256+8l..), so
 // in == out is allowed.
 #include "internal.cuh"
+#include "launchers.cuh"
 #include "quant.cuh"
 
 namespace dsv4kv {

@@ -1,6 +1,7 @@
-// Launch parameters and launchers shared between the kernel files and the
-// C-ABI layer.  Everything here is device-pointer plumbing; argument checks
-// happen in capi.cu before any launcher is reached.
+// Kernel parameters and device helpers shared between the kernel files and
+// the C-ABI layer (the launchers are declared in launchers.cuh).  Everything
+// here is device-pointer plumbing; argument checks happen in capi.cu before
+// any launcher is reached.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -38,8 +39,6 @@ struct StoreParams {
   int ring_size;
 };
 
-cudaError_t launch_compress_store(const StoreParams& p, int layout, int ratio, cudaStream_t stream);
-
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the previous kernel in the stream finishes; it waits
 // (grid_dependency_wait) before touching global memory.
@@ -58,29 +57,6 @@ cudaError_t launch_dependent(void (*kern)(Params...), int grid, int block, size_
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
-
-cudaError_t launch_dequant_gather(int layout, const uint8_t* pool, long long pool_rows,
-                                  const int* ids, long long n, __nv_bfloat16* out, int* err,
-                                  cudaStream_t stream);
-
-// topk == nullptr: the short-context form, ids j < fill_len[t] (else -1)
-cudaError_t launch_dequant_gather_topk(int layout, const uint8_t* pool, long long pool_rows,
-                                       const int* topk, const int* fill_len, int n_tok, int k,
-                                       const int* token_to_req, const unsigned char* is_valid,
-                                       const int* page_table, int n_req, int max_pages,
-                                       int page_bits, __nv_bfloat16* out, int* lens, int* err,
-                                       cudaStream_t stream);
-
-cudaError_t launch_fill_all_indices(int* out, int n_tok, int k, const int* lens,
-                                    cudaStream_t stream);
-
-cudaError_t launch_fake_quant(int layout, const __nv_bfloat16* in, long long n,
-                              long long in_stride, __nv_bfloat16* out, cudaStream_t stream);
-
-cudaError_t launch_topk_to_slots(const int* topk, int n_tok, int k, const int* token_to_req,
-                                 const unsigned char* is_valid, const int* page_table, int n_req,
-                                 int max_pages, int page_bits, int* slots, int* lens, int* err,
-                                 cudaStream_t stream);
 
 // Streaming 16-byte global load that bypasses L1 (inputs read exactly once).
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
@@ -101,13 +77,6 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
   asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
-
-cudaError_t launch_bounded_wait_selftest(uint32_t polls, int* err, int* gave_up,
-                                         cudaStream_t stream);
-
-cudaError_t launch_fp4_quotient_selftest(const float* x, const unsigned char* scale_codes,
-                                         long long n, float* q_fast, float* q_ieee,
-                                         cudaStream_t stream);
 
 // Multiprocessor count of the current device (cached), for persistent grids.
 int device_sm_count();

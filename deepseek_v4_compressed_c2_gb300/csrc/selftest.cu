@@ -5,6 +5,7 @@
 // A second warp waits on the same barrier and must notice the first one's
 // abort flag and give up too.
 #include "internal.cuh"
+#include "launchers.cuh"
 #include "quant.cuh"
 #include "tma.cuh"
 

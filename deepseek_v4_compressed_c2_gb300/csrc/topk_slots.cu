@@ -8,6 +8,7 @@
 // become -1; CUDA-graph padding rows (is_valid_token == 0) attend nothing.
 //
 #include "internal.cuh"
+#include "launchers.cuh"
 
 namespace dsv4kv {
 
