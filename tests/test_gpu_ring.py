@@ -143,3 +143,36 @@ def test_negative_start_positions_fault_like_the_oracle(B, rope):
     assert ref["faults"] > 0 and int(err.item()) == ref["faults"]
     assert np.array_equal(host_u16(ring).reshape(ref_ring.shape), ref_ring)
     assert np.array_equal(pool.cpu().numpy(), ref_pool)
+
+
+@pytest.mark.parametrize("n_new", [1, 4, 9])
+def test_ring_form_with_separate_score_or_padded_stride_equals_fused(B, n_new):
+    """The ring form reading kv and score from separate buffers, or from rows
+    padded to 1536 elements, writes the same pool and ring bytes as the fused
+    | kv | score | rows (the producer's per-half copies, ring-sourced pairs
+    included)."""
+    cfg = W.decode_verify(seed=30 + n_new, n_req=300, n_new=n_new, ring_size=4, max_prefix=512)
+    rows = dev_bf16(cfg["rows"])
+    common = dict(page_table=dev(cfg["page_table"]), page_bits=cfg["page_bits"],
+                  rmsnorm_w=dev_bf16(cfg["norm_w"]), eps=cfg["eps"], freqs_cis=dev(cfg["freqs"]),
+                  n_out=cfg["n_out"], start_pos=dev(cfg["start_pos"]))
+
+    def run(r, score=None):
+        pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device="cuda")
+        ring = dev_bf16(cfg["ring"])
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        B.dsv4kv_compress_store(1, 2, r, dev(cfg["ext"]), pool, score=score, ring=ring,
+                                err_word=err, **common)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        return pool.cpu().numpy(), host_u16(ring)
+
+    fused = run(rows)
+    kv = rows[:, :512].contiguous()
+    sc = rows[:, 512:].contiguous()
+    split = run(kv, score=sc)
+    padded = torch.zeros((rows.shape[0], 1536), dtype=torch.bfloat16, device="cuda")
+    padded[:, :1024] = rows
+    wide = run(padded[:, :1024].as_strided((rows.shape[0], 1024), (1536, 1)))
+    for got in (split, wide):
+        assert np.array_equal(got[0], fused[0]) and np.array_equal(got[1], fused[1])
