@@ -176,3 +176,26 @@ def test_ring_form_with_separate_score_or_padded_stride_equals_fused(B, n_new):
     wide = run(padded[:, :1024].as_strided((rows.shape[0], 1024), (1536, 1)))
     for got in (split, wide):
         assert np.array_equal(got[0], fused[0]) and np.array_equal(got[1], fused[1])
+
+
+@pytest.mark.parametrize("n_new", [3, 9])
+def test_ring_form_with_fewer_output_rows_than_the_step_makes(B, n_new):
+    """n_out below the step's row count: rows k >= n_out are neither computed
+    nor stored, in the tiles and in the ring phase (n >= 2R rows), while the
+    ring is still updated for every request, as in the oracle."""
+    cfg = W.decode_verify(seed=50 + n_new, n_req=200, n_new=n_new, ring_size=4, max_prefix=512)
+    n_out = cfg["n_out"] // 2
+    cfg = dict(cfg, n_out=n_out, layout=oracle.V41)
+    pool = torch.full((cfg["pool_rows"] * 528,), 0xA5, dtype=torch.uint8, device="cuda")
+    ring = dev_bf16(cfg["ring"])
+    pre, err = gpu_step(B, cfg, pool, ring)
+    ref_ring = cfg["ring"].copy()
+    same_pool = np.full(cfg["pool_rows"] * 528, 0xA5, np.uint8)
+    ref = oracle.compress_store(oracle.V41, 2, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
+                                page_bits=cfg["page_bits"], norm_w=cfg["norm_w"], eps=cfg["eps"],
+                                freqs=cfg["freqs"], n_out=n_out, start_pos=cfg["start_pos"],
+                                pool=same_pool, pool_rows=cfg["pool_rows"], ring=ref_ring,
+                                prequant_in=pre)
+    assert err == ref["faults"] == 0
+    assert np.array_equal(pool.cpu().numpy(), same_pool)
+    assert np.array_equal(host_u16(ring).reshape(ref_ring.shape), ref_ring)
