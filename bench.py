@@ -215,13 +215,19 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
-def _timed(fn, flush, stream, reps):
-    """median CUDA-event time of fn() in ms, L2 flushed before each launch"""
+def _timed(fn, flush, stream, reps, scrub=None):
+    """median CUDA-event time of fn() in ms, L2 flushed before each launch:
+    a write of `flush` (512 MB, 4x the L2); with `scrub`, then a read of it
+    (256 MB), which evicts the dirty lines of the write, so the timed kernel
+    starts from a cold L2 that holds neither its inputs nor lines still to be
+    written back"""
     import torch
     times = []
     with torch.cuda.stream(stream):
         for i in range(reps + 3):
             flush.fill_(i & 0xFF)
+            if scrub is not None:
+                scrub.max()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
@@ -235,11 +241,12 @@ def cold_gather(B, dev, stream, reps):
     """The store-only fill and the gather, each timed alone with a cold L2:
     1,048,576-row pools (page 0 reserved) in the V41, V41_FP4 and V4 layouts,
     filled by the ratio-1 store from bf16 N(0,1) latents (torch generator,
-    seed 4); 262,144 unique row ids (numpy seed 4); a 512 MB buffer written
-    between launches.  Also, per layout, the fake quantization of the same
-    1,048,512 latent rows (bf16 in, bf16 out), and on the V41 pool the
-    short-context gather: 128 tokens of one request, each selecting every
-    compressed row it sees (lengths uniform in [1, 2048], numpy seed 5)."""
+    seed 4); 262,144 unique row ids (numpy seed 4); between launches a 512 MB
+    buffer written and a 256 MB one read (see _timed).  Also, per layout, the
+    fake quantization of the same 1,048,512 latent rows (bf16 in, bf16 out),
+    and on the V41 pool the short-context gather: 128 tokens of one request,
+    each selecting every compressed row it sees (lengths uniform in
+    [1, 2048], numpy seed 5)."""
     import torch
     pool_rows, n_ids = 1 << 20, 1 << 18
     g = torch.Generator(device=dev)
@@ -253,6 +260,7 @@ def cold_gather(B, dev, stream, reps):
                            .astype(np.int32)).to(dev)
     out = torch.empty((n_ids, 512), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    scrub = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
     peak, kind = _peaks()
     res = {}
     fq_out = torch.empty((pool_rows - 64, 512), dtype=torch.bfloat16, device=dev)
@@ -261,8 +269,8 @@ def cold_gather(B, dev, stream, reps):
         store = B.prepare_compress_store(layout, 1, lat, ext, pool, page_table=pt, page_bits=6,
                                          n_out=pool_rows - 64, err_word=err, stream=stream)
         gather = B.prepare_dequant_gather(layout, pool, ids, out, err_word=err, stream=stream)
-        ms_s = _timed(store, flush, stream, max(3, reps // 5))
-        ms_g = _timed(gather, flush, stream, reps)
+        ms_s = _timed(store, flush, stream, max(3, reps // 5), scrub)
+        ms_g = _timed(gather, flush, stream, reps, scrub)
         assert int(err.item()) == 0
         sb, gb = 1024 + rb, rb + 4 + 1024
         res[f"store_ratio1_{name}_1048512rows"] = {
@@ -274,7 +282,7 @@ def cold_gather(B, dev, stream, reps):
             "frac": gb * n_ids / (ms_g / 1e3) / 1e9 / peak, "frac_of_8000": gb * n_ids / (ms_g / 1e3) / 8e12,
             "bytes_per_row": gb}
         ms_f = _timed(lambda: B.dsv4kv_fake_quant(layout, lat, fq_out, stream=stream), flush,
-                      stream, max(3, reps // 5))
+                      stream, max(3, reps // 5), scrub)
         res[f"fake_quant_{name}_1048512rows"] = {
             "ms": ms_f, "rows_per_s": (pool_rows - 64) / (ms_f / 1e3),
             "gbs": 2048 * (pool_rows - 64) / (ms_f / 1e3) / 1e9,
@@ -287,8 +295,16 @@ def cold_gather(B, dev, stream, reps):
             ms_a = _timed(lambda: B.dsv4kv_dequant_gather_all(1, pool, lens_in, k, ttr, pt, 6,
                                                               out[:n_tok * k], err_word=err,
                                                               stream=stream),
-                          flush, stream, reps)
+                          flush, stream, reps, scrub)
             n_rows = int(lens_in.sum().item())
+            # the same gather after the write-only flush: it also pays the
+            # write-back of the flush's dirty lines
+            ms_gd = _timed(gather, flush, stream, reps)
+            res["gather_v41_262144_of_1048576_dirty_l2"] = {
+                "ms": ms_gd, "gbs": 1556 * n_ids / (ms_gd / 1e3) / 1e9,
+                "frac": 1556 * n_ids / (ms_gd / 1e3) / 1e9 / peak,
+                "note": "L2 flushed by the 512 MB write alone; ~129 MB of its dirty lines are "
+                        "written back during the gather"}
             res["gather_all_v41_128tok_2048"] = {
                 "ms": ms_a, "rows": n_tok * k, "selected_rows": n_rows,
                 "rows_per_s": n_tok * k / (ms_a / 1e3),
