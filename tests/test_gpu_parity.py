@@ -661,3 +661,28 @@ def test_fake_quant_matches_oracle_and_store_then_gather(B, layout):
                                                              device="cuda"))
     torch.cuda.synchronize()
     assert np.array_equal(host_u16(back), want)
+
+
+def test_requests_past_65536_rows_plan_and_store_bit_exact(B):
+    """No 16-bit limit in the plan: one request of 70,001 rows and another of
+    65,536 (ratio 1, store-only, random permuted page table) store every row
+    at its page-table slot, bit-exact against the oracle."""
+    rng = np.random.default_rng(65)
+    lens = [70001, 65536, 3]
+    n_rows = sum(lens)
+    rows = W.bf16_from_f32(rng.standard_normal((n_rows, 512)).astype(np.float32))
+    ext = np.array([[0, lens[0], lens[0] + lens[1]], lens], np.int32)
+    pages = [-(-n // 64) for n in lens]
+    perm = rng.permutation(sum(pages)).astype(np.int32) + 1
+    pt = np.zeros((3, max(pages)), np.int32)
+    o = 0
+    for r, p in enumerate(pages):
+        pt[r, :p] = perm[o:o + p]
+        o += p
+    pool_rows = (sum(pages) + 1) * 64
+    cfg = dict(layout=oracle.V41, ratio=1, rows=rows, ext=ext, page_table=pt, page_bits=6,
+               norm_w=None, eps=1e-6, freqs=None, n_out=n_rows, pool_rows=pool_rows)
+    g = gpu_store(B, cfg, pool_fill=0xA5, want_pre=False, want_lat=False)
+    ref = oracle_store(cfg, pool_fill=0xA5)
+    assert g["err"] == ref["faults"] == 0 and ref["total"] == n_rows
+    assert np.array_equal(g["pool"], ref["pool"])
