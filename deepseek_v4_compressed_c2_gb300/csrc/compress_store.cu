@@ -42,18 +42,22 @@
 
 namespace dsv4kv {
 
-// Two launch shapes.  Streaming (large batches): 8 consumer warps, 3 stages,
-// two CTAs per SM, so each SM keeps 48 rows' inputs in flight.  Latency
-// (ring-form steps small enough for one row per consumer warp: decode and
-// speculative verify): 16 consumer warps, 2 stages, one CTA per SM, so a step
-// of up to 16 rows per SM finishes after one row's latency per warp.
-enum StoreShapeId : int { kShapeStream = 0, kShapeLatency = 1 };
+// Three launch shapes.  Streaming (large batches): 8 consumer warps, 3
+// stages, two CTAs per SM, so each SM keeps 48 rows' inputs in flight.
+// Latency (ring-form steps small enough for one row per consumer warp: decode
+// and speculative verify): 16 consumer warps, 2 stages, one CTA per SM, so a
+// step of up to 16 rows per SM finishes after one row's latency per warp.
+// Wide (ratio-1 rows that are only stored): 8 consumer warps of 2 rows, 2
+// stages, three CTAs per SM (72 registers): the store-only quantizers are
+// latency-bound at two CTAs per SM.
+enum StoreShapeId : int { kShapeStream = 0, kShapeLatency = 1, kShapeWide = 2 };
 
 template <int SHAPE>
 struct StoreShape {
   static constexpr int kWarps = SHAPE == kShapeLatency ? 16 : 8;     // consumer warps
-  static constexpr int kStages = SHAPE == kShapeLatency ? 2 : 3;
-  static constexpr int kMinBlocks = SHAPE == kShapeLatency ? 1 : 2;  // CTAs per SM
+  static constexpr int kStages = SHAPE == kShapeStream ? 3 : 2;
+  static constexpr int kMinBlocks =                                  // CTAs per SM
+      SHAPE == kShapeLatency ? 1 : (SHAPE == kShapeWide ? 3 : 2);
   static constexpr int kThreads = (kWarps + 1) * 32;
 };
 
@@ -74,13 +78,14 @@ struct __align__(16) RowDesc {
 
 // Rows per consumer warp per stage: one ratio-2 pair (4 KB), four ratio-1
 // rows when the row is only stored (32 KB stages either way), two ratio-1
-// rows with RMSNorm or RoPE (four would spill registers).
+// rows with RMSNorm or RoPE, or in the wide shape (four would spill).
 template <int RATIO, bool NORM, bool ROPE, int SHAPE>
 struct StoreTile {
   static constexpr int kWarps = StoreShape<SHAPE>::kWarps;
   static constexpr int kStages = StoreShape<SHAPE>::kStages;
   static constexpr int kThreads = StoreShape<SHAPE>::kThreads;
-  static constexpr int kRowsPerWarp = RATIO == 2 ? 1 : (NORM || ROPE ? 2 : 4);
+  static constexpr int kRowsPerWarp =
+      RATIO == 2 ? 1 : (NORM || ROPE || SHAPE == kShapeWide ? 2 : 4);
   static constexpr int kRows = kWarps * kRowsPerWarp;              // rows per stage
   static constexpr int kInBytes = RATIO == 2 ? 4096 : 1024;        // kv0|s0|kv1|s1, or kv
   static constexpr int kRopeBytes = ROPE ? kRopeDim * 4 : 0;
@@ -812,7 +817,13 @@ static cudaError_t launch_norm_rope(const StoreParams& p, cudaStream_t s) {
 // over more SMs in the streaming shape.
 template <int L>
 static cudaError_t launch_ratio(const StoreParams& p, int ratio, cudaStream_t s) {
-  if (ratio == 1) return launch_norm_rope<L, 1, false, kShapeStream>(p, s);
+  if (ratio == 1) {
+    const bool norm = p.norm_w != nullptr, rope = p.freqs != nullptr;
+    if (norm && rope) return launch_variant<L, 1, true, true, false, kShapeStream>(p, s);
+    if (norm) return launch_variant<L, 1, true, false, false, kShapeStream>(p, s);
+    if (rope) return launch_variant<L, 1, false, true, false, kShapeStream>(p, s);
+    return launch_variant<L, 1, false, false, false, kShapeWide>(p, s);
+  }
   if (p.start_pos == nullptr && p.ring == nullptr)
     return launch_norm_rope<L, 2, false, kShapeStream>(p, s);
   const long long sms = device_sm_count();
