@@ -78,6 +78,7 @@ def lib():
             "dsv4kv_dequant_gather_all": (I, [I, P, LL, P, I, I, P, P, P, I, I, I, P, P, P, P]),
             "dsv4kv_selftest_bounded_wait": (I, [I, P, P, P]),
             "dsv4kv_selftest_fp4_quotient": (I, [P, P, LL, P, P, P]),
+            "dsv4kv_selftest_e4m3_recip": (I, [P, LL, P, P, P]),
             "dsv4kv_kvbuf_init": (I, [KB, P, LL]),
             "dsv4kv_kvbuf_begin_forward": (None, [KB]),
             "dsv4kv_kvbuf_get": (I, [KB, LL, ctypes.POINTER(ctypes.c_void_p)]),

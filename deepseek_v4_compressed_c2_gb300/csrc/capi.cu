@@ -276,6 +276,16 @@ int dsv4kv_selftest_fp4_quotient(const float* x, const unsigned char* scale_code
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+int dsv4kv_selftest_e4m3_recip(const unsigned char* codes, long long n, float* y_fast,
+                               float* y_ieee, void* stream) {
+  if (n < 0) return DSV4KV_EINVAL;
+  if (n == 0) return DSV4KV_OK;
+  if (!codes || !y_fast || !y_ieee || ((uintptr_t)y_fast & 3u) || ((uintptr_t)y_ieee & 3u))
+    return DSV4KV_EINVAL;
+  return cuda_status(launch_e4m3_recip_selftest(codes, n, y_fast, y_ieee,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 // ----------------------------------------------------------------- reuse
 int dsv4kv_kvbuf_init(dsv4kv_kvbuf* buf, void* storage_bf16, long long capacity_rows) {
   if (!buf || capacity_rows < 0) return DSV4KV_EINVAL;

@@ -358,8 +358,7 @@ __device__ __forceinline__ void load_row(const uint8_t* in_row, const uint8_t* r
 template <int L, int RATIO, bool NORM, bool ROPE>
 __device__ __forceinline__ void process_row(const StoreParams& p, long long k, const RowDesc& d,
                                             long long slot, const RowIn<RATIO, ROPE>& in,
-                                            const float (&w)[16], int lane,
-                                            uint32_t fp4_table) {
+                                            const float (&w)[16], int lane) {
   if (d.state == kRowNone || d.state == kRowRing) return;
   if (d.state != kRowOk && d.state != kRowOkRing) {
     if (d.state == kRowBad && lane == 0 && p.err) atomicAdd(p.err, 1);
@@ -447,7 +446,7 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
       o[64 + 2 * lane] = make_float4(x[8], x[9], x[10], x[11]);
       o[64 + 2 * lane + 1] = make_float4(x[12], x[13], x[14], x[15]);
     }
-    if (store) store_row_split<L>(x, PagedKV<L>{p.pool, p.page_bits}.row(slot), lane, fp4_table);
+    if (store) store_row_split<L>(x, PagedKV<L>{p.pool, p.page_bits}.row(slot), lane);
   } else if (store) {
     f2_unpack16(x2, x);
     store_row_v41_scaled(x, inv, PagedKV<kV41>{p.pool, p.page_bits}.row(slot), lane);
@@ -513,8 +512,7 @@ __device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s
       }
       slot = dest_slot(p, k, d);
     }
-    process_row<L, 2, NORM, ROPE>(p, k, d, slot, in, w, lane,
-                                  L == kV41Fp4 ? fp4_recip_table(lane) : 0u);
+    process_row<L, 2, NORM, ROPE>(p, k, d, slot, in, w, lane);
   }
   if (p.ring == nullptr) return;
   __syncwarp();
@@ -592,7 +590,6 @@ __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_
                                               uint64_t* s_empty, volatile int* abort,
                                               long long n_tiles, int warp, int lane) {
   using TL = StoreTile<RATIO, NORM, ROPE, SHAPE>;
-  const uint32_t fp4_table = L == kV41Fp4 ? fp4_recip_table(lane) : 0u;
   float w[16];
   if constexpr (NORM) {
     const uint4* wp = reinterpret_cast<const uint4*>(p.norm_w);
@@ -623,7 +620,7 @@ __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_
 #pragma unroll
     for (int q = 0; q < TL::kRowsPerWarp; ++q) {
       const long long k = tile * TL::kRows + warp * TL::kRowsPerWarp + q;
-      process_row<L, RATIO, NORM, ROPE>(p, k, d[q], slot[q], in[q], w, lane, fp4_table);
+      process_row<L, RATIO, NORM, ROPE>(p, k, d[q], slot[q], in[q], w, lane);
     }
   }
 }

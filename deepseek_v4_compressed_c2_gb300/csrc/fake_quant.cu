@@ -26,7 +26,6 @@ __global__ void __launch_bounds__(kFqWarps * 32)
 fake_quant_kernel(const __nv_bfloat16* in, long long n, long long in_stride, __nv_bfloat16* out) {
   __shared__ __align__(16) uint8_t s_row[kFqWarps][kFqRowBuf];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t fp4_table = L == kV41Fp4 ? fp4_recip_table(lane) : 0u;
   uint8_t* row = s_row[warp];
   for (long long i = (long long)blockIdx.x * kFqWarps + warp; i < n;
        i += (long long)gridDim.x * kFqWarps) {
@@ -34,7 +33,7 @@ fake_quant_kernel(const __nv_bfloat16* in, long long n, long long in_stride, __n
     float x[16];
     unpack_bf16x8(src[lane], x);
     unpack_bf16x8(src[32 + lane], x + 8);
-    store_row_split<L>(x, row, lane, fp4_table);
+    store_row_split<L>(x, row, lane);
     __syncwarp();
     uint4 lo, hi;
     if constexpr (L == kV41) {

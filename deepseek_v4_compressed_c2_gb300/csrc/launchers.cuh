@@ -42,4 +42,7 @@ cudaError_t launch_fp4_quotient_selftest(const float* x, const unsigned char* sc
                                          long long n, float* q_fast, float* q_ieee,
                                          cudaStream_t stream);
 
+cudaError_t launch_e4m3_recip_selftest(const unsigned char* codes, long long n, float* y_fast,
+                                       float* y_ieee, cudaStream_t stream);
+
 }  // namespace dsv4kv

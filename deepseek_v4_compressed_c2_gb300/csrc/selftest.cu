@@ -41,19 +41,16 @@ cudaError_t launch_bounded_wait_selftest(uint32_t polls, int* err, int* gave_up,
 // scale_codes[i].
 __global__ void fp4_quotient_selftest_kernel(const float* x, const unsigned char* scale_codes,
                                              long long n, float* q_fast, float* q_ieee) {
-  // elements 2j and 2j + 1 go through the paired form used by the FP4 store
-  // (each with its own divisor and the quantizer's reciprocal table); the
-  // loop bound is per warp, so every lane reaches the table's shuffle
-  const int lane = threadIdx.x & 31;
-  const uint32_t table = fp4_recip_table(lane);
+  // elements 2j and 2j + 1 go through the paired form used by the FP4 store,
+  // each with its own divisor
   const long long pairs = (n + 1) / 2;
-  for (long long j0 = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); j0 < pairs;
-       j0 += (long long)gridDim.x * blockDim.x) {
-    const long long i = 2 * (j0 + lane);
+  for (long long j = (long long)blockIdx.x * blockDim.x + threadIdx.x; j < pairs;
+       j += (long long)gridDim.x * blockDim.x) {
+    const long long i = 2 * j;
     const bool has0 = i < n, has1 = i + 1 < n;
     const uint32_t c0 = has0 ? scale_codes[i] : 1u, c1 = has1 ? scale_codes[i + 1] : 1u;
-    const float y0 = e4m3_recip(c0, table), y1 = e4m3_recip(c1, table);
     const float s0 = e4m3_to_f32(c0), s1 = e4m3_to_f32(c1);
+    const float y0 = e4m3_recip(s0), y1 = e4m3_recip(s1);
     float a, b;
     f2_split(div2_by_recip(f2(has0 ? x[i] : 0.f, has1 ? x[i + 1] : 0.f), f2(-s0, -s1), f2(y0, y1)),
              a, b);
@@ -66,6 +63,26 @@ __global__ void fp4_quotient_selftest_kernel(const float* x, const unsigned char
       q_ieee[i + 1] = __fdiv_rn(x[i + 1], s1);
     }
   }
+}
+
+// The FP4 quantizer's reciprocal of an e4m3 value next to the IEEE
+// reciprocal: element i is the value of code codes[i].
+__global__ void e4m3_recip_selftest_kernel(const unsigned char* codes, long long n, float* y_fast,
+                                           float* y_ieee) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float s = e4m3_to_f32(codes[i]);
+    y_fast[i] = e4m3_recip(s);
+    y_ieee[i] = __frcp_rn(s);
+  }
+}
+
+cudaError_t launch_e4m3_recip_selftest(const unsigned char* codes, long long n, float* y_fast,
+                                       float* y_ieee, cudaStream_t stream) {
+  const long long want = (n + 255) / 256;
+  const int grid = (int)(want < 1024 ? want : 1024);
+  e4m3_recip_selftest_kernel<<<grid, 256, 0, stream>>>(codes, n, y_fast, y_ieee);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_fp4_quotient_selftest(const float* x, const unsigned char* scale_codes,

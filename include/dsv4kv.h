@@ -297,6 +297,18 @@ int dsv4kv_selftest_fp4_quotient(const float *x, const unsigned char *scale_code
                                  float *q_fast, float *q_ieee, void *stream);
 
 /*
+ * Self-test of the reciprocal that the V41_FP4 quantizer's division starts
+ * from (no counterpart on the pages): for each i, with s = the e4m3 value of
+ * codes[i], writes the quantizer's reciprocal (one Newton-Raphson step from
+ * the hardware approximation) to y_fast[i] and the IEEE reciprocal to
+ * y_ieee[i]; for every positive finite code (0x01..0x7E) the two must agree
+ * bit for bit.  codes: uint8 [n] device; y_fast, y_ieee: fp32 [n] device.
+ * Returns DSV4KV_EINVAL for n < 0, a null or misaligned pointer.
+ */
+int dsv4kv_selftest_e4m3_recip(const unsigned char *codes, long long n, float *y_fast,
+                               float *y_ieee, void *stream);
+
+/*
  * Fake quantization [KVL test table: fake_quant_compressed_kv,
  * fake_quant_fp4]: out_bf16[i] = bf16(dequant(store_row(in_bf16[i]))) for
  * each of n rows, with the layout's own store_row and dequantizer, so the

@@ -511,6 +511,23 @@ def test_fp4_quotient_matches_ieee_division_for_every_scale(B):
     assert int(bad.sum()) == 0, f"{int(bad.sum())} quotients differ, e.g. {x[bad][:4].tolist()}"
 
 
+def test_fp4_reciprocal_is_the_ieee_reciprocal_for_every_scale(B):
+    """The FP4 quantizer's reciprocal of the e4m3 scale (one Newton-Raphson
+    step from the hardware approximation) equals the IEEE reciprocal, and
+    hence the oracle's fp64 1/s rounded to fp32, for all 126 positive finite
+    e4m3 codes."""
+    codes = torch.arange(1, 127, dtype=torch.uint8, device="cuda")
+    y_fast = torch.empty(126, dtype=torch.float32, device="cuda")
+    y_ieee = torch.empty_like(y_fast)
+    st = B.lib().dsv4kv_selftest_e4m3_recip(codes.data_ptr(), 126, y_fast.data_ptr(),
+                                            y_ieee.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    want = np.array([1.0 / oracle.e4m3_value(c) for c in range(1, 127)]).astype(np.float32)
+    assert np.array_equal(y_ieee.cpu().numpy().view(np.int32), want.view(np.int32))
+    assert np.array_equal(y_fast.cpu().numpy().view(np.int32), want.view(np.int32))
+
+
 @pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4, oracle.V4])
 def test_guard_regions_around_pool_output_and_ring_stay_untouched(B, layout):
     """The pool, the gathered output and the ring sit inside larger buffers
