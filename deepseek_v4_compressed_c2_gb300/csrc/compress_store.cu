@@ -288,10 +288,10 @@ __device__ __forceinline__ RowDesc plan_row(const StoreParams& p, long long k, l
 // compressed index c (-1 when the page index is past the table).
 __device__ __forceinline__ long long dest_slot(const StoreParams& p, long long k, const RowDesc& d) {
   if (p.out_loc) return p.out_loc[k];
-  const long long lp = (long long)d.c >> p.page_bits;
+  const int lp = d.c >> p.page_bits;     // page_bits <= 16
   if (d.c < 0 || lp >= p.max_pages) return -1;
   return ((long long)p.page_table[(long long)d.r * p.max_pages + lp] << p.page_bits)
-         | ((long long)d.c & ((1LL << p.page_bits) - 1));
+         | (long long)(d.c & ((1 << p.page_bits) - 1));
 }
 
 __device__ __forceinline__ void zero_row_outputs(const StoreParams& p, long long k, int lane) {
@@ -588,7 +588,7 @@ template <int L, int RATIO, bool NORM, bool ROPE, int SHAPE>
 __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_t* s_stage,
                                               const RowDesc* s_desc, uint64_t* s_full,
                                               uint64_t* s_empty, volatile int* abort,
-                                              long long n_tiles, int warp, int lane) {
+                                              int n_tiles, int warp, int lane) {
   using TL = StoreTile<RATIO, NORM, ROPE, SHAPE>;
   float w[16];
   if constexpr (NORM) {
@@ -596,9 +596,11 @@ __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_
     unpack_bf16x8(__ldg(wp + lane), w);
     unpack_bf16x8(__ldg(wp + 32 + lane), w + 8);
   }
-  long long it = 0;
-  for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
-    const int s = (int)(it % TL::kStages);
+  // iteration it uses stage it % kStages for the (it / kStages)-th time (32-bit:
+  // the producer's incremental form costs this loop registers and spills)
+  int it = 0;
+  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+    const int s = it % TL::kStages;
     const uint32_t use = (uint32_t)(it / TL::kStages);
     if (!mbar_wait(&s_full[s * TL::kWarps + warp], use & 1u, abort, p.err)) break;
     RowDesc d[TL::kRowsPerWarp];
@@ -609,7 +611,7 @@ __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_
       const int t = warp * TL::kRowsPerWarp + q;
       d[q] = s_desc[s * TL::kRows + t];
       const bool ok = d[q].state == kRowOk || d[q].state == kRowOkRing;
-      slot[q] = ok ? dest_slot(p, tile * TL::kRows + t, d[q]) : 0;
+      slot[q] = ok ? dest_slot(p, (long long)tile * TL::kRows + t, d[q]) : 0;
       const uint8_t* stage = s_stage + s * TL::kStageBytes;
       if (ok)
         load_row<RATIO, ROPE>(stage + t * TL::kInBytes,
@@ -619,7 +621,7 @@ __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_
     if (lane == 0) mbar_arrive(&s_empty[s]);
 #pragma unroll
     for (int q = 0; q < TL::kRowsPerWarp; ++q) {
-      const long long k = tile * TL::kRows + warp * TL::kRowsPerWarp + q;
+      const long long k = (long long)tile * TL::kRows + warp * TL::kRowsPerWarp + q;
       process_row<L, RATIO, NORM, ROPE>(p, k, d[q], slot[q], in[q], w, lane);
     }
   }
@@ -663,7 +665,7 @@ compress_store_kernel(const StoreParams p) {
     return;
   __syncthreads();
   const long long total = s_base[p.n_slots];
-  const long long n_tiles = ((long long)p.n_out + TL::kRows - 1) / TL::kRows;
+  const int n_tiles = (int)(((long long)p.n_out + TL::kRows - 1) / TL::kRows);
 
   if (warp == TL::kWarps) {
     // ------------------------------------------------------------ producer
@@ -671,17 +673,16 @@ compress_store_kernel(const StoreParams p) {
     const __nv_bfloat16* score_base = p.score ? p.score : p.rows + kDim;
     const long long sstride = p.score ? p.score_stride : p.row_stride;
     const bool fused_pair = p.score == nullptr && p.row_stride == 2 * kDim;
-    long long it = 0;
-    for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
-      const int s = (int)(it % kStages);
-      const uint32_t use = (uint32_t)(it / kStages);
+    int it = 0, s = 0;          // iterations; stage s, used `use` times before
+    uint32_t use = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
       if (use > 0 && !mbar_wait(&s_empty[s], (use - 1) & 1u, abort, p.err)) break;
       RowDesc d;
       d.state = kRowNone;
       long long src = 0;
       if (lane < TL::kRows) {
-        d = plan_row<RATIO, ROPE, RING>(p, tile * TL::kRows + lane, total, s_base, s_first, s_start,
-                                        s_count, src);
+        d = plan_row<RATIO, ROPE, RING>(p, (long long)tile * TL::kRows + lane, total, s_base, s_first,
+                                        s_start, s_count, src);
         s_desc[s * TL::kRows + lane] = d;
       }
       // each consumer warp's rows complete on that warp's own barrier: the
@@ -740,12 +741,13 @@ compress_store_kernel(const StoreParams p) {
           bulk_g2s(stage + TL::kRows * TL::kInBytes + lane * TL::kRopeBytes,
                    p.freqs + (long long)d.pos * kRopeDim, kRopeDim * 4, bar, pol);
       }
+      if (++s == kStages) { s = 0; ++use; }
     }
     // every issued copy has landed before the CTA may exit (bounded)
     if (lane < TL::kWarps) {
-      for (int s = 0; s < kStages && s < it; ++s) {
-        const uint32_t last_use = (uint32_t)((it - 1 - s) / kStages);
-        uint64_t* bar = &s_full[s * TL::kWarps + lane];
+      for (int st = 0; st < kStages && st < it; ++st) {
+        const uint32_t last_use = (uint32_t)((it - 1 - st) / kStages);
+        uint64_t* bar = &s_full[st * TL::kWarps + lane];
         for (uint32_t i = 0; i < kSpinLimit && !mbar_try_wait(bar, last_use & 1u); ++i) {
         }
       }

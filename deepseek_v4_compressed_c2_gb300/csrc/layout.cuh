@@ -68,11 +68,10 @@ template <int L>
 struct PagedKV {
   uint8_t* base;
   int page_bits;
+  // pages are unpadded, so row (page, off) sits at (page * 2^page_bits + off)
+  // = slot rows from the base
   __device__ __forceinline__ uint8_t* row(long long slot) const {
-    const long long page = slot >> page_bits;
-    const long long off = slot & ((1LL << page_bits) - 1);
-    return base + page * ((long long)LayoutTraits<L>::kRowBytes << page_bits)
-                + off * LayoutTraits<L>::kRowBytes;
+    return base + slot * LayoutTraits<L>::kRowBytes;
   }
 };
 
