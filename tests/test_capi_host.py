@@ -236,3 +236,23 @@ def test_fake_quant_rejects_bad_arguments(B):
     assert f(1, FAKE, 10, 500, FAKE, None) == -1            # stride below 512
     assert f(1, FAKE, 10, 516, FAKE, None) == -1            # stride not a multiple of 8
     assert f(1, None, 0, 512, None, None) == 0              # nothing to do
+
+
+def test_selftests_reject_bad_arguments(B):
+    """The self-test calls validate on the host like the others: no launch for
+    a negative count or a null or misaligned pointer; n = 0 is a no-op."""
+    L = B.lib()
+    q = L.dsv4kv_selftest_fp4_quotient
+    assert q(FAKE, FAKE, -1, FAKE, FAKE, None) == -1
+    assert q(None, FAKE, 4, FAKE, FAKE, None) == -1
+    assert q(FAKE + 2, FAKE, 4, FAKE, FAKE, None) == -1     # misaligned fp32 input
+    assert q(None, None, 0, None, None, None) == 0
+    r = L.dsv4kv_selftest_e4m3_recip
+    assert r(FAKE, -1, FAKE, FAKE, None) == -1
+    assert r(None, 4, FAKE, FAKE, None) == -1
+    assert r(FAKE, 4, FAKE + 2, FAKE, None) == -1           # misaligned fp32 output
+    assert r(FAKE, 4, FAKE, None, None) == -1
+    assert r(None, 0, None, None, None) == 0
+    w = L.dsv4kv_selftest_bounded_wait
+    assert w(0, FAKE, FAKE, None) == -3                      # polls outside 1..2^24: ERANGE
+    assert w(100, None, FAKE, None) == -1
