@@ -627,6 +627,71 @@ __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_
   }
 }
 
+// The wide launch (ratio 1, rows only stored): each half-warp takes one of
+// the warp's two rows in the half-warp layout of the chunk quantizers, so the
+// per-row work (descriptor, row state, destination lookup, addressing) is
+// one instruction stream for both rows instead of one per row.  Row states
+// and outputs follow process_row: none -> nothing; pad / bad -> zeroed debug
+// outputs (bad: one fault); ok -> a fault if the slot is past the pool, the
+// debug outputs, and the stored row when 0 < slot < pool_rows.
+template <int L>
+__device__ __forceinline__ void consume_tiles_half(const StoreParams& p, const uint8_t* s_stage,
+                                                   const RowDesc* s_desc, uint64_t* s_full,
+                                                   uint64_t* s_empty, volatile int* abort,
+                                                   int n_tiles, int warp, int lane) {
+  using TL = StoreTile<1, false, false, kShapeWide>;
+  static_assert(TL::kRowsPerWarp == 2, "one row per half-warp");
+  const int l = lane & 15;
+  const int t = warp * 2 + (lane >> 4);     // this half's row in the tile
+  int it = 0;
+  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+    const int s = it % TL::kStages;
+    const uint32_t use = (uint32_t)(it / TL::kStages);
+    if (!mbar_wait(&s_full[s * TL::kWarps + warp], use & 1u, abort, p.err)) break;
+    const RowDesc d = s_desc[s * TL::kRows + t];
+    const long long k = (long long)tile * TL::kRows + t;
+    const bool ok = d.state == kRowOk;
+    const long long slot = ok ? dest_slot(p, k, d) : 0;
+    const uint4* src = reinterpret_cast<const uint4*>(s_stage + s * TL::kStageBytes + t * TL::kInBytes);
+    uint4 v[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) v[c] = ok ? src[16 * c + l] : make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_empty[s]);
+    if (!ok && d.state != kRowNone) {       // pad or bad (no shuffles on this branch)
+      if (d.state == kRowBad && l == 0 && p.err) atomicAdd(p.err, 1);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (p.latent_out)
+          reinterpret_cast<uint4*>(p.latent_out + k * kDim)[16 * c + l] = make_uint4(0u, 0u, 0u, 0u);
+        if (p.prequant_out) {
+          float4* o = reinterpret_cast<float4*>(p.prequant_out + k * kDim) + 32 * c + 2 * l;
+          o[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+          o[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+    const bool store = ok && slot > 0 && slot < p.pool_rows;
+    if (ok && slot != 0 && !store && l == 0 && p.err) atomicAdd(p.err, 1);   // destination fault
+    uint8_t* row = store ? PagedKV<L>{p.pool, p.page_bits}.row(slot) : nullptr;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float x[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        f2_split(f2_from_bf16x2(word_of(v[c], q)), x[2 * q], x[2 * q + 1]);
+      if (ok && p.latent_out)   // no RMSNorm: the latent is the row itself
+        reinterpret_cast<uint4*>(p.latent_out + k * kDim)[16 * c + l] = pack_bf16x8(x);
+      if (ok && p.prequant_out) {
+        float4* o = reinterpret_cast<float4*>(p.prequant_out + k * kDim) + 32 * c + 2 * l;
+        o[0] = make_float4(x[0], x[1], x[2], x[3]);
+        o[1] = make_float4(x[4], x[5], x[6], x[7]);
+      }
+      store_chunk<L>(x, row, c, l, store);
+    }
+  }
+}
+
 // RING: ratio 2 with start positions and/or the pair-state ring.  The
 // launches without either take RING = false, whose kernel has no ring code.
 template <int L, int RATIO, bool NORM, bool ROPE, bool RING, int SHAPE>
@@ -757,8 +822,11 @@ compress_store_kernel(const StoreParams p) {
     // ------------------------------------------------------------ consumers
     if constexpr (RATIO == 2 && RING)
       ring_phase<L, NORM, ROPE, TL::kWarps>(p, s_base, s_first, s_start, s_count, warp, lane);
-    consume_tiles<L, RATIO, NORM, ROPE, SHAPE>(p, s_stage, s_desc, s_full, s_empty, abort, n_tiles,
-                                               warp, lane);
+    if constexpr (SHAPE == kShapeWide)
+      consume_tiles_half<L>(p, s_stage, s_desc, s_full, s_empty, abort, n_tiles, warp, lane);
+    else
+      consume_tiles<L, RATIO, NORM, ROPE, SHAPE>(p, s_stage, s_desc, s_full, s_empty, abort,
+                                                 n_tiles, warp, lane);
     allow_dependent_launch();
   }
 }
