@@ -73,18 +73,34 @@ fake_quant_kernel(const __nv_bfloat16* in, long long n, long long in_stride, __n
   }
 }
 
+// One wave: the grid is the resident CTAs (SMs x CTAs per SM at the kernel's
+// register count), so no CTA starts after another has finished its rows.
+template <int L>
+static cudaError_t launch_fq(const __nv_bfloat16* in, long long n, long long in_stride,
+                             __nv_bfloat16* out, cudaStream_t stream) {
+  static int per_sm_of_device[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int per_sm = dev < 64 ? per_sm_of_device[dev] : 0;
+  if (per_sm == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fake_quant_kernel<L>, kFqWarps * 32, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    if (dev < 64) per_sm_of_device[dev] = per_sm;
+  }
+  const long long want = (n + kFqWarps - 1) / kFqWarps;
+  const long long cap = (long long)device_sm_count() * per_sm;
+  const int grid = (int)(want < cap ? want : cap);
+  fake_quant_kernel<L><<<grid, kFqWarps * 32, 0, stream>>>(in, n, in_stride, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fake_quant(int layout, const __nv_bfloat16* in, long long n,
                               long long in_stride, __nv_bfloat16* out, cudaStream_t stream) {
-  const long long want = (n + kFqWarps - 1) / kFqWarps;
-  const long long cap = (long long)device_sm_count() * 8;
-  const int grid = (int)(want < cap ? want : cap);
-  if (layout == kV41)
-    fake_quant_kernel<kV41><<<grid, kFqWarps * 32, 0, stream>>>(in, n, in_stride, out);
-  else if (layout == kV41Fp4)
-    fake_quant_kernel<kV41Fp4><<<grid, kFqWarps * 32, 0, stream>>>(in, n, in_stride, out);
-  else
-    fake_quant_kernel<kV4><<<grid, kFqWarps * 32, 0, stream>>>(in, n, in_stride, out);
-  return cudaGetLastError();
+  if (layout == kV41) return launch_fq<kV41>(in, n, in_stride, out, stream);
+  if (layout == kV41Fp4) return launch_fq<kV41Fp4>(in, n, in_stride, out, stream);
+  return launch_fq<kV4>(in, n, in_stride, out, stream);
 }
 
 }  // namespace dsv4kv

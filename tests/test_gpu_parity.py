@@ -204,6 +204,42 @@ def test_every_layout_ratio_norm_rope_combination(B):
                     check_store(B, cfg, min_allowed=3)
 
 
+@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4, oracle.V4])
+def test_ratio1_store_only_row_states_and_faults(B, layout):
+    """The store-only ratio-1 launch (one row per half-warp) against the
+    oracle with rows of every state next to each other in a warp: valid rows,
+    rows of a request that starts before the rows buffer or runs past it
+    (faults; zeroed debug outputs), padding past the plan's total, and
+    destinations that are padding (0), past the pool or negative (faults).
+    Store-only rows are exact bf16, so the pool must equal the oracle's
+    byte for byte."""
+    rng = np.random.default_rng(41 + layout)
+    lens = [37, 5, 64, 3, 90, 1]
+    n_rows = sum(lens)
+    rows = W.bf16_normal(rng, (n_rows, 512))
+    ext = np.zeros((2, len(lens)), np.int32)
+    ext[0] = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    ext[1] = lens
+    ext[0, 1] = -3                       # starts before the rows buffer
+    ext[0, 3] = n_rows - 1               # runs two rows past it
+    total = n_rows
+    n_out = total + 11                   # padding rows at the end
+    pool_rows = 512
+    out_loc = (rng.permutation(pool_rows - 1)[:n_out] + 1).astype(np.int32)
+    out_loc[[4, 40, 41]] = 0             # padding destinations: not stored, no fault
+    out_loc[[7, 100]] = pool_rows        # past the pool: faults
+    out_loc[[12, 150]] = -9              # negative: faults
+    cfg = dict(layout=layout, ratio=1, rows=rows, score=None, ext=ext, page_table=None,
+               page_bits=6, norm_w=None, freqs=None, eps=1e-6, n_out=n_out,
+               pool_rows=pool_rows)
+    g, ref = check_store(B, cfg, out_loc=out_loc, exact_codes=True)
+    assert g["err"] == ref["faults"] == 9
+    # output rows of source rows -3..-1 (request 1) and n_rows, n_rows + 1
+    # (request 3): faults with zeroed debug outputs
+    bad = np.array([37, 38, 39, 107, 108])
+    assert not g["pre"][bad].any() and not g["lat"][bad].any()
+
+
 # ------------------------------------------------------------ edge cases
 def test_empty_and_all_padding_calls(B):
     cfg = W.cfg1_v41_roundtrip()
