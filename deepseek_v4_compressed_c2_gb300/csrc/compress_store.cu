@@ -643,6 +643,12 @@ __device__ __forceinline__ void consume_tiles_half(const StoreParams& p, const u
   static_assert(TL::kRowsPerWarp == 2, "one row per half-warp");
   const int l = lane & 15;
   const int t = warp * 2 + (lane >> 4);     // this half's row in the tile
+  // the 16-byte unit (8 dims) of the row that chunk c of sub-lane l holds:
+  // dims 128c + 8l, or for FP4 the halves of groups l (c = 0, 1) and 16 + l
+  // (c = 2, 3)
+  int unit[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) unit[c] = L == kV41Fp4 ? 32 * (c >> 1) + 2 * l + (c & 1) : 16 * c + l;
   int it = 0;
   for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
     const int s = it % TL::kStages;
@@ -655,7 +661,7 @@ __device__ __forceinline__ void consume_tiles_half(const StoreParams& p, const u
     const uint4* src = reinterpret_cast<const uint4*>(s_stage + s * TL::kStageBytes + t * TL::kInBytes);
     uint4 v[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) v[c] = ok ? src[16 * c + l] : make_uint4(0u, 0u, 0u, 0u);
+    for (int c = 0; c < 4; ++c) v[c] = ok ? src[unit[c]] : make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
     if (lane == 0) mbar_arrive(&s_empty[s]);
     if (!ok && d.state != kRowNone) {       // pad or bad (no shuffles on this branch)
@@ -663,9 +669,9 @@ __device__ __forceinline__ void consume_tiles_half(const StoreParams& p, const u
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         if (p.latent_out)
-          reinterpret_cast<uint4*>(p.latent_out + k * kDim)[16 * c + l] = make_uint4(0u, 0u, 0u, 0u);
+          reinterpret_cast<uint4*>(p.latent_out + k * kDim)[unit[c]] = make_uint4(0u, 0u, 0u, 0u);
         if (p.prequant_out) {
-          float4* o = reinterpret_cast<float4*>(p.prequant_out + k * kDim) + 32 * c + 2 * l;
+          float4* o = reinterpret_cast<float4*>(p.prequant_out + k * kDim) + 2 * unit[c];
           o[0] = make_float4(0.f, 0.f, 0.f, 0.f);
           o[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -674,6 +680,7 @@ __device__ __forceinline__ void consume_tiles_half(const StoreParams& p, const u
     const bool store = ok && slot > 0 && slot < p.pool_rows;
     if (ok && slot != 0 && !store && l == 0 && p.err) atomicAdd(p.err, 1);   // destination fault
     uint8_t* row = store ? PagedKV<L>{p.pool, p.page_bits}.row(slot) : nullptr;
+    float xg[16];                             // FP4: the group being assembled
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       float x[8];
@@ -681,13 +688,19 @@ __device__ __forceinline__ void consume_tiles_half(const StoreParams& p, const u
       for (int q = 0; q < 4; ++q)
         f2_split(f2_from_bf16x2(word_of(v[c], q)), x[2 * q], x[2 * q + 1]);
       if (ok && p.latent_out)   // no RMSNorm: the latent is the row itself
-        reinterpret_cast<uint4*>(p.latent_out + k * kDim)[16 * c + l] = pack_bf16x8(x);
+        reinterpret_cast<uint4*>(p.latent_out + k * kDim)[unit[c]] = pack_bf16x8(x);
       if (ok && p.prequant_out) {
-        float4* o = reinterpret_cast<float4*>(p.prequant_out + k * kDim) + 32 * c + 2 * l;
+        float4* o = reinterpret_cast<float4*>(p.prequant_out + k * kDim) + 2 * unit[c];
         o[0] = make_float4(x[0], x[1], x[2], x[3]);
         o[1] = make_float4(x[4], x[5], x[6], x[7]);
       }
-      store_chunk<L>(x, row, c, l, store);
+      if constexpr (L == kV41Fp4) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xg[8 * (c & 1) + i] = x[i];
+        if (c & 1) store_group_fp4(xg, row, 16 * (c >> 1) + l, store);
+      } else {
+        store_chunk<L>(x, row, c, l, store);
+      }
     }
   }
 }
