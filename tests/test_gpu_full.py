@@ -81,6 +81,43 @@ def test_gather_262144_of_1m_rows_with_4_layer_reuse(B):
     assert np.array_equal(host_u16(buf.storage), want)
 
 
+@pytest.mark.parametrize("layout", [oracle.V41_FP4, oracle.V4])
+def test_store_only_1m_rows_sampled(B, layout):
+    """The store-only ratio-1 launch at the size the benchmark times it
+    (1,048,512 rows into a 1 Mi-row pool, page 0 reserved) in the FP4 and V4
+    layouts: 4096 sampled rows against the oracle's quantizer (store-only rows
+    are the bf16 inputs exactly), page 0 untouched, and the dequant of the
+    sampled rows equal to the oracle's."""
+    rb = oracle.row_bytes(layout)
+    pool_rows = 1 << 20
+    n = pool_rows - 64
+    g = torch.Generator(device="cuda")
+    g.manual_seed(40 + layout)
+    lat = torch.randn((n, 512), generator=g, device="cuda").to(torch.bfloat16)
+    ext = torch.tensor([[0], [n]], dtype=torch.int32, device="cuda")
+    pt = torch.arange(1, pool_rows // 64, dtype=torch.int32, device="cuda").view(1, -1)
+    pool = torch.zeros(pool_rows * rb, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsv4kv_compress_store(layout, 1, lat, ext, pool, page_table=pt, page_bits=6, n_out=n,
+                            err_word=err)
+    rng = np.random.default_rng(layout)
+    sample = np.sort(rng.choice(n, 4096, replace=False))
+    ids = dev((sample + 64).astype(np.int32))
+    out = B.dsv4kv_dequant_gather(layout, pool, ids, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = host_u16(lat[torch.from_numpy(sample).cuda()])
+    x = oracle.bf16_to_f64(rows).astype(np.float32)
+    want_rows = oracle.quantize_rows(layout, x)
+    host_pool = pool.cpu().numpy()
+    assert np.array_equal(host_pool.reshape(-1, rb)[64 + sample], want_rows)
+    assert not host_pool[:64 * rb].any()
+    want, faults = oracle.dequant_gather(layout, want_rows.reshape(-1), 4096,
+                                         np.arange(4096, dtype=np.int32))
+    assert faults == 0
+    assert np.array_equal(host_u16(out), want)
+
+
 def test_long_prefill_ratio2_store_and_topk_gather(B):
     cfg = W.cfg5_long_prefill()
     rb = 528
