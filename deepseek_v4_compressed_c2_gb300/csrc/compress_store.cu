@@ -29,7 +29,9 @@
 //    normalise, rotate, quantize and store the row.  Lane l
 //    holds dims 8l..8l+7 and 256+8l..263+8l, so every shared-memory read is
 //    conflict-free and every global store of a row half is one contiguous
-//    warp access;
+//    warp access; the wide launch of store-only ratio-1 rows gives each
+//    half-warp one row instead (consume_tiles_half), so the per-row work of
+//    a warp's two rows is one instruction stream;
 //  * with start positions or the pair-state ring (decode, verify, chunked
 //    prefill) the consumers first run the per-request ring phase.
 //  All waits are bounded (see tma.cuh).
@@ -47,9 +49,9 @@ namespace dsv4kv {
 // Latency (ring-form steps small enough for one row per consumer warp: decode
 // and speculative verify): 16 consumer warps, 2 stages, one CTA per SM, so a
 // step of up to 16 rows per SM finishes after one row's latency per warp.
-// Wide (ratio-1 rows that are only stored): 8 consumer warps of 2 rows, 2
-// stages, three CTAs per SM (72 registers): the store-only quantizers are
-// latency-bound at two CTAs per SM.
+// Wide (ratio-1 rows that are only stored): 8 consumer warps of 2 rows, one
+// per half-warp, 2 stages, three CTAs per SM (72 registers): the store-only
+// quantizers are latency-bound at two CTAs per SM.
 enum StoreShapeId : int { kShapeStream = 0, kShapeLatency = 1, kShapeWide = 2 };
 
 template <int SHAPE>
