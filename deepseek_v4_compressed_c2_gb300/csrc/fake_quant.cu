@@ -12,6 +12,8 @@
 // equals a store followed by a gather of that row bit for bit.  A lane reads
 // and writes only its own 16-byte chunks (dims 8l..8l+7 and 256+8l..), so
 // in == out is allowed.
+#include <atomic>
+
 #include "internal.cuh"
 #include "launchers.cuh"
 #include "quant.cuh"
@@ -78,16 +80,16 @@ fake_quant_kernel(const __nv_bfloat16* in, long long n, long long in_stride, __n
 template <int L>
 static cudaError_t launch_fq(const __nv_bfloat16* in, long long n, long long in_stride,
                              __nv_bfloat16* out, cudaStream_t stream) {
-  static int per_sm_of_device[64] = {0};
+  static std::atomic<int> per_sm_of_device[64];   // 0: not queried yet
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int per_sm = dev < 64 ? per_sm_of_device[dev] : 0;
+  int per_sm = dev < 64 ? per_sm_of_device[dev].load(std::memory_order_relaxed) : 0;
   if (per_sm == 0) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fake_quant_kernel<L>, kFqWarps * 32, 0);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    if (dev < 64) per_sm_of_device[dev] = per_sm;
+    if (dev < 64) per_sm_of_device[dev].store(per_sm, std::memory_order_relaxed);
   }
   const long long want = (n + kFqWarps - 1) / kFqWarps;
   const long long cap = (long long)device_sm_count() * per_sm;
