@@ -41,7 +41,10 @@ class dsv4kv_kvbuf(ctypes.Structure):
                 ("head_valid", ctypes.c_int), ("head_layout", ctypes.c_int),
                 ("head_pool", ctypes.c_void_p), ("head_pool_rows", ctypes.c_longlong),
                 ("head_ids", ctypes.c_void_p), ("head_n", ctypes.c_longlong),
-                ("head_map", ctypes.c_ulonglong)]
+                ("head_form", ctypes.c_int), ("head_k", ctypes.c_int),
+                ("head_token_to_req", ctypes.c_void_p), ("head_is_valid", ctypes.c_void_p),
+                ("head_page_table", ctypes.c_void_p), ("head_n_req", ctypes.c_int),
+                ("head_max_pages", ctypes.c_int), ("head_page_bits", ctypes.c_int)]
 
 
 def lib():

@@ -4,6 +4,7 @@
 // Every host-checkable error is rejected here, before any CUDA call, so a
 // failing call launches nothing.  Device-only faults are counted by the
 // kernels in the caller's err_word.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -26,15 +27,20 @@ static int cuda_status(cudaError_t e) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// SMs of the current device, cached per device (atomics: host threads may
+// launch concurrently; a race only repeats the query)
 int device_sm_count() {
   constexpr int kMaxDevices = 64;
-  static int cache[kMaxDevices] = {0};
+  static std::atomic<int> cache[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
-  if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+  if (dev < kMaxDevices) {
+    const int seen = cache[dev].load(std::memory_order_relaxed);
+    if (seen > 0) return seen;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  if (dev < kMaxDevices) cache[dev] = n;
+  if (dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -287,18 +293,100 @@ int dsv4kv_selftest_e4m3_recip(const unsigned char* codes, long long n, float* y
 }
 
 // ----------------------------------------------------------------- reuse
-int dsv4kv_kvbuf_init(dsv4kv_kvbuf* buf, void* storage_bf16, long long capacity_rows) {
-  if (!buf || capacity_rows < 0) return DSV4KV_EINVAL;
-  if (capacity_rows > 0 && (!storage_bf16 || !aligned16(storage_bf16))) return DSV4KV_EINVAL;
-  buf->storage = storage_bf16;
-  buf->capacity_rows = capacity_rows;
+}  // extern "C"
+
+namespace {
+
+// What the reuse buffer's storage holds: the gathered source, and for the
+// top-k and short-context forms the id mapping, every field kept as given.
+struct KvbufKey {
+  int form;
+  int layout;
+  const void* pool;
+  long long pool_rows;
+  const int* ids;
+  long long n;
+  int k;
+  const int* token_to_req;
+  const unsigned char* is_valid;
+  const int* page_table;
+  int n_req, max_pages, page_bits;
+};
+
+KvbufKey ids_key(int layout, const void* pool, long long pool_rows, const int* ids, long long n) {
+  return KvbufKey{DSV4KV_KVBUF_IDS, layout, pool, pool_rows, ids, n, 0, nullptr, nullptr, nullptr,
+                  0, 0, 0};
+}
+
+KvbufKey mapped_key(int form, int layout, const void* pool, long long pool_rows, const int* ids,
+                    int n_tok, int k, const int* token_to_req, const unsigned char* is_valid,
+                    const int* page_table, int n_req, int max_pages, int page_bits) {
+  return KvbufKey{form,         layout,   pool,       pool_rows, ids,       (long long)n_tok * k,
+                  k,            token_to_req, is_valid, page_table, n_req, max_pages, page_bits};
+}
+
+void kvbuf_clear(dsv4kv_kvbuf* buf) {
   buf->head_valid = 0;
+  buf->head_form = DSV4KV_KVBUF_IDS;
   buf->head_layout = -1;
   buf->head_pool = nullptr;
   buf->head_pool_rows = 0;
   buf->head_ids = nullptr;
   buf->head_n = 0;
-  buf->head_map = 0;
+  buf->head_k = 0;
+  buf->head_token_to_req = nullptr;
+  buf->head_is_valid = nullptr;
+  buf->head_page_table = nullptr;
+  buf->head_n_req = 0;
+  buf->head_max_pages = 0;
+  buf->head_page_bits = 0;
+}
+
+// The head decision: a hit when every field equals the head's; on a miss the
+// key becomes the head.
+int kvbuf_lookup_key(dsv4kv_kvbuf* buf, const KvbufKey& q, int* hit) {
+  if (!buf || !hit || q.n < 0) return DSV4KV_EINVAL;
+  if (q.n > buf->capacity_rows) return DSV4KV_ERANGE;
+  const bool same = buf->head_valid && buf->head_form == q.form &&
+                    buf->head_layout == q.layout && buf->head_pool == q.pool &&
+                    buf->head_pool_rows == q.pool_rows && buf->head_ids == q.ids &&
+                    buf->head_n == q.n && buf->head_k == q.k &&
+                    buf->head_token_to_req == q.token_to_req &&
+                    buf->head_is_valid == q.is_valid && buf->head_page_table == q.page_table &&
+                    buf->head_n_req == q.n_req && buf->head_max_pages == q.max_pages &&
+                    buf->head_page_bits == q.page_bits;
+  if (same) {
+    *hit = 1;
+    return DSV4KV_OK;
+  }
+  *hit = 0;
+  buf->head_valid = 1;
+  buf->head_form = q.form;
+  buf->head_layout = q.layout;
+  buf->head_pool = q.pool;
+  buf->head_pool_rows = q.pool_rows;
+  buf->head_ids = q.ids;
+  buf->head_n = q.n;
+  buf->head_k = q.k;
+  buf->head_token_to_req = q.token_to_req;
+  buf->head_is_valid = q.is_valid;
+  buf->head_page_table = q.page_table;
+  buf->head_n_req = q.n_req;
+  buf->head_max_pages = q.max_pages;
+  buf->head_page_bits = q.page_bits;
+  return DSV4KV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dsv4kv_kvbuf_init(dsv4kv_kvbuf* buf, void* storage_bf16, long long capacity_rows) {
+  if (!buf || capacity_rows < 0) return DSV4KV_EINVAL;
+  if (capacity_rows > 0 && (!storage_bf16 || !aligned16(storage_bf16))) return DSV4KV_EINVAL;
+  buf->storage = storage_bf16;
+  buf->capacity_rows = capacity_rows;
+  kvbuf_clear(buf);
   return DSV4KV_OK;
 }
 
@@ -314,55 +402,9 @@ int dsv4kv_kvbuf_get(dsv4kv_kvbuf* buf, long long n, void** rows) {
   return DSV4KV_OK;
 }
 
-}  // extern "C"
-
-// The head decision with the mapping fingerprint (0: plain ids).
-static int kvbuf_lookup_map(dsv4kv_kvbuf* buf, int layout, const void* pool, long long pool_rows,
-                            const int* ids, long long n, unsigned long long map, int* hit) {
-  if (!buf || !hit || n < 0) return DSV4KV_EINVAL;
-  if (n > buf->capacity_rows) return DSV4KV_ERANGE;
-  const bool same = buf->head_valid && buf->head_layout == layout && buf->head_pool == pool &&
-                    buf->head_pool_rows == pool_rows && buf->head_ids == ids && buf->head_n == n &&
-                    buf->head_map == map;
-  if (same) {
-    *hit = 1;
-    return DSV4KV_OK;
-  }
-  *hit = 0;
-  buf->head_valid = 1;
-  buf->head_layout = layout;
-  buf->head_pool = pool;
-  buf->head_pool_rows = pool_rows;
-  buf->head_ids = ids;
-  buf->head_n = n;
-  buf->head_map = map;
-  return DSV4KV_OK;
-}
-
-// FNV-1a over the top-k form's mapping arguments; never 0 (0 marks plain ids).
-static unsigned long long topk_map_fingerprint(const int* token_to_req,
-                                               const unsigned char* is_valid,
-                                               const int* page_table, int n_req, int max_pages,
-                                               int page_bits, int k) {
-  const unsigned long long words[7] = {
-      (unsigned long long)(uintptr_t)token_to_req, (unsigned long long)(uintptr_t)is_valid,
-      (unsigned long long)(uintptr_t)page_table, (unsigned long long)(unsigned)n_req,
-      (unsigned long long)(unsigned)max_pages, (unsigned long long)(unsigned)page_bits,
-      (unsigned long long)(unsigned)k};
-  unsigned long long h = 1469598103934665603ull;
-  for (unsigned long long w : words)
-    for (int b = 0; b < 8; ++b) {
-      h ^= (w >> (8 * b)) & 0xFFu;
-      h *= 1099511628211ull;
-    }
-  return h | 1ull;
-}
-
-extern "C" {
-
 int dsv4kv_kvbuf_lookup(dsv4kv_kvbuf* buf, int layout, const void* pool, long long pool_rows,
                         const int* ids, long long n, int* hit) {
-  return kvbuf_lookup_map(buf, layout, pool, pool_rows, ids, n, 0ull, hit);
+  return kvbuf_lookup_key(buf, ids_key(layout, pool, pool_rows, ids, n), hit);
 }
 
 int dsv4kv_kvbuf_get_with_head(dsv4kv_kvbuf* buf, int layout, const void* pool,
@@ -391,12 +433,10 @@ int dsv4kv_kvbuf_get_with_head_all(dsv4kv_kvbuf* buf, int layout, const void* po
   const long long n = (long long)n_tok * k;
   st = check_gather(layout, pool, pool_rows, lens_in, n, buf->storage);
   if (st != DSV4KV_OK) return st;
-  // the short-context form's fingerprint differs from the top-k form's for
-  // the same pointers (its "ids" pointer is the lengths array)
-  const unsigned long long map =
-      topk_map_fingerprint(token_to_req, is_valid, page_table, n_req, max_pages, page_bits, k) ^
-      0x5a5a5a5a5a5a5a5aull;
-  st = kvbuf_lookup_map(buf, layout, pool, pool_rows, lens_in, n, map | 1ull, hit);
+  st = kvbuf_lookup_key(buf,
+                        mapped_key(DSV4KV_KVBUF_ALL, layout, pool, pool_rows, lens_in, n_tok, k,
+                                   token_to_req, is_valid, page_table, n_req, max_pages, page_bits),
+                        hit);
   if (st != DSV4KV_OK) return st;
   if (rows) *rows = buf->storage;
   if (*hit || n == 0) return DSV4KV_OK;
@@ -418,9 +458,9 @@ int dsv4kv_kvbuf_get_with_head_topk(dsv4kv_kvbuf* buf, int layout, const void* p
   const long long n = (long long)n_tok * k;
   st = check_gather(layout, pool, pool_rows, topk, n, buf->storage);
   if (st != DSV4KV_OK) return st;
-  st = kvbuf_lookup_map(buf, layout, pool, pool_rows, topk, n,
-                        topk_map_fingerprint(token_to_req, is_valid, page_table, n_req, max_pages,
-                                             page_bits, k),
+  st = kvbuf_lookup_key(buf,
+                        mapped_key(DSV4KV_KVBUF_TOPK, layout, pool, pool_rows, topk, n_tok, k,
+                                   token_to_req, is_valid, page_table, n_req, max_pages, page_bits),
                         hit);
   if (st != DSV4KV_OK) return st;
   if (rows) *rows = buf->storage;

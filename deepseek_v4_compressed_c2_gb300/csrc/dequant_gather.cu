@@ -50,9 +50,21 @@ struct GatherSrc {
   int* lens;                       // [n_tok], caller-zeroed, or nullptr
 };
 
+// Slot of request-local id `id` in page-table entry `phys` (64-bit, no wrap):
+// -1 with one fault when the entry is negative or the slot does not fit int32.
+__device__ __forceinline__ int page_slot(int phys, int id, int page_bits, int* err) {
+  const long long slot =
+      phys < 0 ? -1LL : ((long long)phys << page_bits) | (id & ((1 << page_bits) - 1));
+  if (slot < 0 || slot > 2147483647LL) {
+    if (err) atomicAdd(err, 1);
+    return -1;
+  }
+  return (int)slot;
+}
+
 // Slot of gathered row i under TOPK; -1 = zero row.  Faults: a token whose
 // request index is outside the table (counted once, at column 0), a page
-// index past the table (per entry).
+// index past the table or a page entry that is no page (per entry).
 __device__ __forceinline__ int topk_row_slot(const GatherSrc& g, long long i, int* err) {
   const long long t = i / g.k;
   const int c = (int)(i - t * g.k);
@@ -68,8 +80,7 @@ __device__ __forceinline__ int topk_row_slot(const GatherSrc& g, long long i, in
     if (err) atomicAdd(err, 1);
     return -1;
   }
-  const unsigned phys = (unsigned)__ldg(g.page_table + (long long)r * g.max_pages + lp);
-  return (int)((phys << g.page_bits) | ((unsigned)id & ((1u << g.page_bits) - 1u)));
+  return page_slot(__ldg(g.page_table + (long long)r * g.max_pages + lp), id, g.page_bits, err);
 }
 
 template <int L, bool TOPK>
@@ -283,8 +294,8 @@ __device__ __forceinline__ int tma_row_slot(const GatherSrc& g, long long base, 
         if (lp >= g.max_pages) {
           if (err) atomicAdd(err, 1);
         } else {
-          const unsigned phys = (unsigned)__ldg(g.page_table + (long long)a.r * g.max_pages + lp);
-          slot = (int)((phys << g.page_bits) | ((unsigned)a.id & ((1u << g.page_bits) - 1u)));
+          slot = page_slot(__ldg(g.page_table + (long long)a.r * g.max_pages + lp), a.id,
+                           g.page_bits, err);
         }
       }
     }

@@ -1,7 +1,11 @@
 // Bulk-copy (TMA, non-tensor) and mbarrier helpers, inline PTX for sm_100-
 // family GPUs.  Every wait is bounded: after kSpinLimit failed polls the
 // waiter raises the CTA's abort flag and reports DSV4KV_FAULT_TIMEOUT through
-// the caller's fault counter, so a kernel can always return.
+// the caller's fault counter, so a kernel can always return.  A producer
+// waits (bounded again) for the copies it issued before its CTA exits; if
+// that wait gives up too, a copy may still land in shared memory that a later
+// CTA on the SM owns, so after a timeout fault every output of the launch --
+// other CTAs' rows included -- is undefined.
 #pragma once
 #include <cstdint>
 

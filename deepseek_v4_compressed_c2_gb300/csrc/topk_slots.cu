@@ -22,8 +22,14 @@ __device__ __forceinline__ int topk_slot(int id, bool tok_ok, int r, const int* 
     if (err) atomicAdd(err, 1);
     return -1;
   }
-  const unsigned phys = (unsigned)page_table[(long long)r * max_pages + lp];
-  return (int)((phys << page_bits) | ((unsigned)id & mask));
+  // 64-bit slot: a negative entry or a slot past int32 is no page (fault)
+  const int phys = page_table[(long long)r * max_pages + lp];
+  const long long slot = phys < 0 ? -1LL : ((long long)phys << page_bits) | ((unsigned)id & mask);
+  if (slot < 0 || slot > 2147483647LL) {
+    if (err) atomicAdd(err, 1);
+    return -1;
+  }
+  return (int)slot;
 }
 
 // One CTA per token row; each thread maps 4 consecutive entries with 16-byte

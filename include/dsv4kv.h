@@ -259,9 +259,11 @@ int dsv4kv_dequant_gather_all(int layout, const void *pool, long long pool_rows,
  * _compressed_topk_to_slots, single-rank branch]:
  *   slots[t][c] = page_table[req][id >> page_bits] << page_bits
  *                 | (id & (2^page_bits - 1)),  id = topk[t][c], req = token_to_req[t]
- * or -1 when id < 0, when is_valid (nullable uint8 [n_tok]) is 0 for t, or on a
- * fault (req outside [0, n_req), page index >= max_pages).  lens (nullable
- * int32 [n_tok]) = number of slots >= 0 in the row.
+ * (formed in 64 bits) or -1 when id < 0, when is_valid (nullable uint8
+ * [n_tok]) is 0 for t, or on a fault: req outside [0, n_req) (one fault per
+ * token), a page index >= max_pages, a negative page entry, or a slot past
+ * 2^31 - 1 (one fault per entry).  lens (nullable int32 [n_tok]) = number of
+ * slots >= 0 in the row.
  *   topk int32 [n_tok, k]; token_to_req int32 [n_tok];
  *   page_table int32 [n_req, max_pages]; slots int32 [n_tok, k];
  *   0 <= k <= 65536, page_bits 0..16.
@@ -280,6 +282,10 @@ int dsv4kv_topk_to_slots(const int *topk, int n_tok, int k,
  * `polls` polls (1..2^24) and a second warp must see its abort flag and give
  * up too.  Expected result: *err_word += DSV4KV_FAULT_TIMEOUT and
  * *gave_up += 2 (both device int32, caller-zeroed).
+ * After any call reports DSV4KV_FAULT_TIMEOUT, everything that launch wrote
+ * (pool rows, gathered rows, ring entries, lens) is undefined, rows of other
+ * CTAs included: a copy still in flight when a CTA gave up may land in shared
+ * memory that a later CTA uses.
  */
 #define DSV4KV_FAULT_TIMEOUT (1 << 24)
 int dsv4kv_selftest_bounded_wait(int polls, int *err_word, int *gave_up, void *stream);
@@ -336,14 +342,27 @@ int dsv4kv_fake_quant(int layout, const void *in_bf16, long long n, long long in
 typedef struct dsv4kv_kvbuf {
     void *storage;
     long long capacity_rows;
+    /* the head: the source the storage holds, compared field by field */
     int head_valid;
     int head_layout;
     const void *head_pool;
     long long head_pool_rows;
-    const int *head_ids;
-    long long head_n;
-    unsigned long long head_map;   /* top-k form: fingerprint of the id mapping; 0 for ids */
+    const int *head_ids;               /* ids, top-k ids, or short-context lengths */
+    long long head_n;                  /* rows gathered */
+    int head_form;                     /* DSV4KV_KVBUF_IDS / _TOPK / _ALL */
+    int head_k;                        /* top-k and short-context forms: ids per token */
+    const int *head_token_to_req;      /* the id mapping (0 / NULL for the ids form) */
+    const unsigned char *head_is_valid;
+    const int *head_page_table;
+    int head_n_req;
+    int head_max_pages;
+    int head_page_bits;
 } dsv4kv_kvbuf;
+
+/* head_form values: which gather filled the storage */
+#define DSV4KV_KVBUF_IDS 0             /* dsv4kv_dequant_gather (pool slots) */
+#define DSV4KV_KVBUF_TOPK 1            /* dsv4kv_dequant_gather_topk */
+#define DSV4KV_KVBUF_ALL 2             /* dsv4kv_dequant_gather_all */
 
 /* (Re)initialise: set storage and capacity, forget the head.  Host only. */
 int dsv4kv_kvbuf_init(dsv4kv_kvbuf *buf, void *storage_bf16, long long capacity_rows);
@@ -369,12 +388,12 @@ int dsv4kv_kvbuf_get_with_head(dsv4kv_kvbuf *buf, int layout, const void *pool,
                                void **rows, int *hit, int *err_word, void *stream);
 
 /* get_with_head whose gather ids are request-local top-k ids: the head is
- * (layout, pool, pool_rows, topk pointer, n_tok * k) plus a fingerprint of
- * the mapping arguments (token_to_req, is_valid and page_table pointers,
- * n_req, max_pages, page_bits, k), so the same top-k buffer mapped through
- * another table is a miss; on a miss runs dsv4kv_dequant_gather_topk into
- * the storage (lens as there, written only on a miss), on a hit launches
- * nothing. */
+ * (layout, pool, pool_rows, topk pointer, n_tok * k) and every mapping
+ * argument (the token_to_req, is_valid and page_table pointers, n_req,
+ * max_pages, page_bits, k), compared exactly, so the same top-k buffer
+ * mapped through another table is a miss; on a miss runs
+ * dsv4kv_dequant_gather_topk into the storage (lens as there, written only
+ * on a miss), on a hit launches nothing. */
 int dsv4kv_kvbuf_get_with_head_topk(dsv4kv_kvbuf *buf, int layout, const void *pool,
                                     long long pool_rows, const int *topk, int n_tok, int k,
                                     const int *token_to_req, const unsigned char *is_valid,
@@ -382,9 +401,10 @@ int dsv4kv_kvbuf_get_with_head_topk(dsv4kv_kvbuf *buf, int layout, const void *p
                                     void **rows, int *lens, int *hit, int *err_word, void *stream);
 
 /* get_with_head whose ids are the short-context ids (dsv4kv_dequant_gather_all):
- * the head is (layout, pool, pool_rows, lens_in pointer, n_tok * k) plus the
- * mapping fingerprint; a miss runs dsv4kv_dequant_gather_all into the
- * storage, a hit launches nothing. */
+ * the head is (layout, pool, pool_rows, lens_in pointer, n_tok * k) and the
+ * mapping arguments as for the top-k form, with its own head_form, so a
+ * top-k fill never hits for it; a miss runs dsv4kv_dequant_gather_all into
+ * the storage, a hit launches nothing. */
 int dsv4kv_kvbuf_get_with_head_all(dsv4kv_kvbuf *buf, int layout, const void *pool,
                                    long long pool_rows, const int *lens_in, int n_tok, int k,
                                    const int *token_to_req, const unsigned char *is_valid,

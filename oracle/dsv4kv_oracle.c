@@ -579,6 +579,9 @@ int64_t orc_dequant_gather(int layout, const uint8_t *pool, int64_t pool_rows,
 /* ids (< 0 = empty).  slot = page_table[req][id >> page_bits] << page_bits   */
 /* | (id & mask), or -1 for an empty entry, a page index past max_pages, or  */
 /* an invalid token.  lens[t] = number of slots >= 0 in row t.               */
+/* The slot is formed in 64-bit arithmetic.  A page entry < 0, or a slot     */
+/* that int32 cannot hold, is not a page the pool has: slot -1 and one fault */
+/* (the pages give physical page numbers only as non-negative int32 slots).  */
 /* ------------------------------------------------------------------------ */
 int64_t orc_topk_to_slots(const int32_t *topk, int64_t n_tok, int k,
                           const int32_t *token_to_req, const uint8_t *is_valid,
@@ -596,11 +599,17 @@ int64_t orc_topk_to_slots(const int32_t *topk, int64_t n_tok, int k,
             int32_t s = -1;
             if (valid && id >= 0) {
                 int64_t lp = (int64_t)id >> page_bits;
-                if (lp < max_pages)
-                    s = (int32_t)(((int64_t)page_table[(int64_t)r * max_pages + lp] << page_bits)
-                                  | (id & ((1 << page_bits) - 1)));
-                else
+                if (lp < max_pages) {
+                    int64_t phys = page_table[(int64_t)r * max_pages + lp];
+                    int64_t slot = phys * ((int64_t)1 << page_bits)
+                                   + (id & ((1 << page_bits) - 1));
+                    if (phys < 0 || slot > INT32_MAX)
+                        ++faults;
+                    else
+                        s = (int32_t)slot;
+                } else {
                     ++faults;
+                }
             }
             slots[t * k + c] = s;
             if (s >= 0) ++cnt;

@@ -197,6 +197,22 @@ def test_topk_reuse_head_covers_the_id_mapping(B):
     assert call(a5=7) == 0                                   # other k (n_tok * k still 0)
     L.dsv4kv_kvbuf_begin_forward(ctypes.byref(buf))
     assert call() == 0 and call() == 1
+    # every field of the head alone: a change is a miss, the same again a hit
+    for field, value in (("a0", 2), ("a1", FAKE + 64), ("a2", 999), ("a3", FAKE + 128),
+                         ("a5", 4), ("a6", FAKE + 4096), ("a7", FAKE + 8192),
+                         ("a8", FAKE + 2048), ("a9", 5), ("a10", 17), ("a11", 7)):
+        assert call() in (0, 1)
+        assert call() == 1
+        assert call(**{field: value}) == 0, field
+        assert call(**{field: value}) == 1, field
+        assert call() == 0, field
+    # the head is kept exactly as given (struct layout shared with C)
+    call(a9=3, a10=12, a11=4)
+    assert (buf.head_valid, buf.head_form, buf.head_layout, buf.head_k, buf.head_n_req,
+            buf.head_max_pages, buf.head_page_bits) == (1, 1, 1, 8, 3, 12, 4)
+    assert (buf.head_pool, buf.head_pool_rows, buf.head_ids, buf.head_token_to_req,
+            buf.head_page_table, buf.head_is_valid) == (FAKE, 1000, FAKE + 256, FAKE + 512,
+                                                        FAKE + 1024, None)
 
 
 def test_short_context_calls_reject_bad_arguments(B):

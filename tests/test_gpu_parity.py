@@ -452,6 +452,39 @@ def test_fused_topk_gather_matches_oracle_composition(B, layout, n_tok, k):
     assert int(err.item()) == f1 + f2 and f1 > 0 and f2 > 0
 
 
+@pytest.mark.parametrize("layout", [oracle.V41, oracle.V41_FP4, oracle.V4])
+def test_page_entries_that_are_no_page_fault_and_give_zero_rows(B, layout):
+    """A negative page-table entry, one whose slot would wrap a 32-bit shift
+    back into the pool (2^26 pages of 64 rows), and one whose slot fits int32
+    but lies past the pool: the standalone mapping and the fused gather both
+    give slot -1 / a zero row and count one fault per entry, as the oracle
+    does (64-bit slots, no wrap)."""
+    cfg = dict(W.cfg2_ratio2_small(), layout=layout)
+    pool = gpu_store(B, cfg)["pool"]
+    pt = cfg["page_table"].copy()
+    pt[0, 0] = -5
+    pt[1, 0] = (1 << 26) + 2            # (2^26 + 2) << 6 wraps to slot 128 in 32 bits
+    pt[2, 0] = (1 << 24)                # slot 2^30: fits int32, past the 65-page pool
+    topk = np.tile(np.array([[3, 9, 40, 63, -1, 70]], np.int32), (6, 1))
+    ttr = np.array([0, 1, 2, 3, 0, 1], np.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots, lens = B.dsv4kv_topk_to_slots(dev(topk), dev(ttr), dev(pt), 6, err_word=err)
+    ws, wl, f1 = oracle.topk_to_slots(topk, ttr, pt, 6)
+    assert np.array_equal(slots.cpu().numpy(), ws)
+    assert np.array_equal(lens.cpu().numpy(), wl)
+    assert int(err.item()) == f1 and f1 == 16          # 4 ids x 4 tokens on entries 0 and 1
+    assert (ws[[0, 1, 4, 5], :4] == -1).all() and (ws[2, :4] >= 1 << 30).all()
+    err.zero_()
+    lens = torch.zeros(6, dtype=torch.int32, device="cuda")
+    out = B.dsv4kv_dequant_gather_topk(layout, dev(pool), dev(topk), dev(ttr), dev(pt), 6,
+                                       lens=lens, err_word=err)
+    want, f2 = oracle.dequant_gather(layout, pool, cfg["pool_rows"], ws.reshape(-1))
+    assert_bf16_equal_nan_aware(host_u16(out), want)
+    assert np.array_equal(lens.cpu().numpy(), wl)
+    assert int(err.item()) == f1 + f2 and f2 == 4      # token 2's slots lie past the pool
+    assert not host_u16(out).reshape(6, 6, 512)[[0, 1, 2, 4, 5], :4].any()
+
+
 def test_fused_topk_reuse_buffer(B):
     cfg = W.cfg2_ratio2_small()
     pool = dev(gpu_store(B, cfg)["pool"])

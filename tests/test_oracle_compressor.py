@@ -212,6 +212,19 @@ def test_topk_to_slots_oracle():
     assert lens.tolist() == [4, 0] and (slots[1] == -1).all()
 
 
+def test_topk_to_slots_oracle_page_entries_past_int32():
+    """Page entries are non-negative page numbers whose slots fit int32: a
+    negative entry, or one whose slot is 2^31 or more, maps to -1 with one
+    fault (no 32-bit wrap to a small, in-range slot); the largest entry that
+    still fits maps exactly.  Worked by hand with 64 rows per page."""
+    big = 1 << 25                                  # slot 2^31 + id offset: past int32
+    pt = np.array([[3, -3, big, big - 1]], np.int32)
+    topk = np.array([[5, 64 + 5, 128 + 5, 192 + 5, 192 + 63]], np.int32)
+    slots, lens, faults = oracle.topk_to_slots(topk, np.array([0], np.int32), pt, 6)
+    assert slots[0].tolist() == [197, -1, -1, 2147483589, 2147483647]
+    assert lens.tolist() == [3] and faults == 2
+
+
 def test_fill_all_indices_oracle():
     """Short-context ids, worked by hand: each row counts up to its token's
     visible length and pads with -1; through topk_to_slots they select every
