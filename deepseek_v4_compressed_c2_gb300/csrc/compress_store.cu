@@ -373,18 +373,33 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
 #pragma unroll
   for (int q = 0; q < 8; ++q) x2[q] = f2_from_bf16x2(word_of(in.kv0[q >> 2], q & 3));
   if constexpr (RATIO == 2) {
-    // softmax over the pair: weight of the first = 1 / (1 + exp(s1 - s0));
-    // x = k1 + (k0 - k1) * w0 (an ex2 overflow gives w0 = 0, i.e. x = k1)
+    // softmax over the pair, anchored on the member with the larger score:
+    // with t = (s1 - s0) log2(e), the other member's weight is
+    // w = 1 / (1 + 2^|t|) <= 1/2 and x = anchor + (other - anchor) * w.
+    // The approximate exp / reciprocal then only perturb the small
+    // correction term, so a saturated pair (w below the anchor's half ulp)
+    // pools to the anchor exactly, as in exact arithmetic (an ex2 overflow
+    // gives w = 0).  The sign of t picks the anchor (negative: k0) and the
+    // sign of the weight together: x = anchor + (k0 - k1) * (+-w).
     const uint64_t log2e = f2(1.4426950408889634f, 1.4426950408889634f), one = f2(1.f, 1.f);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const uint64_t k1 = f2_from_bf16x2(word_of(in.kv1[q >> 2], q & 3));
       const uint64_t a = f2_from_bf16x2(word_of(in.s0[q >> 2], q & 3));
       const uint64_t b = f2_from_bf16x2(word_of(in.s1[q >> 2], q & 3));
-      float t0, t1, d0, d1;
+      float t0, t1, d0, d1, ka0, ka1, kb0, kb1;
       f2_split(f2_mul(f2_sub(b, a), log2e), t0, t1);
-      f2_split(f2_add(f2(ex2_approx(t0), ex2_approx(t1)), one), d0, d1);
-      x2[q] = f2_fma(f2_sub(x2[q], k1), f2(rcp_approx(d0), rcp_approx(d1)), k1);
+      f2_split(f2_add(f2(ex2_approx(fabsf(t0)), ex2_approx(fabsf(t1))), one), d0, d1);
+      f2_split(x2[q], ka0, ka1);
+      f2_split(k1, kb0, kb1);
+      const uint32_t u0 = __float_as_uint(t0), u1 = __float_as_uint(t1);
+      const uint32_t m0 = (uint32_t)((int32_t)u0 >> 31), m1 = (uint32_t)((int32_t)u1 >> 31);
+      const uint64_t anchor =
+          f2(__uint_as_float((__float_as_uint(ka0) & m0) | (__float_as_uint(kb0) & ~m0)),
+             __uint_as_float((__float_as_uint(ka1) & m1) | (__float_as_uint(kb1) & ~m1)));
+      const uint64_t w = f2(__uint_as_float(__float_as_uint(rcp_approx(d0)) ^ (u0 & 0x80000000u)),
+                            __uint_as_float(__float_as_uint(rcp_approx(d1)) ^ (u1 & 0x80000000u)));
+      x2[q] = f2_fma(f2_sub(x2[q], k1), w, anchor);
     }
   }
   // RMSNorm: x_n = (x * w) * inv with inv = rsqrt(mean(x^2) + eps).  The
@@ -852,16 +867,18 @@ static cudaError_t launch_variant(const StoreParams& p, cudaStream_t stream) {
   auto kern = compress_store_kernel<L, RATIO, NORM, ROPE, RING, SHAPE>;
   const size_t smem = (size_t)TL::kFixedSmem + sizeof(long long) * (size_t)((p.n_slots + 2) & ~1)
                     + 3 * sizeof(int) * (size_t)p.n_slots;
-  static int attr_set_for_device[64] = {0};  // the largest size any call can need, once per device
+  // the largest size any call can need, set once per device; the flag is
+  // published (release) only after the attribute call succeeded
+  static std::atomic<int> attr_set_for_device[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !attr_set_for_device[dev]) {
+  if (dev >= 64 || !attr_set_for_device[dev].load(std::memory_order_acquire)) {
     const size_t max_smem = (size_t)TL::kFixedSmem + sizeof(long long) * ((kMaxSlots + 2) & ~1)
                           + 3 * sizeof(int) * kMaxSlots;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
     if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set_for_device[dev] = 1;
+    if (dev < 64) attr_set_for_device[dev].store(1, std::memory_order_release);
   }
   // resident CTAs per SM at this shared-memory size, cached per device as
   // (smem << 8 | per_sm): the query costs more host time than the launch
