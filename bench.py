@@ -7,10 +7,24 @@ One step = one long-prefill batch through the whole path:
   2. the sparse-prefill read of each request's top-2048 compressed ids: 4
      layers share the source; the first get_with_head_topk runs the fused
      top-k -> slot -> gather-dequant kernel, the other three are reuse hits.
-value = (rows stored + rows gathered) / step time, inputs resident in HBM.
-e2e   = the same through host buffers: pinned host -> device copy of the
-        step's inputs and device -> host copy of the gathered rows inside the
-        timed region (request chunks, copies overlapped with the kernels).
+value = (rows stored + real rows gathered) / step time, inputs resident in
+        HBM; the top-k list's -1 padding (requests with fewer than 2048
+        compressed rows) yields zero rows that are not counted.
+e2e   = the same step through host buffers: pinned host -> device copy of
+        the step's inputs and device -> host copy of the gathered rows inside
+        the timed region (request chunks, copies overlapped with the kernels,
+        the same store + 1 dequant + 3 reuse hits per chunk).
+
+Besides the headline line's timed region, the run measures (each reported
+in the same JSON line): the store and the gather of the step one launch at
+a time (medians of >= 50 event pairs, the roofline's durations); each of
+the five workloads on its own (`configs`: µs and rows/s, L2 flushed before
+each launch, and warm where the working set fits in L2; the 1 Mi-row
+gather as 4 dequant launches against 1 dequant + 3 reuse hits); the other
+layouts' store-only, gather and fake-quantization launches (`cold_l2`); the
+decode / verify ring steps; the CPU oracle per workload on one core and on
+all cores (`cpu_baseline`, `oracle_per_config`).  nvidia-smi clocks are
+sampled across the whole run.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own batch (weak scaling, no collective on
@@ -24,6 +38,7 @@ import subprocess
 import sys
 import threading
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -33,12 +48,13 @@ if ROOT not in sys.path:
 
 METRIC = "compressed-KV rows/s (store, gather-dequant) and achieved HBM GB/s vs 8 TB/s"
 LAYERS = 4
-EVENT_EVERY = 10     # steps between per-kernel event samples in the timed region
+KERNEL_SAMPLES = 100   # launches of the store / gather timed one by one (median)
+CONFIG_REPS = 50       # timed launches per workload leg (median), after 5 warm-ups
 E2E_CHUNKS = 8
 # algorithmic bytes per unit (what the method must move)
 STORE_BYTES_PER_ROW = 2 * (1024 + 1024) + 256 + 528   # 2 x (kv + score) bf16, RoPE row, V41 row
 GATHER_BYTES_PER_ROW = 528 + 4 + 1024                  # V41 row + id, bf16 row out
-
+PAD_BYTES_PER_ROW = 4 + 1024                           # a -1 id: read the id, write a zero row
 
 _CSRC = os.path.join("deepseek_v4_compressed_c2_gb300", "csrc")
 STORE_SOURCES = [os.path.join(_CSRC, f) for f in
@@ -77,63 +93,76 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """nvidia-smi clocks and throttle reasons, one query every ~`period` s on
+    a host thread for the whole run (a one-shot query per sample, so nothing
+    is lost to output buffering).  `busy(name)` brackets GPU work: the
+    reported median SM clock is taken over samples inside those windows."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.idx = gpu_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, gpu_index, period=0.02):
+        self.idx, self.period = gpu_index, period
+        self.samples = []           # (t_mid, sm, max, reasons)
+        self.windows = []           # (name, t0, t1)
+        self._stop = threading.Event()
+        self._t = None
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
-        except Exception:
-            self.proc = None
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def _run(self):
+        cmd = ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+               "--format=csv,noheader,nounits"]
+        while not self._stop.is_set():
+            t0 = time.monotonic()
+            try:
+                out = subprocess.run(cmd, capture_output=True, text=True, timeout=5).stdout
+            except Exception:
+                return
+            t1 = time.monotonic()
+            parts = [p.strip() for p in out.strip().split(",")]
+            if len(parts) >= 7:
+                try:
+                    sm, mx = float(parts[0]), float(parts[1])
+                    reasons = {n for n, v in zip(self.NAMES, parts[3:7]) if v.lower() == "active"}
+                    self.samples.append(((t0 + t1) / 2, sm, mx, reasons))
+                except ValueError:
+                    pass
+            self._stop.wait(self.period)
+
+    class _Window:
+        def __init__(self, s, name):
+            self.s, self.name = s, name
+
+        def __enter__(self):
+            self.t0 = time.monotonic()
+
+        def __exit__(self, *exc):
+            self.s.windows.append((self.name, self.t0, time.monotonic()))
+
+    def busy(self, name):
+        return ClockSampler._Window(self, name)
 
     def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.t.join(timeout=2)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        self._stop.set()
+        if self._t is not None:
+            self._t.join(timeout=10)
+        inside = [s for s in self.samples if any(t0 <= s[0] <= t1 for _, t0, t1 in self.windows)]
+        use = inside or self.samples
+        if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
-
-
-def make_inputs(seed=7):
-    from deepseek_v4_compressed_c2_gb300 import workloads as W
-    return W.cfg5_long_prefill(seed=seed)
+        reasons = set()
+        for s in use:
+            reasons |= s[3]
+        return {"sm_mhz": statistics.median(s[1] for s in use),
+                "sm_max_mhz": max(s[2] for s in use), "reasons": sorted(reasons),
+                "samples": len(self.samples), "samples_during_gpu_work": len(inside),
+                "sm_mhz_min_during_gpu_work": min(s[1] for s in use),
+                "gpu_work_windows": [n for n, _, _ in self.windows],
+                "period_s": self.period}
 
 
 def max_over_ranks(values, world, device="cpu"):
@@ -153,167 +182,449 @@ def whole_job_rate(units_per_rank, world, slowest_ms):
     return units_per_rank * world / (slowest_ms / 1e3)
 
 
-def _oracle_sample(cfg, m):
-    """The oracle as it stands, single-threaded: the batch's first m
-    compressed rows (ratio-2 compress, RMSNorm, RoPE, V41 store) and m
-    gathered rows.  Returns seconds."""
-    import oracle
-    n = cfg["n_out"]
-    pool = np.zeros(cfg["pool_rows"] * 528, np.uint8)
-    which = np.arange(m, dtype=np.int64)
+def make_inputs(seed=7):
+    from deepseek_v4_compressed_c2_gb300 import workloads as W
+    return W.cfg5_long_prefill(seed=seed)
+
+
+def gather_rows_valid(cfg):
+    """real rows of the step's gather: the top-k ids >= 0"""
+    return int((cfg["topk"] >= 0).sum())
+
+
+def headline_config(cfg, world):
+    """The `config` both arms print for the long-prefill step."""
+    n_tok, k = cfg["topk"].shape
+    return {"workload": cfg["name"], "requests": len(cfg["lengths"]),
+            "tokens": int(sum(cfg["lengths"])), "store_rows": int(cfg["n_out"]),
+            "gather_rows_valid": gather_rows_valid(cfg), "gather_id_slots": int(n_tok * k),
+            "layers_reading_source": LAYERS, "layout": "V41", "ratio": 2, "page_size": 64,
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (fused rows %d MB per step)"
+                  % (cfg["rows"].nbytes // 10 ** 6)}
+
+
+# ------------------------------------------------------------------ oracle
+def cpu_info():
+    """(cores this process may run on, CPU model string)"""
+    cores = len(os.sched_getaffinity(0))
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu model")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return cores, model or "unknown"
+
+
+def _split(a, parts):
+    return [c for c in np.array_split(a, parts) if len(c)]
+
+
+def _run_parts(fn, chunks, threads):
+    """fn over the chunks, on `threads` host threads (the oracle's C calls
+    release the interpreter lock); returns wall seconds"""
     t0 = time.perf_counter()
-    oracle.compress_store(1, 2, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
-                          page_bits=cfg["page_bits"], norm_w=cfg["norm_w"], eps=cfg["eps"],
-                          freqs=cfg["freqs"], n_out=n, which=which, pool=pool,
-                          pool_rows=cfg["pool_rows"], want_f64=False, want_f32=False,
-                          want_latent=False)
-    oracle.dequant_gather(1, pool, cfg["pool_rows"], np.arange(64, 64 + m, dtype=np.int32))
+    if threads <= 1:
+        for c in chunks:
+            fn(c)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(fn, chunks))
     return time.perf_counter() - t0
 
 
-def _sample_rows(cfg, budget_s):
-    """rows per oracle sample so that one sample takes about budget_s"""
-    probe = min(256, cfg["n_out"])
-    t = _oracle_sample(cfg, probe)
-    return int(min(cfg["n_out"], max(16, probe * budget_s / max(t, 1e-6))))
+class OracleStep:
+    """The oracle as it stands on a bounded sample of the long-prefill step:
+    the store of the batch's first m compressed rows (ratio-2 compress,
+    RMSNorm, RoPE, V41 quantize, paged store) and the gather of the same
+    fraction of the step's real top-k rows (the oracle's own slots), with the
+    rows split over `threads` host threads."""
+
+    def __init__(self, cfg):
+        import oracle
+        self.o, self.cfg = oracle, cfg
+        self.pool = np.zeros(cfg["pool_rows"] * 528, np.uint8)
+        slots, _, _ = oracle.topk_to_slots(cfg["topk"], cfg["token_to_req"], cfg["page_table"],
+                                           cfg["page_bits"])
+        self.slots = slots.reshape(-1)[slots.reshape(-1) >= 0].astype(np.int32)
+
+    def rows_for(self, m):
+        g = int(round(m * len(self.slots) / self.cfg["n_out"]))
+        return m, g
+
+    def run(self, m, threads):
+        cfg, o = self.cfg, self.o
+        m, g = self.rows_for(m)
+
+        def store(which):
+            o.compress_store(1, 2, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
+                             page_bits=cfg["page_bits"], norm_w=cfg["norm_w"], eps=cfg["eps"],
+                             freqs=cfg["freqs"], n_out=cfg["n_out"], which=which,
+                             pool=self.pool, pool_rows=cfg["pool_rows"], want_f64=False,
+                             want_f32=False, want_latent=False)
+
+        def gather(ids):
+            o.dequant_gather(1, self.pool, cfg["pool_rows"], ids)
+
+        t = _run_parts(store, _split(np.arange(m, dtype=np.int64), threads), threads)
+        t += _run_parts(gather, _split(self.slots[:g], threads), threads)
+        return m + g, t
+
+    def size_for(self, budget_s, threads):
+        """compressed rows per sample so that one sample takes ~budget_s"""
+        probe = min(512, self.cfg["n_out"])
+        units, t = self.run(probe, threads)
+        return int(min(self.cfg["n_out"], max(16, probe * budget_s / max(t, 1e-6))))
 
 
-def cpu_baseline(cfg, budget_s=10.0):
-    """The oracle timed on the host cores on a bounded sample (~budget_s) of
-    the same workload."""
-    m = _sample_rows(cfg, budget_s)
-    t = _oracle_sample(cfg, m)
-    return {"value": 2 * m / t, "unit": "rows/s", "cores": 1, "kind": "oracle",
+def cpu_baseline(cfg, budget_s=6.0):
+    """The oracle on the long-prefill step, timed on the host cores: one core
+    and all cores (threads over rows), each on a sample of ~budget_s."""
+    cores, model = cpu_info()
+    step = OracleStep(cfg)
+    res = {}
+    for threads in (1, cores):
+        m = step.size_for(budget_s, threads)
+        units, t = step.run(m, threads)
+        res[threads] = (units, t, m)
+    units, t, m = res[cores]
+    u1, t1, m1 = res[1]
+    return {"value": units / t, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "cpu_model": model,
             "sample": f"first {m} of {cfg['n_out']} compressed rows of the batch (ratio-2 "
-                      f"compress, RMSNorm, RoPE, V41 store) + {m} gathered rows, {t:.2f} s"}
+                      f"compress, RMSNorm, RoPE, V41 store) + the same fraction of the real "
+                      f"top-k rows gathered, rows split over {cores} threads, {t:.2f} s",
+            "single_thread": {"value": u1 / t1, "unit": "rows/s", "cores": 1,
+                              "sample": f"first {m1} compressed rows + the same fraction of "
+                                        f"the gathered rows, {t1:.2f} s"}}
+
+
+def oracle_per_config(cfgs, budget_s=2.0):
+    """The oracle on each workload, one core and then all cores (threads over
+    rows), the store and the gather / dequant timed apart: each on a bounded
+    sample (~budget_s on one core) of the workload's store rows and of its
+    ids (cfg1, cfg3: the written slots; cfg4: the 262,144 ids, whose rows the
+    oracle stores first, untimed; cfg2 has no read)."""
+    import oracle
+    cores, model = cpu_info()
+    out = {"cores": cores, "cpu_model": model}
+    for key, c in cfgs.items():
+        layout = c["layout"]
+        pool = np.zeros(c["pool_rows"] * oracle.row_bytes(layout), np.uint8)
+        p = oracle.plan(c["ratio"], c["ext"], c["page_table"], c["page_bits"])
+
+        def store(which, c=c, pool=pool, layout=layout):
+            oracle.compress_store(layout, c["ratio"], c["rows"], c["ext"],
+                                  page_table=c["page_table"], page_bits=c["page_bits"],
+                                  norm_w=c["norm_w"], eps=c["eps"], freqs=c["freqs"],
+                                  n_out=c["n_out"], which=which, pool=pool,
+                                  pool_rows=c["pool_rows"], want_f64=False, want_f32=False,
+                                  want_latent=False)
+
+        def gather(ids, c=c, pool=pool, layout=layout):
+            oracle.dequant_gather(layout, pool, c["pool_rows"], ids)
+
+        if "ids" in c:                       # gather only; its rows stored first, untimed
+            rows, ids = np.zeros(0, np.int64), np.asarray(c["ids"], np.int32)
+            _run_parts(store, _split(ids.astype(np.int64) - (1 << c["page_bits"]), cores), cores)
+        elif c["ratio"] == 1:                # store, then dequant of the written slots
+            rows, ids = np.arange(p["total"], dtype=np.int64), p["slot"][p["slot"] > 0].astype(np.int32)
+        else:                                # store only
+            rows, ids = np.arange(p["total"], dtype=np.int64), np.zeros(0, np.int32)
+        entry = {"name": c["name"]}
+        for part, fn, items, probe in (("store", store, rows, 256), ("gather", gather, ids, 4096)):
+            if not len(items):
+                continue
+            k0 = min(probe, len(items))
+            t = _run_parts(fn, [items[:k0]], 1)
+            n = int(min(len(items), max(k0, k0 * budget_s / max(t, 1e-6))))
+            d = {"sample_rows": n, "of_rows": int(len(items))}
+            for threads in (1, cores):
+                t = _run_parts(fn, _split(items[:n], threads), threads)
+                d["rows_per_s_1core" if threads == 1 else "rows_per_s_all_cores"] = n / t
+            entry[part] = d
+        out[key] = entry
+    return out
 
 
 def run_reference(args, rank):
-    """The reference arm: the CPU oracle, on rank 0 only, each step a bounded
-    sample sized so that warm-up + steps take about two minutes in all."""
+    """The reference arm: the CPU oracle on all host cores, on rank 0 only,
+    each step a bounded sample sized so that warm-up + steps take about two
+    minutes in all."""
     if rank != 0:
         return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     cfg = make_inputs()
+    cores, model = cpu_info()
+    step = OracleStep(cfg)
+    step.run(64, 1)                          # the oracle's tables, built on one thread
     per_step = max(0.005, 120.0 / (args.steps + args.warmup))
-    m = _sample_rows(cfg, per_step)
+    m = step.size_for(per_step, cores)
     for _ in range(args.warmup):
-        _oracle_sample(cfg, m)
-    secs = [_oracle_sample(cfg, m) for _ in range(args.steps)]
-    t = statistics.median(secs)
-    v = 2 * m / t
+        step.run(m, cores)
+    runs = [step.run(m, cores) for _ in range(args.steps)]
+    t = statistics.median(r[1] for r in runs)
+    v = runs[0][0] / t
     sample = (f"first {m} of {cfg['n_out']} compressed rows (ratio-2 compress, RMSNorm, RoPE, "
-              f"V41 store) + {m} gathered rows per step, median {t * 1e3:.1f} ms")
+              f"V41 store) + the same fraction of the real top-k rows gathered per step, rows "
+              f"split over {cores} threads, median {t * 1e3:.1f} ms")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "rows/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg["name"], "sample": sample},
-            "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "config": headline_config(cfg, world),
+            "cpu_baseline": {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                             "cpu_model": model, "sample": sample},
             "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def _timed(fn, flush, stream, reps, scrub=None):
-    """median CUDA-event time of fn() in ms, L2 flushed before each launch:
-    a write of `flush` (512 MB, 4x the L2); with `scrub`, then a read of it
-    (256 MB), which evicts the dirty lines of the write, so the timed kernel
-    starts from a cold L2 that holds neither its inputs nor lines still to be
-    written back"""
+# ------------------------------------------------------------------ GPU legs
+class Flusher:
+    """Before a timed launch: write `flush` (512 MB, 4x the L2), then read
+    `scrub` (256 MB), which evicts the write's dirty lines, so the launch
+    starts from an L2 that holds neither its inputs nor lines still to be
+    written back."""
+
+    def __init__(self, dev):
+        import torch
+        self.flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.scrub = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+        self.i = 0
+
+    def __call__(self, clean=True):
+        self.i += 1
+        self.flush.fill_(self.i & 0xFF)
+        if clean:
+            self.scrub.max()
+
+
+def _timed(fn, stream, reps, flusher=None, clean=True, warm=5):
+    """median and count of CUDA-event times (ms) of fn() on `stream`; with a
+    flusher the L2 is flushed before every launch, else the launches run back
+    to back (the working set stays wherever the previous launch left it)"""
     import torch
     times = []
     with torch.cuda.stream(stream):
-        for i in range(reps + 3):
-            flush.fill_(i & 0xFF)
-            if scrub is not None:
-                scrub.max()
+        for i in range(reps + warm):
+            if flusher is not None:
+                flusher(clean)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
             b.record(stream)
             times.append((a, b))
     torch.cuda.synchronize()
-    return statistics.median(a.elapsed_time(b) for a, b in times[3:])
+    return statistics.median(a.elapsed_time(b) for a, b in times[warm:])
 
 
-def cold_gather(B, dev, stream, reps):
-    """The store-only fill and the gather, each timed alone with a cold L2:
-    1,048,576-row pools (page 0 reserved) in the V41, V41_FP4 and V4 layouts,
-    filled by the ratio-1 store from bf16 N(0,1) latents (torch generator,
-    seed 4); 262,144 unique row ids (numpy seed 4); between launches a 512 MB
-    buffer written and a 256 MB one read (see _timed).  Also, per layout, the
-    fake quantization of the same 1,048,512 latent rows (bf16 in, bf16 out),
-    and on the V41 pool the short-context gather: 128 tokens of one request,
-    each selecting every compressed row it sees (lengths uniform in
-    [1, 2048], numpy seed 5)."""
+def _graph_us(fn, stream, reps=50):
+    """device time per launch (us) of fn() captured `reps` times in one CUDA
+    graph: median of 5 replays; the launch-bound legs' serving-loop figure"""
     import torch
-    pool_rows, n_ids = 1 << 20, 1 << 18
-    g = torch.Generator(device=dev)
-    g.manual_seed(4)
-    lat = torch.randn((pool_rows - 64, 512), generator=g, device=dev).to(torch.bfloat16)
-    ext = torch.tensor([[0], [pool_rows - 64]], dtype=torch.int32, device=dev)
-    pt = torch.arange(1, pool_rows // 64, dtype=torch.int32, device=dev).view(1, -1)
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            fn()
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            times.append((a, b))
+    torch.cuda.synchronize()
+    del g
+    return statistics.median(a.elapsed_time(b) for a, b in times[3:]) * 1e3 / reps
+
+
+def _leg(ms, units, bytes_per_unit=None, peak=None, **extra):
+    d = {"us": ms * 1e3, "rows": units, "rows_per_s": units / (ms / 1e3)}
+    if bytes_per_unit is not None:
+        gbs = bytes_per_unit * units / (ms / 1e3) / 1e9
+        d.update(gbs=gbs, bytes_per_row=bytes_per_unit)
+        if peak is not None:
+            d.update(frac=gbs / peak, frac_of_8000=gbs / 8000.0)
+    d.update(extra)
+    return d
+
+
+def config_legs(B, dev, stream, flusher, cfg4, peak):
+    """Each workload on its own, with the L2 flushed before every launch
+    ("cold"), and back to back ("warm") where the working set fits in L2."""
+    import torch
+    from deepseek_v4_compressed_c2_gb300 import workloads as W
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def t(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    rng = np.random.default_rng(4)
-    ids = torch.from_numpy((rng.choice(pool_rows - 64, n_ids, replace=False) + 64)
-                           .astype(np.int32)).to(dev)
-    out = torch.empty((n_ids, 512), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    scrub = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
-    peak, kind = _peaks()
     res = {}
-    fq_out = torch.empty((pool_rows - 64, 512), dtype=torch.bfloat16, device=dev)
+
+    def store_call(c, pool):
+        return B.prepare_compress_store(
+            c["layout"], c["ratio"], bf(c["rows"]), t(c["ext"]), pool, page_table=t(c["page_table"]),
+            page_bits=c["page_bits"], rmsnorm_w=None if c["norm_w"] is None else bf(c["norm_w"]),
+            eps=c["eps"], freqs_cis=t(c["freqs"]), n_out=c["n_out"], err_word=err, stream=stream)
+
+    # cfg1: V41 ratio-1 store of 256 rows, then dequant of the 256 slots
+    c1 = W.cfg1_v41_roundtrip()
+    pool = torch.zeros(c1["pool_rows"] * 528, dtype=torch.uint8, device=dev)
+    st = store_call(c1, pool)
+    ids = torch.arange(64, 64 + 256, dtype=torch.int32, device=dev)
+    out = torch.empty((256, 512), dtype=torch.bfloat16, device=dev)
+    ga = B.prepare_dequant_gather(1, pool, ids, out, err_word=err, stream=stream)
+    res["cfg1_" + c1["name"]] = {
+        "store_cold": _leg(_timed(st, stream, CONFIG_REPS, flusher), 256),
+        "store_warm": _leg(_timed(st, stream, CONFIG_REPS), 256),
+        "store_in_graph": _leg(_graph_us(st, stream) / 1e3, 256),
+        "dequant_cold": _leg(_timed(ga, stream, CONFIG_REPS, flusher), 256),
+        "dequant_warm": _leg(_timed(ga, stream, CONFIG_REPS), 256),
+        "dequant_in_graph": _leg(_graph_us(ga, stream) / 1e3, 256),
+        "note": "0.4 MB each way: launch-latency bound, no roofline claim; *_in_graph = "
+                "device time per launch inside a CUDA graph of 50 launches"}
+
+    # cfg2: ratio-2 V41 compressor, 4 requests (1809 rows of 2048 output rows)
+    c2 = W.cfg2_ratio2_small()
+    pool = torch.zeros(c2["pool_rows"] * 528, dtype=torch.uint8, device=dev)
+    st = store_call(c2, pool)
+    n2 = int(sum(n // 2 for n in c2["lengths"]))
+    res["cfg2_" + c2["name"]] = {
+        "store_cold": _leg(_timed(st, stream, CONFIG_REPS, flusher), n2, STORE_BYTES_PER_ROW),
+        "store_warm": _leg(_timed(st, stream, CONFIG_REPS), n2, STORE_BYTES_PER_ROW),
+        "store_in_graph": _leg(_graph_us(st, stream) / 1e3, n2, STORE_BYTES_PER_ROW),
+        "note": "8.8 MB of algorithmic bytes: L2-resident and launch-latency bound, "
+                "no roofline claim"}
+
+    # cfg3: FP4 ratio-1 store of 32768 rows, then the full dequant
+    c3 = W.cfg3_fp4_store()
+    pool = torch.zeros(c3["pool_rows"] * 288, dtype=torch.uint8, device=dev)
+    st = store_call(c3, pool)
+    ids = torch.arange(128, 128 + 32768, dtype=torch.int32, device=dev)
+    out = torch.empty((32768, 512), dtype=torch.bfloat16, device=dev)
+    ga = B.prepare_dequant_gather(2, pool, ids, out, err_word=err, stream=stream)
+    res["cfg3_" + c3["name"]] = {
+        "store_cold": _leg(_timed(st, stream, CONFIG_REPS, flusher), 32768, 1024 + 288, peak),
+        "store_warm": _leg(_timed(st, stream, CONFIG_REPS), 32768, 1024 + 288),
+        "dequant_cold": _leg(_timed(ga, stream, CONFIG_REPS, flusher), 32768, 288 + 4 + 1024, peak),
+        "dequant_warm": _leg(_timed(ga, stream, CONFIG_REPS), 32768, 288 + 4 + 1024),
+        "note": "43 MB each way: fits in L2, so warm launches read L2"}
+
+    # cfg4: 1 Mi-row V41 pool, 262,144 ids, read by 4 layers
+    pool = torch.zeros(cfg4["pool_rows"] * 528, dtype=torch.uint8, device=dev)
+    rows4 = bf(cfg4["rows"])
+    fill = B.prepare_compress_store(1, 1, rows4, t(cfg4["ext"]), pool,
+                                    page_table=t(cfg4["page_table"]), page_bits=cfg4["page_bits"],
+                                    n_out=cfg4["n_out"], err_word=err, stream=stream)
+    ms_fill = _timed(fill, stream, max(5, CONFIG_REPS // 5), flusher)
+    ids = t(cfg4["ids"])
+    n_ids = ids.numel()
+    kv = B.SparsePrefillKVBuffer(torch.empty((n_ids, 512), dtype=torch.bfloat16, device=dev))
+    ga = B.prepare_dequant_gather(1, pool, ids, kv.storage, err_word=err, stream=stream)
+    gwh = B.prepare_get_with_head(kv, 1, pool, ids, err_word=err, stream=stream)
+    ms_one = _timed(ga, stream, CONFIG_REPS, flusher)
+
+    def no_reuse():
+        for _ in range(LAYERS):
+            ga()
+
+    hits = []
+
+    def with_reuse():
+        kv.dsv4kv_kvbuf_begin_forward()
+        hits[:] = [gwh() for _ in range(LAYERS)]
+
+    ms_4 = _timed(no_reuse, stream, CONFIG_REPS, flusher)
+    ms_r = _timed(with_reuse, stream, CONFIG_REPS, flusher)
+    assert hits == [False] + [True] * (LAYERS - 1)
+    res["cfg4_" + cfg4["name"]] = {
+        "store_fill_cold": _leg(ms_fill, cfg4["n_out"], 1024 + 528, peak),
+        "gather_cold": _leg(ms_one, n_ids, GATHER_BYTES_PER_ROW, peak),
+        "four_layers_without_reuse": {"us": ms_4 * 1e3, "dequant_launches": LAYERS,
+                                      "rows_per_s": LAYERS * n_ids / (ms_4 / 1e3)},
+        "four_layers_with_reuse": {"us": ms_r * 1e3, "dequant_launches": 1, "reuse_hits": 3,
+                                   "rows_per_s": LAYERS * n_ids / (ms_r / 1e3)},
+        "reuse_speedup": ms_4 / ms_r,
+        "note": "L2 flushed before each timed group; rows_per_s of the 4-layer legs counts "
+                "the rows every layer reads"}
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return res, pool, rows4, ids
+
+
+def cold_paths(B, dev, stream, flusher, cfg4, rows4, ids, peak):
+    """The other layouts on the 1 Mi-row workload, each launch timed alone
+    with a cold L2: the ratio-1 store-only fill (1,048,512 rows of the same
+    bf16 latents) and the gather of the same 262,144 ids in the V41_FP4 and
+    V4 layouts; the fake quantization of the latents in every layout; on the
+    V41 pool the short-context gather (128 tokens of one request, lengths
+    uniform in [1, 2048], numpy seed 5) and the gather after a write-only
+    flush (dirty L2)."""
+    import torch
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ext = torch.from_numpy(cfg4["ext"]).to(dev)
+    pt = torch.from_numpy(cfg4["page_table"]).to(dev)
+    n_rows, n_ids = cfg4["n_out"], ids.numel()
+    out = torch.empty((n_ids, 512), dtype=torch.bfloat16, device=dev)
+    fq_out = torch.empty((n_rows, 512), dtype=torch.bfloat16, device=dev)
+    res = {}
     for layout, name, rb in ((1, "v41", 528), (2, "fp4", 288), (0, "v4", 584)):
-        pool = torch.zeros(pool_rows * rb, dtype=torch.uint8, device=dev)
-        store = B.prepare_compress_store(layout, 1, lat, ext, pool, page_table=pt, page_bits=6,
-                                         n_out=pool_rows - 64, err_word=err, stream=stream)
+        pool = torch.zeros(cfg4["pool_rows"] * rb, dtype=torch.uint8, device=dev)
+        store = B.prepare_compress_store(layout, 1, rows4, ext, pool, page_table=pt,
+                                         page_bits=cfg4["page_bits"], n_out=n_rows, err_word=err,
+                                         stream=stream)
         gather = B.prepare_dequant_gather(layout, pool, ids, out, err_word=err, stream=stream)
-        ms_s = _timed(store, flush, stream, max(3, reps // 5), scrub)
-        ms_g = _timed(gather, flush, stream, reps, scrub)
-        assert int(err.item()) == 0
-        sb, gb = 1024 + rb, rb + 4 + 1024
-        res[f"store_ratio1_{name}_1048512rows"] = {
-            "ms": ms_s, "rows_per_s": (pool_rows - 64) / (ms_s / 1e3),
-            "gbs": sb * (pool_rows - 64) / (ms_s / 1e3) / 1e9,
-            "frac": sb * (pool_rows - 64) / (ms_s / 1e3) / 1e9 / peak, "bytes_per_row": sb}
-        res[f"gather_{name}_262144_of_1048576"] = {
-            "ms": ms_g, "rows_per_s": n_ids / (ms_g / 1e3), "gbs": gb * n_ids / (ms_g / 1e3) / 1e9,
-            "frac": gb * n_ids / (ms_g / 1e3) / 1e9 / peak, "frac_of_8000": gb * n_ids / (ms_g / 1e3) / 8e12,
-            "bytes_per_row": gb}
-        ms_f = _timed(lambda: B.dsv4kv_fake_quant(layout, lat, fq_out, stream=stream), flush,
-                      stream, max(3, reps // 5), scrub)
-        res[f"fake_quant_{name}_1048512rows"] = {
-            "ms": ms_f, "rows_per_s": (pool_rows - 64) / (ms_f / 1e3),
-            "gbs": 2048 * (pool_rows - 64) / (ms_f / 1e3) / 1e9,
-            "frac": 2048 * (pool_rows - 64) / (ms_f / 1e3) / 1e9 / peak, "bytes_per_row": 2048}
+        ms_s = _timed(store, stream, max(5, CONFIG_REPS // 5), flusher)
+        ms_g = _timed(gather, stream, CONFIG_REPS, flusher)
+        res[f"store_ratio1_{name}_{n_rows}rows"] = _leg(ms_s, n_rows, 1024 + rb, peak)
+        res[f"gather_{name}_{n_ids}_of_{cfg4['pool_rows']}"] = _leg(ms_g, n_ids, rb + 4 + 1024, peak)
+        ms_f = _timed(lambda: B.dsv4kv_fake_quant(layout, rows4, fq_out, stream=stream), stream,
+                      max(5, CONFIG_REPS // 5), flusher)
+        res[f"fake_quant_{name}_{n_rows}rows"] = _leg(ms_f, n_rows, 2048, peak)
         if layout == 1:
             n_tok, k = 128, 2048
             lens_in = torch.from_numpy(np.random.default_rng(5).integers(1, k + 1, n_tok)
                                        .astype(np.int32)).to(dev)
             ttr = torch.zeros(n_tok, dtype=torch.int32, device=dev)
-            ms_a = _timed(lambda: B.dsv4kv_dequant_gather_all(1, pool, lens_in, k, ttr, pt, 6,
-                                                              out[:n_tok * k], err_word=err,
-                                                              stream=stream),
-                          flush, stream, reps, scrub)
-            n_rows = int(lens_in.sum().item())
-            # the same gather after the write-only flush: it also pays the
-            # write-back of the flush's dirty lines
-            ms_gd = _timed(gather, flush, stream, reps)
-            res["gather_v41_262144_of_1048576_dirty_l2"] = {
-                "ms": ms_gd, "gbs": 1556 * n_ids / (ms_gd / 1e3) / 1e9,
-                "frac": 1556 * n_ids / (ms_gd / 1e3) / 1e9 / peak,
-                "note": "L2 flushed by the 512 MB write alone; ~129 MB of its dirty lines are "
-                        "written back during the gather"}
-            res["gather_all_v41_128tok_2048"] = {
-                "ms": ms_a, "rows": n_tok * k, "selected_rows": n_rows,
-                "rows_per_s": n_tok * k / (ms_a / 1e3),
-                "out_gbs": 1024 * n_tok * k / (ms_a / 1e3) / 1e9,
-                "note": "every token of one request re-reads the same <= 2048 compressed rows "
-                        "(L2-resident after the first); bound by the 1 KB/row output"}
+            ms_a = _timed(lambda: B.dsv4kv_dequant_gather_all(1, pool, lens_in, k, ttr, pt,
+                                                              cfg4["page_bits"], out[:n_tok * k],
+                                                              err_word=err, stream=stream),
+                          stream, CONFIG_REPS, flusher)
+            ms_gd = _timed(gather, stream, CONFIG_REPS, flusher, clean=False)
+            res[f"gather_v41_{n_ids}_of_{cfg4['pool_rows']}_dirty_l2"] = _leg(
+                ms_gd, n_ids, GATHER_BYTES_PER_ROW, peak,
+                note="L2 flushed by the 512 MB write alone; ~129 MB of its dirty lines are "
+                     "written back during the gather")
+            res["gather_all_v41_128tok_2048"] = _leg(
+                ms_a, n_tok * k, None, None, selected_rows=int(lens_in.sum().item()),
+                out_gbs=1024 * n_tok * k / (ms_a / 1e3) / 1e9,
+                note="every token of one request re-reads the same <= 2048 compressed rows "
+                     "(L2-resident after the first); bound by the 1 KB/row output")
+        torch.cuda.synchronize()
         assert int(err.item()) == 0
         del pool
-    res["peak_kind"] = kind
+    res["peak_kind"] = _peaks()[1]
     return res
 
 
@@ -357,17 +668,22 @@ def decode_verify_steps(B, dev, stream, reps=50, max_prefix=4096):
         with torch.cuda.graph(graph, stream=stream):
             for _ in range(reps):
                 call()
+        graph_us = []
         with torch.cuda.stream(stream):
             for _ in range(3):
                 graph.replay()
-            a.record(stream)
-            graph.replay()
-            b.record(stream)
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+                graph_us.append((a, b))
         torch.cuda.synchronize(dev)
         assert int(err.item()) == 0
-        us = a.elapsed_time(b) * 1e3 / reps
+        us = statistics.median(a.elapsed_time(b) for a, b in graph_us) * 1e3 / reps
         res[name] = {"us_per_launch": us, "eager_us_per_launch": eager_us, "rows": cfg["n_out"],
-                     "tokens": n_req * n_new, "rows_per_s": cfg["n_out"] / (us / 1e6)}
+                     "tokens": n_req * n_new, "rows_per_s": cfg["n_out"] / (us / 1e6),
+                     "timing": f"median of 5 replays of a graph of {reps} launches"}
         del graph
     return res
 
@@ -377,10 +693,13 @@ def run_ours(args, rank, world):
     import torch.distributed as dist
 
     from deepseek_v4_compressed_c2_gb300 import binding as B
+    from deepseek_v4_compressed_c2_gb300 import workloads as W
     B.lib()
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    clocks = ClockSampler(local)
+    clocks.start()
     cfg = make_inputs()
 
     def to_dev_bf16(a):
@@ -395,86 +714,87 @@ def run_ours(args, rank, world):
     ttr = torch.from_numpy(cfg["token_to_req"]).to(dev)
     n_store = cfg["n_out"]
     n_tok, k = cfg["topk"].shape
-    n_gather = n_tok * k
+    n_slots = n_tok * k
+    n_valid = gather_rows_valid(cfg)
     pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    kvbuf = B.SparsePrefillKVBuffer(torch.empty((n_gather, 512), dtype=torch.bfloat16, device=dev))
+    kvbuf = B.SparsePrefillKVBuffer(torch.empty((n_slots, 512), dtype=torch.bfloat16, device=dev))
     stream = torch.cuda.Stream(device=dev)
     launches = [0]
+    store = B.prepare_compress_store(1, 2, rows, ext, pool, page_table=pt, page_bits=6,
+                                     rmsnorm_w=w, eps=cfg["eps"], freqs_cis=freqs, n_out=n_store,
+                                     err_word=err, stream=stream)
+    gwh = B.prepare_get_with_head_topk(kvbuf, 1, pool, topk, ttr, pt, 6, err_word=err,
+                                       stream=stream)
 
-    def prepared(rows_t, ext_t, pt_t, topk_t, ttr_t):
-        """the step's three C-ABI calls, marshalled once"""
-        store = B.prepare_compress_store(1, 2, rows_t, ext_t, pool, page_table=pt_t, page_bits=6,
-                                         rmsnorm_w=w, eps=cfg["eps"], freqs_cis=freqs,
-                                         n_out=n_store, err_word=err, stream=stream)
-        gwh = B.prepare_get_with_head_topk(kvbuf, 1, pool, topk_t, ttr_t, pt_t, 6, err_word=err,
-                                           stream=stream)
-        return store, gwh
+    def read_layers():
+        kvbuf.dsv4kv_kvbuf_begin_forward()
+        hits = [gwh() for _layer in range(LAYERS)]
+        assert hits == [False] + [True] * (LAYERS - 1)
 
-    resident = prepared(rows, ext, pt, topk, ttr)
-
-    def step(ev=None, calls=resident):
-        store, gwh = calls
+    def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
         store()
         if ev is not None:
             ev[1].record(stream)
-        kvbuf.dsv4kv_kvbuf_begin_forward()
-        hits = [gwh() for _layer in range(LAYERS)]
+        read_layers()
         if ev is not None:
             ev[2].record(stream)
-        assert hits == [False] + [True] * (LAYERS - 1)
         launches[0] += 2
-        return kvbuf.storage
 
     def barrier():
         if world > 1:
             dist.barrier()
 
-    with torch.cuda.stream(stream):
+    with clocks.busy("warmup"), torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
             step()
-    torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
     assert int(err.item()) == 0, "device faults during warm-up"
 
-    # ---- device-resident timing.  The per-kernel durations come from CUDA
-    # events around the store and the gather on every EVENT_EVERY-th step of
-    # the timed region: each event record costs ~2 us of stream time, so
-    # events on every step would lengthen the step by ~4 %.
-    ev_steps = list(range(0, args.steps, EVENT_EVERY))
-    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in ev_steps}
+    # ---- the timed region: K steps back to back, inputs resident in HBM
+    # (537 MB of fused rows per step, larger than the L2)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
     barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
     launches[0] = 0
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for i in range(args.steps):
-            step(evs.get(i))
-        t1.record(stream)
-    torch.cuda.synchronize(dev)
+    with clocks.busy("timed_region"):
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(args.steps):
+                step()
+            t1.record(stream)
+        torch.cuda.synchronize(dev)
     barrier()
-    clk = clocks.stop()
     n_launch = launches[0]
     elapsed_ms = t0.elapsed_time(t1)
-    store_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs.values())
-    gather_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs.values())
+
+    # ---- per-kernel durations: KERNEL_SAMPLES more steps with events around
+    # the store and around the gather (the events sit between the kernels, so
+    # these steps do not overlap one launch's tail with the next's start)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(KERNEL_SAMPLES)]
+    with clocks.busy("per_kernel"), torch.cuda.stream(stream):
+        for e in evs:
+            step(e)
+        torch.cuda.synchronize(dev)
+    store_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    gather_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
 
     # ---- end to end through host buffers (pinned host -> device -> host).
     # The batch is split into request chunks whose rows are contiguous; chunk
-    # c's rows travel host -> device while chunk c-1 is stored and gathered,
-    # and gathered rows travel back on a third stream.  Each step still moves
-    # every input row in and every gathered row out.
+    # c's rows travel host -> device while chunk c-1 is stored and read, and
+    # gathered rows travel back on a third stream.  Each chunk runs the same
+    # sequence as the device-resident step: the store, then 4 layers' reads
+    # through a reuse buffer (1 dequant + 3 hits) over its slice of the
+    # output.  Each step moves every input row in and every gathered row out.
     n_req = len(cfg["lengths"])
     bounds = np.linspace(0, n_req, E2E_CHUNKS + 1).astype(int)
     first, counts = cfg["ext"][0].astype(np.int64), cfg["ext"][1].astype(np.int64)
     h_rows = torch.from_numpy(cfg["rows"].view(np.int16)).view(torch.bfloat16).pin_memory()
     d_rows = rows.clone()
-    d_out = torch.empty((n_gather, 512), dtype=torch.bfloat16, device=dev)
-    h_out = torch.empty((n_gather, 512), dtype=torch.bfloat16).pin_memory()
+    d_out = torch.empty((n_slots, 512), dtype=torch.bfloat16, device=dev)
+    h_out = torch.empty((n_slots, 512), dtype=torch.bfloat16).pin_memory()
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     chunks, h2d = [], 0
     for c in range(E2E_CHUNKS):
@@ -489,18 +809,17 @@ def run_ours(args, rank, world):
         h_meta = {k2: torch.from_numpy(v).pin_memory() for k2, v in meta.items()}
         d_meta = {k2: v.to(dev) for k2, v in h_meta.items()}
         n_out_c = int((counts[r0:r1] // 2).sum())
-        k_tok = cfg["topk"].shape[1]
-        store_c = B.prepare_compress_store(1, 2, d_rows, d_meta["ext"], pool, page_table=d_meta["pt"],
-                                           page_bits=6, rmsnorm_w=w, eps=cfg["eps"],
-                                           freqs_cis=freqs, n_out=n_out_c, err_word=err,
-                                           stream=stream)
-        gather_c = B.prepare_dequant_gather_topk(1, pool, d_meta["topk"], d_meta["ttr"],
-                                                 d_meta["pt"], 6, d_out[r0 * k_tok:r1 * k_tok],
-                                                 err_word=err, stream=stream)
+        store_c = B.prepare_compress_store(1, 2, d_rows, d_meta["ext"], pool,
+                                           page_table=d_meta["pt"], page_bits=6, rmsnorm_w=w,
+                                           eps=cfg["eps"], freqs_cis=freqs, n_out=n_out_c,
+                                           err_word=err, stream=stream)
+        kv_c = B.SparsePrefillKVBuffer(d_out[r0 * k:r1 * k])
+        gwh_c = B.prepare_get_with_head_topk(kv_c, 1, pool, d_meta["topk"], d_meta["ttr"],
+                                             d_meta["pt"], 6, err_word=err, stream=stream)
         h2d += (row1 - row0) * rows.stride(0) * 2 + sum(v.numel() * v.element_size()
                                                          for v in h_meta.values())
-        chunks.append(dict(rows=(row0, row1), out=(r0 * k_tok, r1 * k_tok), h=h_meta, d=d_meta,
-                           store=store_c, gather=gather_c,
+        chunks.append(dict(rows=(row0, row1), out=(r0 * k, r1 * k), h=h_meta, d=d_meta,
+                           store=store_c, kv=kv_c, gwh=gwh_c,
                            ev_in=torch.cuda.Event(), ev_done=torch.cuda.Event(),
                            ev_out=torch.cuda.Event()))
     d2h = h_out.numel() * h_out.element_size()
@@ -515,11 +834,13 @@ def run_ours(args, rank, world):
                 a, b = ch["rows"]
                 d_rows[a:b].copy_(h_rows[a:b], non_blocking=True)
                 ch["ev_in"].record(s_in)
-        for ch in chunks:                          # store + gather
+        for ch in chunks:                          # store + 4 layers' reads
             stream.wait_event(ch["ev_in"])
             stream.wait_event(ch["ev_out"])        # d_out chunk copied out by the last step
             ch["store"]()
-            ch["gather"]()
+            ch["kv"].dsv4kv_kvbuf_begin_forward()
+            hits = [ch["gwh"]() for _layer in range(LAYERS)]
+            assert hits == [False] + [True] * (LAYERS - 1)
             ch["ev_done"].record(stream)
         for ch in chunks:                          # gathered rows out
             with torch.cuda.stream(s_out):
@@ -529,60 +850,67 @@ def run_ours(args, rank, world):
                 ch["ev_out"].record(s_out)
         launches[0] += 2 * len(chunks)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize(dev)
-    e0.record(s_in)
-    for _ in range(e2e_steps):
-        e2e_step()
-    s_out.wait_event(chunks[-1]["ev_out"])
-    e1.record(s_out)
-    torch.cuda.synchronize(dev)
+    with clocks.busy("e2e"):
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(s_in)
+        for _ in range(e2e_steps):
+            e2e_step()
+        s_out.wait_event(chunks[-1]["ev_out"])
+        e1.record(s_out)
+        torch.cuda.synchronize(dev)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     assert int(err.item()) == 0, "device faults during the timed region"
     # the host copy of the gathered rows equals the device-resident step's
-    assert torch.equal(h_out.view(torch.int16), kvbuf.storage[:n_gather].cpu().view(torch.int16))
+    assert torch.equal(h_out.view(torch.int16), kvbuf.storage[:n_slots].cpu().view(torch.int16))
+    del d_rows, chunks
 
-    # ---- the gather alone on a cold L2: a 1 Mi-row V41 pool (553 MB), 262,144
-    # unique random ids, L2 flushed (a 512 MB write) before every launch
-    cold = None
+    # ---- the five workloads one by one, the other layouts, decode / verify
+    peak, peak_kind = _peaks()
+    configs = cold = decode = None
+    cfg4 = None
     if not args.no_cold_gather:
-        cold = cold_gather(B, dev, stream, max(5, min(args.steps, 50)))
-        decode = decode_verify_steps(B, dev, stream, max_prefix=args.decode_prefix)
-    else:
-        decode = None
+        cfg4 = W.cfg4_gather()
+        flusher = Flusher(dev)
+        with clocks.busy("configs"):
+            configs, _pool4, rows4, ids4 = config_legs(B, dev, stream, flusher, cfg4, peak)
+            del _pool4
+            cold = cold_paths(B, dev, stream, flusher, cfg4, rows4, ids4, peak)
+            del rows4, ids4, flusher
+            torch.cuda.empty_cache()
+        with clocks.busy("decode_verify"):
+            decode = decode_verify_steps(B, dev, stream, max_prefix=args.decode_prefix)
+    clk = clocks.stop()
 
     # ---- max over ranks
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
     if rank != 0:
         return
     ms_per_step = elapsed_ms / args.steps
-    value = whole_job_rate(n_store + n_gather, world, ms_per_step)
-    peak, peak_kind = _peaks()
+    units = n_store + n_valid
+    value = whole_job_rate(units, world, ms_per_step)
     store_gbs = STORE_BYTES_PER_ROW * n_store / (store_ms / 1e3) / 1e9
-    gather_gbs = GATHER_BYTES_PER_ROW * n_gather / (gather_ms / 1e3) / 1e9
+    gather_bytes = GATHER_BYTES_PER_ROW * n_valid + PAD_BYTES_PER_ROW * (n_slots - n_valid)
+    gather_gbs = gather_bytes / (gather_ms / 1e3) / 1e9
     traffic = _profiled_traffic("compress_store_long_prefill", STORE_SOURCES)
-    step_bytes = STORE_BYTES_PER_ROW * n_store + GATHER_BYTES_PER_ROW * n_gather
+    step_bytes = STORE_BYTES_PER_ROW * n_store + gather_bytes
     step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": cfg["name"], "requests": len(cfg["lengths"]),
-                   "tokens": int(sum(cfg["lengths"])), "store_rows": n_store,
-                   "gather_rows": n_gather, "layers_reading_source": LAYERS, "layout": "V41",
-                   "ratio": 2, "page_size": 64, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (fused rows %d MB per step)"
-                         % (cfg["rows"].nbytes // 10 ** 6)},
+        "config": headline_config(cfg, world),
         "roofline": {"bound": "hbm", "achieved": store_gbs, "peak": peak, "unit": "GB/s",
                      "frac": store_gbs / peak, "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": "compress_store_kernel<V41, ratio 2, norm, rope>",
-                     "bytes_per_row": STORE_BYTES_PER_ROW, "frac_of_8000": store_gbs / 8000.0},
+                     "bytes_per_row": STORE_BYTES_PER_ROW, "frac_of_8000": store_gbs / 8000.0,
+                     "duration": f"median of {KERNEL_SAMPLES} in-step launches, CUDA events"},
         # the whole step against the same peak: both kernels' algorithmic bytes
         # over the step time (the gathered rows are written with evict-first
         # stores, so part of their write-back lands in the next store's time)
@@ -591,20 +919,34 @@ def run_ours(args, rank, world):
                           "bytes_per_step": step_bytes},
         "kernels": {
             "compress_store": {"ms": store_ms, "rows_per_s": n_store / (store_ms / 1e3),
-                               "gbs": store_gbs},
+                               "gbs": store_gbs, "samples": KERNEL_SAMPLES},
             "dequant_gather_topk_x1_plus_3_hits": {"ms": gather_ms,
-                                              "rows_per_s": n_gather / (gather_ms / 1e3),
-                                              "gbs": gather_gbs}},
+                                                  "rows_per_s": n_valid / (gather_ms / 1e3),
+                                                  "gbs": gather_gbs, "samples": KERNEL_SAMPLES,
+                                                  "bytes": gather_bytes}},
+        "configs": configs,
         "cold_l2": cold,
         "decode_verify_ring": decode,
-        "e2e": {"value": whole_job_rate(n_store + n_gather, world, e2e_ms), "unit": "rows/s",
-                "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "e2e": {"value": whole_job_rate(units, world, e2e_ms), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "sequence": f"{E2E_CHUNKS} request chunks, each: store, then {LAYERS} layers' "
+                            f"reads through a reuse buffer (1 dequant + {LAYERS - 1} hits); "
+                            "copies on two more streams"},
         "gpu_launches": n_launch,
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg)
+        if cfg4 is not None:
+            line["oracle_per_config"] = oracle_per_config(
+                {"cfg1": W.cfg1_v41_roundtrip(), "cfg2": W.cfg2_ratio2_small(),
+                 "cfg3": W.cfg3_fp4_store(), "cfg4": cfg4})
+            line["oracle_per_config"]["cfg5"] = {
+                "name": cfg["name"],
+                "store_and_gather": {
+                    "rows_per_s_1core": line["cpu_baseline"]["single_thread"]["value"],
+                    "rows_per_s_all_cores": line["cpu_baseline"]["value"],
+                    "sample": line["cpu_baseline"]["sample"]}}
     print(json.dumps(line), flush=True)
 
 
@@ -615,7 +957,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-cold-gather", action="store_true")
+    ap.add_argument("--no-cold-gather", action="store_true",
+                    help="skip the per-workload, other-layout and decode / verify legs")
     ap.add_argument("--decode-only", action="store_true",
                     help="diagnostic: only the decode / verify ring-form launches, one JSON line")
     ap.add_argument("--decode-prefix", type=int, default=4096,
