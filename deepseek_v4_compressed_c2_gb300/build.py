@@ -18,8 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdsv4kv.so")
-SOURCES = ["capi.cu", "compress_store.cu", "dequant_gather.cu", "topk_slots.cu", "selftest.cu",
-           "fake_quant.cu"]
+SOURCES = ["capi.cu", "compress_store.cu", "compress_decode.cu", "dequant_gather.cu",
+           "topk_slots.cu", "selftest.cu", "fake_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

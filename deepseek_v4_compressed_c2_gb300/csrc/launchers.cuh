@@ -12,6 +12,12 @@ namespace dsv4kv {
 
 cudaError_t launch_compress_store(const StoreParams& p, int layout, int ratio, cudaStream_t stream);
 
+// ratio-2 steps with start positions / the ring of at most kDecodeRowsPerCta
+// output rows per SM (large decode and speculative-verify steps): one CTA per
+// tile of kDecodeRowsPerCta rows (compress_decode.cu)
+constexpr int kDecodeRowsPerCta = 16;
+cudaError_t launch_compress_decode(const StoreParams& p, int layout, cudaStream_t stream);
+
 cudaError_t launch_dequant_gather(int layout, const uint8_t* pool, long long pool_rows,
                                   const int* ids, long long n, __nv_bfloat16* out, int* err,
                                   cudaStream_t stream);

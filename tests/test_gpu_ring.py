@@ -33,14 +33,17 @@ def gpu_step(B, cfg, pool, ring, *, want_pre=True):
     return None if pre is None else pre.cpu().numpy(), int(err.item())
 
 
-# The ring form's launch shape follows the rows per SM: 512 x 1 and 512 x 4
-# (<= 8 rows per SM) and 2048 x 5 (~5000 rows, > 16 per SM) take the
-# streaming shape, 512 x 7 and 4096 x 1 (8-16 per SM) the latency shape;
-# 4096 request slots is the largest plan (222 KB of shared memory there).
+# The ring form's launch follows the rows per SM: more than 8 and at most 16
+# (512 x 7, 4096 x 1, 320 x 9: ~1800, ~2000, ~1440 rows) take the decode
+# kernel (one 16-row tile per CTA; 4096 request slots is its largest plan),
+# fewer (512 x 1, 512 x 4) or more (2048 x 5, 1024 x 9: ~5000, ~4600 rows)
+# the streaming kernel; the x 9 steps have n >= 2R, so the ring update
+# rewrites the entry the step's first pair reads.
 @pytest.mark.parametrize("n_new,layout,n_req", [(1, oracle.V41, 512), (4, oracle.V41, 512),
                                                 (4, oracle.V41_FP4, 512), (7, oracle.V41, 512),
                                                 (7, oracle.V41_FP4, 512), (7, oracle.V4, 512),
-                                                (5, oracle.V41, 2048), (1, oracle.V41, 4096)])
+                                                (5, oracle.V41, 2048), (1, oracle.V41, 4096),
+                                                (9, oracle.V41, 320), (9, oracle.V4, 1024)])
 def test_decode_verify_step_matches_oracle(B, n_new, layout, n_req):
     cfg = dict(W.decode_verify(seed=11 + n_new, n_req=n_req, n_new=n_new, ring_size=4,
                                max_prefix=1024), layout=layout)
@@ -145,13 +148,13 @@ def test_negative_start_positions_fault_like_the_oracle(B, rope):
     assert np.array_equal(pool.cpu().numpy(), ref_pool)
 
 
-@pytest.mark.parametrize("n_new", [1, 4, 9])
-def test_ring_form_with_separate_score_or_padded_stride_equals_fused(B, n_new):
+@pytest.mark.parametrize("n_new,n_req", [(1, 300), (4, 300), (9, 300), (1, 2800), (9, 320)])
+def test_ring_form_with_separate_score_or_padded_stride_equals_fused(B, n_new, n_req):
     """The ring form reading kv and score from separate buffers, or from rows
     padded to 1536 elements, writes the same pool and ring bytes as the fused
-    | kv | score | rows (the producer's per-half copies, ring-sourced pairs
-    included)."""
-    cfg = W.decode_verify(seed=30 + n_new, n_req=300, n_new=n_new, ring_size=4, max_prefix=512)
+    | kv | score | rows (the streaming kernel's per-half copies, and the decode
+    kernel's loads for 2800 x 1 and 320 x 9, ring-sourced pairs included)."""
+    cfg = W.decode_verify(seed=30 + n_new, n_req=n_req, n_new=n_new, ring_size=4, max_prefix=512)
     rows = dev_bf16(cfg["rows"])
     common = dict(page_table=dev(cfg["page_table"]), page_bits=cfg["page_bits"],
                   rmsnorm_w=dev_bf16(cfg["norm_w"]), eps=cfg["eps"], freqs_cis=dev(cfg["freqs"]),
@@ -178,12 +181,14 @@ def test_ring_form_with_separate_score_or_padded_stride_equals_fused(B, n_new):
         assert np.array_equal(got[0], fused[0]) and np.array_equal(got[1], fused[1])
 
 
-@pytest.mark.parametrize("n_new", [3, 9])
-def test_ring_form_with_fewer_output_rows_than_the_step_makes(B, n_new):
+@pytest.mark.parametrize("n_new,n_req", [(3, 200), (9, 200), (9, 640)])
+def test_ring_form_with_fewer_output_rows_than_the_step_makes(B, n_new, n_req):
     """n_out below the step's row count: rows k >= n_out are neither computed
     nor stored, in the tiles and in the ring phase (n >= 2R rows), while the
-    ring is still updated for every request, as in the oracle."""
-    cfg = W.decode_verify(seed=50 + n_new, n_req=200, n_new=n_new, ring_size=4, max_prefix=512)
+    ring is still updated for every request, as in the oracle (640 x 9 with
+    n_out = half its ~2880 rows takes the decode kernel, whose plan then
+    saturates at n_out)."""
+    cfg = W.decode_verify(seed=50 + n_new, n_req=n_req, n_new=n_new, ring_size=4, max_prefix=512)
     n_out = cfg["n_out"] // 2
     cfg = dict(cfg, n_out=n_out, layout=oracle.V41)
     pool = torch.full((cfg["pool_rows"] * 528,), 0xA5, dtype=torch.uint8, device="cuda")
