@@ -58,7 +58,8 @@ PAD_BYTES_PER_ROW = 4 + 1024                           # a -1 id: read the id, w
 
 _CSRC = os.path.join("deepseek_v4_compressed_c2_gb300", "csrc")
 STORE_SOURCES = [os.path.join(_CSRC, f) for f in
-                 ("compress_store.cu", "quant.cuh", "tma.cuh", "layout.cuh", "internal.cuh")]
+                 ("compress_store.cu", "compress_row.cuh", "quant.cuh", "tma.cuh", "layout.cuh",
+                  "internal.cuh")]
 
 
 def _profiled_traffic(name, sources):
@@ -165,6 +166,33 @@ class ClockSampler:
                 "period_s": self.period}
 
 
+def set_l2_fetch_granularity(nbytes):
+    """The serving process's L2 fetch granularity (cudaLimitMaxL2FetchGranularity,
+    a limit of this process's CUDA context: it ends with the process).  The
+    step's read is a gather of random 288-584 B rows, and a whole 128-byte
+    line fetched per partly wanted line is DRAM traffic the gather does not
+    need; 0 leaves the context's default.  Returns the limit read back."""
+    import ctypes
+    import torch
+    torch.zeros(1, device="cuda")                 # the context exists
+    lib = None
+    for cand in (os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64", "libcudart.so"),
+                 "libcudart.so.13", "libcudart.so"):
+        try:
+            lib = ctypes.CDLL(cand)
+            break
+        except OSError:
+            continue
+    if lib is None:
+        return None
+    limit = 0x05                                  # cudaLimitMaxL2FetchGranularity
+    if nbytes:
+        if lib.cudaDeviceSetLimit(limit, ctypes.c_size_t(nbytes)) != 0:
+            return None
+    v = ctypes.c_size_t(0)
+    return int(v.value) if lib.cudaDeviceGetLimit(ctypes.byref(v), limit) == 0 else None
+
+
 def max_over_ranks(values, world, device="cpu"):
     """Element-wise max of per-rank floats over the process group (the bench
     reports the slowest rank's time); identity when world == 1."""
@@ -192,8 +220,9 @@ def gather_rows_valid(cfg):
     return int((cfg["topk"] >= 0).sum())
 
 
-def headline_config(cfg, world):
-    """The `config` both arms print for the long-prefill step."""
+def headline_config(cfg, world, l2_fetch):
+    """The `config` both arms print for the long-prefill step (l2_fetch: the
+    GPU arm's L2 fetch granularity setting, bytes)."""
     n_tok, k = cfg["topk"].shape
     return {"workload": cfg["name"], "requests": len(cfg["lengths"]),
             "tokens": int(sum(cfg["lengths"])), "store_rows": int(cfg["n_out"]),
@@ -201,7 +230,8 @@ def headline_config(cfg, world):
             "layers_reading_source": LAYERS, "layout": "V41", "ratio": 2, "page_size": 64,
             "parallelism": f"replicas x{world}",
             "l2": "inputs larger than L2 (fused rows %d MB per step)"
-                  % (cfg["rows"].nbytes // 10 ** 6)}
+                  % (cfg["rows"].nbytes // 10 ** 6),
+            "l2_fetch_granularity_bytes": l2_fetch}
 
 
 # ------------------------------------------------------------------ oracle
@@ -385,7 +415,7 @@ def run_reference(args, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": headline_config(cfg, world),
+            "config": headline_config(cfg, world, args.l2_fetch_granularity or None),
             "cpu_baseline": {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
                              "cpu_model": model, "sample": sample},
             "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0,
@@ -483,6 +513,7 @@ def config_legs(B, dev, stream, flusher, cfg4, peak):
     res = {}
 
     def store_call(c, pool):
+        stream.wait_stream(torch.cuda.current_stream(dev))   # the pool's zero fill first
         return B.prepare_compress_store(
             c["layout"], c["ratio"], bf(c["rows"]), t(c["ext"]), pool, page_table=t(c["page_table"]),
             page_bits=c["page_bits"], rmsnorm_w=None if c["norm_w"] is None else bf(c["norm_w"]),
@@ -534,6 +565,7 @@ def config_legs(B, dev, stream, flusher, cfg4, peak):
     # cfg4: 1 Mi-row V41 pool, 262,144 ids, read by 4 layers
     pool = torch.zeros(cfg4["pool_rows"] * 528, dtype=torch.uint8, device=dev)
     rows4 = bf(cfg4["rows"])
+    stream.wait_stream(torch.cuda.current_stream(dev))
     fill = B.prepare_compress_store(1, 1, rows4, t(cfg4["ext"]), pool,
                                     page_table=t(cfg4["page_table"]), page_bits=cfg4["page_bits"],
                                     n_out=cfg4["n_out"], err_word=err, stream=stream)
@@ -591,6 +623,7 @@ def cold_paths(B, dev, stream, flusher, cfg4, rows4, ids, peak):
     res = {}
     for layout, name, rb in ((1, "v41", 528), (2, "fp4", 288), (0, "v4", 584)):
         pool = torch.zeros(cfg4["pool_rows"] * rb, dtype=torch.uint8, device=dev)
+        stream.wait_stream(torch.cuda.current_stream(dev))
         store = B.prepare_compress_store(layout, 1, rows4, ext, pool, page_table=pt,
                                          page_bits=cfg4["page_bits"], n_out=n_rows, err_word=err,
                                          stream=stream)
@@ -648,6 +681,7 @@ def decode_verify_steps(B, dev, stream, reps=50, max_prefix=4096):
         err = torch.zeros(1, dtype=torch.int32, device=dev)
         rows = bf(cfg["rows"])
         ext = torch.from_numpy(cfg["ext"]).to(dev)
+        stream.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(stream):
             call = B.prepare_compress_store(
                 1, 2, rows, ext, pool, page_table=torch.from_numpy(cfg["page_table"]).to(dev),
@@ -688,6 +722,81 @@ def decode_verify_steps(B, dev, stream, reps=50, max_prefix=4096):
     return res
 
 
+PROFILE_LEGS = ("store_long_prefill", "step_gather", "gather_v41", "gather_fp4", "gather_v4",
+                "store_fp4_1m", "decode", "verify")
+
+
+def profile_leg(name):
+    """One leg's launches alone, for an ncu capture (three launches, the L2
+    flushed before each): the long-prefill store; the step's fused top-k
+    gather (after one store); the cold gather of the 262,144 cfg4 ids from
+    the 1 Mi-row pool in a layout (the pool filled by one store-only launch
+    first); the FP4 store-only fill of that pool; the decode (4096 x 1) or
+    verify (1024 x 4) ring step.  Prints one JSON line; times nothing."""
+    import torch
+    from deepseek_v4_compressed_c2_gb300 import binding as B
+    from deepseek_v4_compressed_c2_gb300 import workloads as W
+    B.lib()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)    # allocations and launches in one order
+    flusher = Flusher(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    if name in ("store_long_prefill", "step_gather"):
+        cfg = make_inputs()
+        pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device=dev)
+        call = B.prepare_compress_store(1, 2, bf(cfg["rows"]), t(cfg["ext"]), pool,
+                                        page_table=t(cfg["page_table"]), page_bits=6,
+                                        rmsnorm_w=bf(cfg["norm_w"]), eps=cfg["eps"],
+                                        freqs_cis=t(cfg["freqs"]), n_out=cfg["n_out"],
+                                        err_word=err, stream=stream)
+        if name == "step_gather":
+            n_tok, k = cfg["topk"].shape
+            out = torch.empty((n_tok * k, 512), dtype=torch.bfloat16, device=dev)
+            call = B.prepare_dequant_gather_topk(1, pool, t(cfg["topk"]), t(cfg["token_to_req"]),
+                                                 t(cfg["page_table"]), 6, out, err_word=err,
+                                                 stream=stream)
+    elif name == "store_fp4_1m":
+        cfg = W.cfg4_gather()
+        pool = torch.zeros(cfg["pool_rows"] * 288, dtype=torch.uint8, device=dev)
+        call = B.prepare_compress_store(2, 1, bf(cfg["rows"]), t(cfg["ext"]), pool,
+                                        page_table=t(cfg["page_table"]), page_bits=cfg["page_bits"],
+                                        n_out=cfg["n_out"], err_word=err, stream=stream)
+    elif name.startswith("gather_"):
+        layout, rb = {"gather_v41": (1, 528), "gather_fp4": (2, 288), "gather_v4": (0, 584)}[name]
+        cfg = W.cfg4_gather()
+        pool = torch.zeros(cfg["pool_rows"] * rb, dtype=torch.uint8, device=dev)
+        B.dsv4kv_compress_store(layout, 1, bf(cfg["rows"]), t(cfg["ext"]), pool,
+                                page_table=t(cfg["page_table"]), page_bits=cfg["page_bits"],
+                                n_out=cfg["n_out"], err_word=err, stream=stream)
+        ids = t(cfg["ids"])
+        out = torch.empty((ids.numel(), 512), dtype=torch.bfloat16, device=dev)
+        call = B.prepare_dequant_gather(layout, pool, ids, out, err_word=err, stream=stream)
+    else:
+        n_req, n_new = (4096, 1) if name == "decode" else (1024, 4)
+        cfg = W.decode_verify(seed=13, n_req=n_req, n_new=n_new, ring_size=4, max_prefix=4096)
+        pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device=dev)
+        call = B.prepare_compress_store(1, 2, bf(cfg["rows"]), t(cfg["ext"]), pool,
+                                        page_table=t(cfg["page_table"]), page_bits=6,
+                                        rmsnorm_w=bf(cfg["norm_w"]), eps=cfg["eps"],
+                                        freqs_cis=t(cfg["freqs"]), n_out=cfg["n_out"],
+                                        err_word=err, stream=stream,
+                                        start_pos=t(cfg["start_pos"]), ring=bf(cfg["ring"]))
+    for _ in range(3):
+        flusher()
+        call()
+    torch.cuda.synchronize(dev)
+    assert int(err.item()) == 0, f"{int(err.item())} device faults"
+    print(json.dumps({"profile_leg": name, "launches": 3 + (name.endswith("gather") or name.startswith("gather_"))}), flush=True)
+
+
 def run_ours(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -698,6 +807,7 @@ def run_ours(args, rank, world):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    l2_fetch = set_l2_fetch_granularity(args.l2_fetch_granularity)
     clocks = ClockSampler(local)
     clocks.start()
     cfg = make_inputs()
@@ -720,6 +830,7 @@ def run_ours(args, rank, world):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     kvbuf = B.SparsePrefillKVBuffer(torch.empty((n_slots, 512), dtype=torch.bfloat16, device=dev))
     stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))   # the zero fills before any launch
     launches = [0]
     store = B.prepare_compress_store(1, 2, rows, ext, pool, page_table=pt, page_bits=6,
                                      rmsnorm_w=w, eps=cfg["eps"], freqs_cis=freqs, n_out=n_store,
@@ -850,6 +961,7 @@ def run_ours(args, rank, world):
                 ch["ev_out"].record(s_out)
         launches[0] += 2 * len(chunks)
 
+    torch.cuda.synchronize(dev)          # the chunks' device buffers are in place
     with clocks.busy("e2e"):
         for _ in range(2):
             e2e_step()
@@ -905,7 +1017,7 @@ def run_ours(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": headline_config(cfg, world),
+        "config": headline_config(cfg, world, l2_fetch),
         "roofline": {"bound": "hbm", "achieved": store_gbs, "peak": peak, "unit": "GB/s",
                      "frac": store_gbs / peak, "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": "compress_store_kernel<V41, ratio 2, norm, rope>",
@@ -963,12 +1075,20 @@ def main():
                     help="diagnostic: only the decode / verify ring-form launches, one JSON line")
     ap.add_argument("--decode-prefix", type=int, default=4096,
                     help="cached prefix bound of the decode / verify requests (sizes their pool)")
+    ap.add_argument("--l2-fetch-granularity", type=int, default=32, choices=[0, 32, 64, 128],
+                    help="this process's L2 fetch granularity in bytes (0: the context default)")
+    ap.add_argument("--profile-leg", choices=PROFILE_LEGS,
+                    help="diagnostic for ncu: one leg's three launches (L2 flushed before each), "
+                         "no timing")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.profile_leg:
+        profile_leg(args.profile_leg)
         return
     if args.decode_only:
         import torch
