@@ -204,3 +204,64 @@ def test_ring_form_with_fewer_output_rows_than_the_step_makes(B, n_new, n_req):
     assert err == ref["faults"] == 0
     assert np.array_equal(pool.cpu().numpy(), same_pool)
     assert np.array_equal(host_u16(ring).reshape(ref_ring.shape), ref_ring)
+
+
+@pytest.mark.parametrize("form", ["odd_slots", "no_start", "no_ring", "out_loc", "latent"])
+def test_decode_kernel_launch_forms_match_oracle(B, form):
+    """The decode kernel (steps of 8-16 rows per SM) in its other launch
+    forms, against the oracle: a slot count that is no multiple of 4 (the
+    plan's scalar loads), no start positions (every slot starts at 0), start
+    positions without a ring (ring rows are faults), out_loc with padding
+    zeros, and the latent output.  Pool bytes exact given the GPU's fp32 rows,
+    ring and fault count equal."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_req, n_new = {"odd_slots": (2801, 1), "no_start": (1400, 2)}.get(form, (2800, 1))
+    cfg = W.decode_verify(seed=60 + len(form), n_req=n_req, n_new=n_new, ring_size=4,
+                          max_prefix=512)
+    start = None if form == "no_start" else cfg["start_pos"]
+    ring0 = None if form == "no_ring" else cfg["ring"]
+    p = oracle.plan(2, cfg["ext"], cfg["page_table"], cfg["page_bits"], start_pos=start)
+    n_out = p["total"]
+    assert 8 * sms < n_out <= 16 * sms, "the case must take the decode kernel"
+    out_loc = None
+    if form == "out_loc":
+        out_loc = p["slot"].astype(np.int32)
+        out_loc[::7] = 0
+    pool = torch.full((cfg["pool_rows"] * 528,), 0xA5, dtype=torch.uint8, device="cuda")
+    ring = None if ring0 is None else dev_bf16(ring0)
+    pre = torch.zeros((n_out, 512), dtype=torch.float32, device="cuda")
+    lat = torch.zeros((n_out, 512), dtype=torch.bfloat16, device="cuda") if form == "latent" else None
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsv4kv_compress_store(oracle.V41, 2, dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
+                            page_table=dev(cfg["page_table"]), page_bits=cfg["page_bits"],
+                            rmsnorm_w=dev_bf16(cfg["norm_w"]), eps=cfg["eps"],
+                            freqs_cis=dev(cfg["freqs"]), n_out=n_out,
+                            out_loc=None if out_loc is None else dev(out_loc),
+                            latent_out=lat, prequant_out=pre, err_word=err,
+                            start_pos=None if start is None else dev(start), ring=ring)
+    torch.cuda.synchronize()
+    pre_h = pre.cpu().numpy()
+    ref_pool = np.full(cfg["pool_rows"] * 528, 0xA5, np.uint8)
+    ref_ring = None if ring0 is None else ring0.copy()
+    ref = oracle.compress_store(oracle.V41, 2, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
+                                page_bits=cfg["page_bits"], norm_w=cfg["norm_w"], eps=cfg["eps"],
+                                freqs=cfg["freqs"], out_loc=out_loc, n_out=n_out, start_pos=start,
+                                pool=ref_pool, pool_rows=cfg["pool_rows"], ring=ref_ring,
+                                prequant_in=pre_h)
+    assert int(err.item()) == ref["faults"]
+    if form == "no_ring":
+        assert ref["faults"] == int((cfg["start_pos"] % 2 == 1).sum()) > 0
+    assert np.array_equal(pool.cpu().numpy(), ref_pool)
+    if ref_ring is not None:
+        assert np.array_equal(host_u16(ring).reshape(ref_ring.shape), ref_ring)
+    e2e = oracle.compress_store(oracle.V41, 2, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
+                                page_bits=cfg["page_bits"], norm_w=cfg["norm_w"], eps=cfg["eps"],
+                                freqs=cfg["freqs"], out_loc=out_loc, n_out=n_out, start_pos=start,
+                                ring=None if ring0 is None else ring0.copy())
+    ok = np.abs(e2e["prequant_f64"]).max(axis=1) > 0
+    assert_prequant_close(pre_h[ok], e2e["prequant_f64"][ok])
+    if lat is not None:
+        lat_g = oracle.bf16_to_f64(host_u16(lat))
+        lat_r = oracle.bf16_to_f64(e2e["latent"])
+        tol = np.abs(lat_r) * 2.0 ** -7 + 1e-5 * np.abs(lat_r).max(axis=1, keepdims=True)
+        assert np.all(np.abs(lat_g - lat_r) <= tol)
