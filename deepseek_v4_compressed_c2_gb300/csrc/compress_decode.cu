@@ -23,11 +23,13 @@
 //    slot, then runs process_row;
 //  * kDecRingWarps ring warps: the ring update (each even-position new token
 //    among the last 2R positions of a request goes to entry (q / 2) % R).
-// A request's ring update is done by the CTA that holds the request's
-// ring-reading row when that row is computed, otherwise by CTA r % grid, and
-// the CTA's ring warps write only after a CTA barrier that follows every row
-// warp's loads: every read of a ring entry precedes any write of it, also for
-// steps of n >= 2R tokens whose update rewrites the entry the step reads.
+// Every read of a ring entry precedes any write of it without a barrier: a
+// request whose ring-reading row (its first row, at an odd start) is computed
+// in this launch is updated by that row's CTA -- by the ring warps when its
+// step has n < 2R tokens (the update then writes other entries than the one
+// read), else by the row's own warp after the row (program order) -- and
+// every other request by CTA r % grid, whose update no row of the launch
+// reads.
 #include <atomic>
 #include <cstddef>
 
@@ -156,7 +158,7 @@ __device__ __forceinline__ int ring_tokens(int n, long long p0, int first, int R
 
 // The ring tokens of request r, none when another CTA does its update (a
 // round-robin candidate whose ring-reading row is computed is updated by
-// that row's CTA, which lists it in sh.list).
+// that row's CTA: listed in sh.list, or by the row's warp when n >= 2R).
 __device__ __forceinline__ RingWork ring_work(const StoreParams& p, const DecodePlan& pl, int r,
                                               bool candidate, unsigned cap) {
   RingWork w{0, 0, r, 0};
