@@ -558,9 +558,12 @@ def config_legs(B, dev, stream, flusher, cfg4, peak):
     res["cfg3_" + c3["name"]] = {
         "store_cold": _leg(_timed(st, stream, CONFIG_REPS, flusher), 32768, 1024 + 288, peak),
         "store_warm": _leg(_timed(st, stream, CONFIG_REPS), 32768, 1024 + 288),
+        "store_in_graph": _leg(_graph_us(st, stream) / 1e3, 32768, 1024 + 288),
         "dequant_cold": _leg(_timed(ga, stream, CONFIG_REPS, flusher), 32768, 288 + 4 + 1024, peak),
         "dequant_warm": _leg(_timed(ga, stream, CONFIG_REPS), 32768, 288 + 4 + 1024),
-        "note": "43 MB each way: fits in L2, so warm launches read L2"}
+        "dequant_in_graph": _leg(_graph_us(ga, stream) / 1e3, 32768, 288 + 4 + 1024),
+        "note": "43 MB each way: fits in L2, so warm launches read L2; *_in_graph = device "
+                "time per launch inside a CUDA graph of 50 launches (warm)"}
 
     # cfg4: 1 Mi-row V41 pool, 262,144 ids, read by 4 layers
     pool = torch.zeros(cfg4["pool_rows"] * 528, dtype=torch.uint8, device=dev)
