@@ -115,19 +115,36 @@ __device__ __forceinline__ void load_row(const uint8_t* in_row, const uint8_t* r
   }
 }
 
-template <int L, int RATIO, bool NORM, bool ROPE>
-__device__ __forceinline__ void process_row(const StoreParams& p, long long k, const RowDesc& d,
-                                            long long slot, const RowIn<RATIO, ROPE>& in,
-                                            const float (&w)[16], int lane) {
-  if (d.state == kRowNone || d.state == kRowRing) return;
-  if (d.state != kRowOk && d.state != kRowOkRing) {
-    if (d.state == kRowBad && lane == 0 && p.err) atomicAdd(p.err, 1);
-    zero_row_outputs(p, k, lane);
-    return;
-  }
+// A row between its arithmetic and its store: the lane's 16 values of x * w
+// (pooled, RMSNorm weight applied, RoPE'd) as 8 fp32 pairs and the norm's
+// deferred 1 / rms.  row_math needs only the row's inputs (and, for the
+// post-norm pre-RoPE latent it writes on the way, the output row latent_k;
+// latent_k < 0 writes none);
+// row_store also needs the output row k and the destination slot, so a
+// launch without the latent output can do the arithmetic before it knows
+// them.
+struct RowMath {
+  uint64_t x2[8];
+  float inv;
+};
+
+// The RMSNorm weights of a lane's pair q (dims 2q, 2q + 1 of its 16): from
+// 16 floats, or from the packed bf16 row (two uint4), with the same bits.
+__device__ __forceinline__ uint64_t norm_w_pair(const float (&w)[16], int q) {
+  return f2(w[2 * q], w[2 * q + 1]);
+}
+__device__ __forceinline__ uint64_t norm_w_pair(const uint4 (&w)[2], int q) {
+  const uint32_t v = word_of(w[q >> 2], q & 3);
+  return f2(bf16_lo(v), bf16_hi(v));
+}
+
+template <int RATIO, bool NORM, bool ROPE, typename NormW>
+__device__ __forceinline__ void row_math(const StoreParams& p, const RowIn<RATIO, ROPE>& in,
+                                         const NormW& w, int lane, RowMath& m,
+                                         long long latent_k) {
   // the lane's 16 values as 8 fp32 pairs: pairs 0..3 = dims 8l.., 4..7 =
   // dims 256+8l..; every pair comes from one bf16 word
-  uint64_t x2[8];
+  uint64_t (&x2)[8] = m.x2;
 #pragma unroll
   for (int q = 0; q < 8; ++q) x2[q] = f2_from_bf16x2(word_of(in.kv0[q >> 2], q & 3));
   if constexpr (RATIO == 2) {
@@ -155,16 +172,16 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
       const uint64_t anchor =
           f2(__uint_as_float((__float_as_uint(ka0) & m0) | (__float_as_uint(kb0) & ~m0)),
              __uint_as_float((__float_as_uint(ka1) & m1) | (__float_as_uint(kb1) & ~m1)));
-      const uint64_t w = f2(__uint_as_float(__float_as_uint(rcp_approx(d0)) ^ (u0 & 0x80000000u)),
-                            __uint_as_float(__float_as_uint(rcp_approx(d1)) ^ (u1 & 0x80000000u)));
-      x2[q] = f2_fma(f2_sub(x2[q], k1), w, anchor);
+      const uint64_t wt = f2(__uint_as_float(__float_as_uint(rcp_approx(d0)) ^ (u0 & 0x80000000u)),
+                             __uint_as_float(__float_as_uint(rcp_approx(d1)) ^ (u1 & 0x80000000u)));
+      x2[q] = f2_fma(f2_sub(x2[q], k1), wt, anchor);
     }
   }
   // RMSNorm: x_n = (x * w) * inv with inv = rsqrt(mean(x^2) + eps).  The
   // product by inv is deferred: RoPE rotates x * w, and the V41 quantizer
   // folds inv into its power-of-two multiplier, which rounds exactly like
   // quantizing the explicit x_n (see store_row_v41_scaled).
-  float inv = 1.f;
+  m.inv = 1.f;
   if constexpr (NORM) {
     uint64_t acc[2] = {0ull, 0ull};     // partial sums of dims = 0,1 and 2,3 (mod 4)
 #pragma unroll
@@ -175,16 +192,16 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
     float t = (s0 + s1) + (s2 + s3);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFullMask, t, o);
-    inv = rsqrtf(fmaf(t, 1.f / kDim, p.eps));
+    m.inv = rsqrtf(fmaf(t, 1.f / kDim, p.eps));
 #pragma unroll
-    for (int q = 0; q < 8; ++q) x2[q] = f2_mul(x2[q], f2(w[2 * q], w[2 * q + 1]));
+    for (int q = 0; q < 8; ++q) x2[q] = f2_mul(x2[q], norm_w_pair(w, q));
   }
-  const uint64_t inv2 = f2(inv, inv);
-  if (p.latent_out) {  // post-norm, pre-RoPE
+  if (p.latent_out && latent_k >= 0) {  // post-norm, pre-RoPE
+    const uint64_t inv2 = f2(m.inv, m.inv);
     float xn[16];
 #pragma unroll
     for (int q = 0; q < 8; ++q) f2_split(f2_mul(x2[q], inv2), xn[2 * q], xn[2 * q + 1]);
-    uint4* o = reinterpret_cast<uint4*>(p.latent_out + k * kDim);
+    uint4* o = reinterpret_cast<uint4*>(p.latent_out + latent_k * kDim);
     o[lane] = pack_bf16x8(xn);
     o[32 + lane] = pack_bf16x8(xn + 8);
   }
@@ -204,6 +221,14 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
       }
     }
   }
+}
+
+// The pre-quant output and the quantized row k at `slot` of a computed row.
+template <int L, bool NORM>
+__device__ __forceinline__ void row_store(const StoreParams& p, long long k, long long slot,
+                                          RowMath& m, int lane) {
+  uint64_t (&x2)[8] = m.x2;
+  const uint64_t inv2 = f2(m.inv, m.inv);
   float x[16];
   const bool store = slot > 0 && slot < p.pool_rows;
   if (slot != 0 && !store && lane == 0 && p.err) atomicAdd(p.err, 1);   // destination fault
@@ -224,8 +249,29 @@ __device__ __forceinline__ void process_row(const StoreParams& p, long long k, c
     if (store) store_row_split<L>(x, PagedKV<L>{p.pool, p.page_bits}.row(slot), lane);
   } else if (store) {
     f2_unpack16(x2, x);
-    store_row_v41_scaled(x, inv, PagedKV<kV41>{p.pool, p.page_bits}.row(slot), lane);
+    store_row_v41_scaled(x, m.inv, PagedKV<kV41>{p.pool, p.page_bits}.row(slot), lane);
   }
+}
+
+// A row that is not computed: nothing for a row another phase computes, else
+// zero debug outputs, and a fault for a bad row.  True when it is computed.
+__device__ __forceinline__ bool row_computed(const StoreParams& p, long long k, const RowDesc& d,
+                                             int lane) {
+  if (d.state == kRowOk || d.state == kRowOkRing) return true;
+  if (d.state == kRowNone || d.state == kRowRing) return false;
+  if (d.state == kRowBad && lane == 0 && p.err) atomicAdd(p.err, 1);
+  zero_row_outputs(p, k, lane);
+  return false;
+}
+
+template <int L, int RATIO, bool NORM, bool ROPE>
+__device__ __forceinline__ void process_row(const StoreParams& p, long long k, const RowDesc& d,
+                                            long long slot, const RowIn<RATIO, ROPE>& in,
+                                            const float (&w)[16], int lane) {
+  if (!row_computed(p, k, d, lane)) return;
+  RowMath m;
+  row_math<RATIO, NORM, ROPE>(p, in, w, lane, m, k);
+  row_store<L, NORM>(p, k, slot, m, lane);
 }
 
 

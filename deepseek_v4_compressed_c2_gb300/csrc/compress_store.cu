@@ -700,13 +700,12 @@ static cudaError_t launch_norm_rope(const StoreParams& p, cudaStream_t s) {
   return launch_variant<L, RATIO, false, false, RING, SHAPE>(p, s);
 }
 
-// The ring form (start positions and/or the pair-state ring) of steps of
-// more than 8 and at most 16 output rows per SM -- large decode and
-// speculative-verify steps -- runs the latency-shaped kernel of
-// compress_decode.cu (one 16-row tile per CTA, no staged copies): there the
-// streaming shape would give warps two rows in sequence.  Smaller steps
-// spread over more SMs in the streaming shape (measured faster up to ~1000
-// rows), longer ones (chunked prefill) stream.
+// The ring form (start positions and/or the pair-state ring) of steps of at
+// most 16 output rows per SM -- decode, speculative-verify and short
+// chunked-prefill steps -- runs the latency-shaped kernel of
+// compress_decode.cu (one chunk of request slots per CTA, no wait for a
+// plan of the whole step before a row's loads); longer steps (chunked
+// prefill) stream.
 template <int L>
 static cudaError_t launch_ratio(const StoreParams& p, int ratio, cudaStream_t s) {
   if (ratio == 1) {
@@ -719,9 +718,10 @@ static cudaError_t launch_ratio(const StoreParams& p, int ratio, cudaStream_t s)
   if (p.start_pos == nullptr && p.ring == nullptr)
     return launch_norm_rope<L, 2, false, kShapeStream>(p, s);
   const long long sms = device_sm_count();
-  if ((long long)p.n_out > sms * StoreShape<kShapeStream>::kWarps &&
-      (long long)p.n_out <= sms * kDecodeRowsPerCta)
-    return launch_compress_decode(p, L, s);
+  if ((long long)p.n_out <= sms * kDecodeRowsPerCta) {
+    const int grid = decode_grid(p.n_slots, p.n_out, (int)sms);
+    if (grid > 0) return launch_compress_decode(p, L, grid, s);
+  }
   return launch_norm_rope<L, 2, true, kShapeStream>(p, s);
 }
 

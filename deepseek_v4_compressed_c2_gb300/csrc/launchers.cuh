@@ -13,10 +13,15 @@ namespace dsv4kv {
 cudaError_t launch_compress_store(const StoreParams& p, int layout, int ratio, cudaStream_t stream);
 
 // ratio-2 steps with start positions / the ring of at most kDecodeRowsPerCta
-// output rows per SM (large decode and speculative-verify steps): one CTA per
-// tile of kDecodeRowsPerCta rows (compress_decode.cu)
+// output rows per SM (decode, speculative-verify and short chunked-prefill
+// steps): one CTA per chunk of at most kDecodeMaxChunk request slots
+// (compress_decode.cu).  decode_grid: the launch's CTA count, 0 when the
+// step does not fit the form.
 constexpr int kDecodeRowsPerCta = 16;
-cudaError_t launch_compress_decode(const StoreParams& p, int layout, cudaStream_t stream);
+constexpr int kDecodeMaxChunk = 32;
+constexpr int kDecodeMaxGrid = 256;
+int decode_grid(int n_slots, int n_out, int sms);
+cudaError_t launch_compress_decode(const StoreParams& p, int layout, int grid, cudaStream_t stream);
 
 cudaError_t launch_dequant_gather(int layout, const uint8_t* pool, long long pool_rows,
                                   const int* ids, long long n, __nv_bfloat16* out, int* err,

@@ -33,12 +33,12 @@ def gpu_step(B, cfg, pool, ring, *, want_pre=True):
     return None if pre is None else pre.cpu().numpy(), int(err.item())
 
 
-# The ring form's launch follows the rows per SM: more than 8 and at most 16
-# (512 x 7, 4096 x 1, 320 x 9: ~1800, ~2000, ~1440 rows) take the decode
-# kernel (one 16-row tile per CTA; 4096 request slots is its largest plan),
-# fewer (512 x 1, 512 x 4) or more (2048 x 5, 1024 x 9: ~5000, ~4600 rows)
-# the streaming kernel; the x 9 steps have n >= 2R, so the ring update
-# rewrites the entry the step's first pair reads.
+# The ring form's launch follows the rows per SM: at most 16 (512 x 1 .. 7,
+# 4096 x 1, 320 x 9: up to ~2000 rows) take the decode kernel (one chunk of
+# request slots per CTA; 4096 slots is its largest step), more (2048 x 5,
+# 1024 x 9: ~5000, ~4600 rows) the streaming kernel; the x 9 steps have
+# n >= 2R, so the ring update rewrites the entry the step's first pair
+# reads, and 512 x 7 makes chunks of more than 16 rows (overflow rows).
 @pytest.mark.parametrize("n_new,layout,n_req", [(1, oracle.V41, 512), (4, oracle.V41, 512),
                                                 (4, oracle.V41_FP4, 512), (7, oracle.V41, 512),
                                                 (7, oracle.V41_FP4, 512), (7, oracle.V4, 512),
@@ -148,12 +148,13 @@ def test_negative_start_positions_fault_like_the_oracle(B, rope):
     assert np.array_equal(pool.cpu().numpy(), ref_pool)
 
 
-@pytest.mark.parametrize("n_new,n_req", [(1, 300), (4, 300), (9, 300), (1, 2800), (9, 320)])
+@pytest.mark.parametrize("n_new,n_req", [(1, 300), (4, 300), (9, 300), (1, 2800), (9, 320),
+                                         (9, 640)])
 def test_ring_form_with_separate_score_or_padded_stride_equals_fused(B, n_new, n_req):
     """The ring form reading kv and score from separate buffers, or from rows
     padded to 1536 elements, writes the same pool and ring bytes as the fused
-    | kv | score | rows (the streaming kernel's per-half copies, and the decode
-    kernel's loads for 2800 x 1 and 320 x 9, ring-sourced pairs included)."""
+    | kv | score | rows (the decode kernel's loads and ring copies, ring-sourced
+    pairs included, and the streaming kernel's per-half copies for 640 x 9)."""
     cfg = W.decode_verify(seed=30 + n_new, n_req=n_req, n_new=n_new, ring_size=4, max_prefix=512)
     rows = dev_bf16(cfg["rows"])
     common = dict(page_table=dev(cfg["page_table"]), page_bits=cfg["page_bits"],
@@ -181,13 +182,13 @@ def test_ring_form_with_separate_score_or_padded_stride_equals_fused(B, n_new, n
         assert np.array_equal(got[0], fused[0]) and np.array_equal(got[1], fused[1])
 
 
-@pytest.mark.parametrize("n_new,n_req", [(3, 200), (9, 200), (9, 640)])
+@pytest.mark.parametrize("n_new,n_req", [(3, 200), (9, 200), (9, 640), (9, 1280)])
 def test_ring_form_with_fewer_output_rows_than_the_step_makes(B, n_new, n_req):
     """n_out below the step's row count: rows k >= n_out are neither computed
     nor stored, in the tiles and in the ring phase (n >= 2R rows), while the
-    ring is still updated for every request, as in the oracle (640 x 9 with
-    n_out = half its ~2880 rows takes the decode kernel, whose plan then
-    saturates at n_out)."""
+    ring is still updated for every request, as in the oracle (the decode
+    kernel, whose chunk prefix then saturates at n_out, up to 640 x 9; the
+    streaming kernel for 1280 x 9 with n_out = half its ~5760 rows)."""
     cfg = W.decode_verify(seed=50 + n_new, n_req=n_req, n_new=n_new, ring_size=4, max_prefix=512)
     n_out = cfg["n_out"] // 2
     cfg = dict(cfg, n_out=n_out, layout=oracle.V41)
@@ -208,7 +209,7 @@ def test_ring_form_with_fewer_output_rows_than_the_step_makes(B, n_new, n_req):
 
 @pytest.mark.parametrize("form", ["odd_slots", "no_start", "no_ring", "out_loc", "latent"])
 def test_decode_kernel_launch_forms_match_oracle(B, form):
-    """The decode kernel (steps of 8-16 rows per SM) in its other launch
+    """The decode kernel (steps of at most 16 rows per SM) in its other launch
     forms, against the oracle: a slot count that is no multiple of 4 (the
     plan's scalar loads), no start positions (every slot starts at 0), start
     positions without a ring (ring rows are faults), out_loc with padding
@@ -222,7 +223,7 @@ def test_decode_kernel_launch_forms_match_oracle(B, form):
     ring0 = None if form == "no_ring" else cfg["ring"]
     p = oracle.plan(2, cfg["ext"], cfg["page_table"], cfg["page_bits"], start_pos=start)
     n_out = p["total"]
-    assert 8 * sms < n_out <= 16 * sms, "the case must take the decode kernel"
+    assert n_out <= 16 * sms, "the case must take the decode kernel"
     out_loc = None
     if form == "out_loc":
         out_loc = p["slot"].astype(np.int32)
