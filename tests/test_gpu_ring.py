@@ -266,3 +266,49 @@ def test_decode_kernel_launch_forms_match_oracle(B, form):
         lat_r = oracle.bf16_to_f64(e2e["latent"])
         tol = np.abs(lat_r) * 2.0 ** -7 + 1e-5 * np.abs(lat_r).max(axis=1, keepdims=True)
         assert np.all(np.abs(lat_g - lat_r) <= tol)
+
+
+def test_decode_kernel_mixed_step_with_long_requests(B):
+    """A step that mixes 600 decode requests with a few long ones, all in the
+    decode kernel (at most 16 rows per SM): requests of 80 new tokens at an
+    odd start make chunks of 40+ rows (overflow rows taken by other CTAs'
+    spare warps) and 40 ring tokens each (more than the ring warp's 32
+    stages, so it moves them in two batches); one request of 130 tokens at
+    an odd start has n >= 2R, so its ring update follows its first row in
+    that row's warp.  Ring, pool bytes (given the GPU's fp32 rows) and fault
+    count equal the oracle's; pre-quant within tolerance."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rng = np.random.default_rng(71)
+    n_req, R = 600, 64
+    lengths = [1] * n_req
+    p0 = rng.integers(0, 2048, n_req).astype(np.int32)
+    for r, n in ((5, 80), (6, 80), (300, 80), (599, 80), (301, 130)):
+        lengths[r] = n
+        p0[r] |= 1                                   # odd start: the first pair reads the ring
+    rows = W.bf16_normal(rng, (sum(lengths), 1024))
+    ring0 = W.bf16_normal(rng, (n_req, R, 1024))
+    norm_w = W.bf16_from_f32(rng.uniform(0.5, 1.5, 512).astype(np.float32))
+    max_c = (2048 + 130) // 2 + 1
+    pt, n_pages = W._page_table(rng, [-(-max_c // 64)] * n_req)
+    ext = W._ext(lengths)
+    n_out = int(sum(((int(a) + n) >> 1) - (int(a) >> 1) for a, n in zip(p0, lengths)))
+    assert n_out <= 16 * sms, "the step must take the decode kernel"
+    cfg = dict(layout=oracle.V41, rows=rows, ext=ext, start_pos=p0, page_table=pt, page_bits=6,
+               norm_w=norm_w, eps=1e-6, freqs=W.rope_table(2048 + 132), n_out=n_out,
+               pool_rows=n_pages << 6)
+    pool = torch.full((cfg["pool_rows"] * 528,), 0xA5, dtype=torch.uint8, device="cuda")
+    ring = dev_bf16(ring0)
+    pre, err = gpu_step(B, cfg, pool, ring)
+    kw = dict(page_table=pt, page_bits=6, norm_w=norm_w, eps=1e-6, freqs=cfg["freqs"], n_out=n_out,
+              start_pos=p0)
+    ref_ring = ring0.copy()
+    ref_pool = np.full(cfg["pool_rows"] * 528, 0xA5, np.uint8)
+    ref = oracle.compress_store(oracle.V41, 2, rows, ext, pool=ref_pool, pool_rows=cfg["pool_rows"],
+                                ring=ref_ring, **kw)
+    assert err == ref["faults"] == 0
+    assert np.array_equal(host_u16(ring).reshape(ref_ring.shape), ref_ring)
+    assert_prequant_close(pre[:n_out], ref["prequant_f64"][:n_out])
+    same_pool = np.full(cfg["pool_rows"] * 528, 0xA5, np.uint8)
+    oracle.compress_store(oracle.V41, 2, rows, ext, pool=same_pool, pool_rows=cfg["pool_rows"],
+                          ring=ring0.copy(), prequant_in=pre, **kw)
+    assert np.array_equal(pool.cpu().numpy(), same_pool)
