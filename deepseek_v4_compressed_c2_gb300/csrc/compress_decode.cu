@@ -210,7 +210,7 @@ __device__ __forceinline__ void copy_ring_tokens(const StoreParams& p, long long
   }
 }
 
-// ---- ring tokens of the chunk through shared memory (warp 0) ------------
+// ---- ring tokens of the chunk through shared memory (the ring warp) -----
 // Lane l holds slot S * b + l's tokens (none when its update follows its
 // first row); the chunk's tokens are numbered lane by lane from g0 and move
 // in batches of kDecStages: bulk loads into the stages, then bulk stores to

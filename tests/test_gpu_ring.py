@@ -207,14 +207,16 @@ def test_ring_form_with_fewer_output_rows_than_the_step_makes(B, n_new, n_req):
     assert np.array_equal(host_u16(ring).reshape(ref_ring.shape), ref_ring)
 
 
-@pytest.mark.parametrize("form", ["odd_slots", "no_start", "no_ring", "out_loc", "latent"])
+@pytest.mark.parametrize("form", ["odd_slots", "no_start", "no_ring", "out_loc", "latent",
+                                  "padded"])
 def test_decode_kernel_launch_forms_match_oracle(B, form):
     """The decode kernel (steps of at most 16 rows per SM) in its other launch
     forms, against the oracle: a slot count that is no multiple of 4 (the
     plan's scalar loads), no start positions (every slot starts at 0), start
     positions without a ring (ring rows are faults), out_loc with padding
-    zeros, and the latent output.  Pool bytes exact given the GPU's fp32 rows,
-    ring and fault count equal."""
+    zeros, the latent output, and n_out past the step's rows (the padding
+    rows' latent and pre-quant outputs zeroed over a sentinel).  Pool bytes
+    exact given the GPU's fp32 rows, ring and fault count equal."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     n_req, n_new = {"odd_slots": (2801, 1), "no_start": (1400, 2)}.get(form, (2800, 1))
     cfg = W.decode_verify(seed=60 + len(form), n_req=n_req, n_new=n_new, ring_size=4,
@@ -222,7 +224,7 @@ def test_decode_kernel_launch_forms_match_oracle(B, form):
     start = None if form == "no_start" else cfg["start_pos"]
     ring0 = None if form == "no_ring" else cfg["ring"]
     p = oracle.plan(2, cfg["ext"], cfg["page_table"], cfg["page_bits"], start_pos=start)
-    n_out = p["total"]
+    n_out = p["total"] + (300 if form == "padded" else 0)
     assert n_out <= 16 * sms, "the case must take the decode kernel"
     out_loc = None
     if form == "out_loc":
@@ -230,8 +232,9 @@ def test_decode_kernel_launch_forms_match_oracle(B, form):
         out_loc[::7] = 0
     pool = torch.full((cfg["pool_rows"] * 528,), 0xA5, dtype=torch.uint8, device="cuda")
     ring = None if ring0 is None else dev_bf16(ring0)
-    pre = torch.zeros((n_out, 512), dtype=torch.float32, device="cuda")
-    lat = torch.zeros((n_out, 512), dtype=torch.bfloat16, device="cuda") if form == "latent" else None
+    pre = torch.full((n_out, 512), 7.0, dtype=torch.float32, device="cuda")
+    lat = (torch.full((n_out, 512), 7.0, dtype=torch.bfloat16, device="cuda")
+           if form in ("latent", "padded") else None)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     B.dsv4kv_compress_store(oracle.V41, 2, dev_bf16(cfg["rows"]), dev(cfg["ext"]), pool,
                             page_table=dev(cfg["page_table"]), page_bits=cfg["page_bits"],
@@ -255,6 +258,10 @@ def test_decode_kernel_launch_forms_match_oracle(B, form):
     assert np.array_equal(pool.cpu().numpy(), ref_pool)
     if ref_ring is not None:
         assert np.array_equal(host_u16(ring).reshape(ref_ring.shape), ref_ring)
+    if form == "padded":
+        tot = p["total"]
+        assert not pre[tot:].any() and not lat[tot:].any()
+        assert np.isfinite(pre_h[:tot]).all()
     e2e = oracle.compress_store(oracle.V41, 2, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
                                 page_bits=cfg["page_bits"], norm_w=cfg["norm_w"], eps=cfg["eps"],
                                 freqs=cfg["freqs"], out_loc=out_loc, n_out=n_out, start_pos=start,
