@@ -664,6 +664,31 @@ def cold_paths(B, dev, stream, flusher, cfg4, rows4, ids, peak):
     return res
 
 
+def c1_leg(B, dev, stream, flusher, cfg, rows, peak):
+    """The full c1 form of the compressor on the long-prefill batch: ratio 1
+    with RMSNorm and RoPE, one V41 row per token (the same 262,144 fused rows,
+    already on the device, their kv half read), into a pool paged by
+    `workloads.c1_page_table`; each launch timed alone with a cold L2."""
+    import torch
+    from deepseek_v4_compressed_c2_gb300 import workloads as W
+    pt_h, pool_rows = W.c1_page_table(cfg["lengths"], page_bits=cfg["page_bits"])
+    n = int(sum(cfg["lengths"]))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pool = torch.zeros(pool_rows * 528, dtype=torch.uint8, device=dev)
+    bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    store = B.prepare_compress_store(1, 1, rows, torch.from_numpy(cfg["ext"]).to(dev), pool,
+                                     page_table=torch.from_numpy(pt_h).to(dev),
+                                     page_bits=cfg["page_bits"], rmsnorm_w=bf(cfg["norm_w"]),
+                                     eps=cfg["eps"], freqs_cis=torch.from_numpy(cfg["freqs"]).to(dev),
+                                     n_out=n, err_word=err, stream=stream)
+    ms = _timed(store, stream, max(5, CONFIG_REPS // 5), flusher)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return {f"store_ratio1_v41_norm_rope_{n}rows": _leg(ms, n, 1024 + 256 + 528, peak,
+                                                         note="1808 B/row: kv row, RoPE row, V41 row")}
+
+
 def decode_verify_steps(B, dev, stream, reps=50, max_prefix=4096):
     """The ring form of the compressor on decode-shaped steps (one new token
     per request; 1 + 3 draft tokens per request).  These are small,
@@ -996,7 +1021,9 @@ def run_ours(args, rank, world):
             configs, _pool4, rows4, ids4 = config_legs(B, dev, stream, flusher, cfg4, peak)
             del _pool4
             cold = cold_paths(B, dev, stream, flusher, cfg4, rows4, ids4, peak)
-            del rows4, ids4, flusher
+            del rows4, ids4
+            cold.update(c1_leg(B, dev, stream, flusher, cfg, rows, peak))
+            del flusher
             torch.cuda.empty_cache()
         with clocks.busy("decode_verify"):
             decode = decode_verify_steps(B, dev, stream, max_prefix=args.decode_prefix)

@@ -226,6 +226,27 @@ def decode_verify(seed: int = 11, n_req: int = 512, n_new: int = 4, ring_size: i
                 lengths=[n_new] * n_req)
 
 
+def c1_page_table(lengths, seed: int = 107, page_bits: int = 6):
+    """Random permuted page tables for one compressed row per token (the
+    ratio-1 compressor over a batch of requests of these lengths): int32
+    [n_req, max_pages] and the pool's row count (page 0 reserved)."""
+    rng = np.random.default_rng(seed)
+    pt, n_pages = _page_table(rng, [-(-n // (1 << page_bits)) for n in lengths])
+    return pt, n_pages << page_bits
+
+
+def c1_long_prefill(seed: int = 7, n_req: int = 64, target: int = 262144, page_bits: int = 6):
+    """The long-prefill batch through the ratio-1 compressor with RMSNorm and
+    RoPE (the full c1 form): the same 64 lognormal requests, fused
+    | kv | score | bf16 rows (the score columns unused), RMSNorm weight and
+    RoPE table as the ratio-2 batch; one V41 row per token at its position,
+    page size 64 over random permuted page tables (seed + 100)."""
+    c = cfg5_long_prefill(seed, n_req, target, page_bits=page_bits)
+    pt, pool_rows = c1_page_table(c["lengths"], seed + 100, page_bits)
+    return dict(c, name=f"c1_long_prefill_{n_req}req_{sum(c['lengths'])}tok", ratio=1,
+                page_table=pt, n_out=sum(c["lengths"]), pool_rows=pool_rows, topk=None)
+
+
 CONFIGS = {
     1: cfg1_v41_roundtrip,
     2: cfg2_ratio2_small,

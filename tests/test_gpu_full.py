@@ -209,3 +209,41 @@ def test_long_prefill_ratio2_norm_rope_store_fp4_and_v4(B, layout):
     assert np.array_equal(got_rows, oracle.quantize_rows(layout, g_pre))
     compare_rows_end_to_end(layout, got_rows, oracle.quantize_rows(layout, ref["prequant_f32"]),
                             ref["prequant_f64"])
+
+
+def test_long_prefill_ratio1_norm_rope_store(B):
+    """The full c1 form on the long-prefill batch: ratio 1 with RMSNorm and
+    RoPE, one V41 row per token (262,144 rows, positions up to 32,767).  The
+    launch without debug outputs writes the same pool bytes as the one with
+    them; 2048 sampled rows match the oracle (pre-quant within 1e-5, bytes
+    exact given the GPU's fp32 rows, codes within the end-to-end budget);
+    every planned slot is written once."""
+    cfg = W.c1_long_prefill()
+    rb = 528
+    pool = torch.full((cfg["pool_rows"] * rb,), 0xA5, dtype=torch.uint8, device="cuda")
+    pre = torch.empty((cfg["n_out"], 512), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _store(B, cfg, pool, prequant=pre, err=err)
+    bench_pool = torch.full_like(pool, 0xA5)
+    _store(B, cfg, bench_pool, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(bench_pool, pool)
+    host_pool = pool.cpu().numpy()
+    p = oracle.plan(1, cfg["ext"], cfg["page_table"], cfg["page_bits"])
+    assert p["total"] == cfg["n_out"]
+    untouched = np.all(host_pool.reshape(-1, rb) == 0xA5, axis=1)
+    assert untouched.sum() == cfg["pool_rows"] - p["total"]
+    assert not untouched[p["slot"]].any()
+    rng = np.random.default_rng(11)
+    which = np.sort(rng.choice(p["total"], 2048, replace=False)).astype(np.int64)
+    ref = oracle.compress_store(1, 1, cfg["rows"], cfg["ext"], page_table=cfg["page_table"],
+                                page_bits=cfg["page_bits"], norm_w=cfg["norm_w"], eps=cfg["eps"],
+                                freqs=cfg["freqs"], n_out=cfg["n_out"], which=which,
+                                want_latent=False)
+    g_pre = pre.cpu().numpy()[which]
+    assert_prequant_close(g_pre, ref["prequant_f64"])
+    got_rows = host_pool.reshape(-1, rb)[p["slot"][which]]
+    assert np.array_equal(got_rows, oracle.quantize_rows(1, g_pre))
+    compare_rows_end_to_end(1, got_rows, oracle.quantize_rows(1, ref["prequant_f32"]),
+                            ref["prequant_f64"])
