@@ -319,3 +319,65 @@ def test_decode_kernel_mixed_step_with_long_requests(B):
     oracle.compress_store(oracle.V41, 2, rows, ext, pool=same_pool, pool_rows=cfg["pool_rows"],
                           ring=ring0.copy(), prequant_in=pre, **kw)
     assert np.array_equal(pool.cpu().numpy(), same_pool)
+
+
+def test_decode_steps_in_a_cuda_graph_with_metadata_refreshed_in_place(B):
+    """The serving loop's shape: one decode step (1024 requests x 1 new token,
+    ring of 4) captured in a CUDA graph and replayed for 4 consecutive steps,
+    with the new tokens' rows and the start positions written into the same
+    device buffers before each replay (positions advance by one; n_out is the
+    graph-static upper bound, so about half the rows are padding).  After
+    every step the pool (given the GPU's fp32 rows) and the pair-state ring
+    equal the oracle's, run step by step on the carried state."""
+    rng = np.random.default_rng(81)
+    n_req, R, steps = 1024, 4, 4
+    p0 = rng.integers(0, 1024, n_req).astype(np.int32)
+    norm_w = W.bf16_from_f32(rng.uniform(0.5, 1.5, 512).astype(np.float32))
+    freqs = W.rope_table(1024 + steps + 2)
+    pt, n_pages = W._page_table(rng, [-(-((1024 + steps) // 2 + 1) // 64)] * n_req)
+    ext = W._ext([1] * n_req)
+    ring0 = W.bf16_normal(rng, (n_req, R, 1024))
+    pool_rows = n_pages << 6
+    d_rows = torch.empty((n_req, 1024), dtype=torch.bfloat16, device="cuda")
+    d_start = torch.empty(n_req, dtype=torch.int32, device="cuda")
+    d_ext, d_pt = dev(ext), dev(pt)
+    ring = dev_bf16(ring0)
+    pool = torch.full((pool_rows * 528,), 0xA5, dtype=torch.uint8, device="cuda")
+    pre = torch.zeros((n_req, 512), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # preparing runs the launch once, and one more warms it outside the
+    # capture: both on valid inputs, then the state is put back
+    d_rows.zero_()
+    d_start.copy_(dev(p0))
+    keep_ring, keep_pool = ring.clone(), pool.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call = B.prepare_compress_store(1, 2, d_rows, d_ext, pool, page_table=d_pt, page_bits=6,
+                                        rmsnorm_w=dev_bf16(norm_w), eps=1e-6,
+                                        freqs_cis=dev(freqs), n_out=n_req, prequant_out=pre,
+                                        err_word=err, stream=s, start_pos=d_start, ring=ring)
+        call()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ring.copy_(keep_ring)
+    pool.copy_(keep_pool)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call()
+    ref_ring, ref_pool = ring0.copy(), np.full(pool_rows * 528, 0xA5, np.uint8)
+    for step in range(steps):
+        rows = W.bf16_normal(rng, (n_req, 1024))
+        start = p0 + step
+        d_rows.copy_(dev_bf16(rows))                      # refreshed in place
+        d_start.copy_(dev(start.astype(np.int32)))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        kw = dict(page_table=pt, page_bits=6, norm_w=norm_w, eps=1e-6, freqs=freqs, n_out=n_req,
+                  start_pos=start.astype(np.int32))
+        oracle.compress_store(oracle.V41, 2, rows, ext, pool=ref_pool, pool_rows=pool_rows,
+                              ring=ref_ring, prequant_in=pre.cpu().numpy(), **kw)
+        assert np.array_equal(host_u16(ring).reshape(ref_ring.shape), ref_ring), step
+        assert np.array_equal(pool.cpu().numpy(), ref_pool), step
