@@ -45,33 +45,37 @@
 
 namespace dsv4kv {
 
-// Two launch shapes.  Streaming (large batches): 8 consumer warps, 3
+// Three launch shapes.  Streaming (large batches): 8 consumer warps, 3
 // stages, two CTAs per SM, so each SM keeps 48 rows' inputs in flight.
-// Wide (ratio-1 rows that are only stored): 8 consumer warps of 2 rows, one
-// per half-warp, 2 stages, three CTAs per SM (72 registers): the store-only
-// quantizers are latency-bound at two CTAs per SM.  Decode and speculative
-// verify steps (at most 16 rows per SM) take the kernel of
-// compress_decode.cu instead.
-enum StoreShapeId : int { kShapeStream = 0, kShapeWide = 2 };
+// Streaming-3 (ratio-1 rows with RMSNorm or RoPE): 8 consumer warps of one
+// row, 2 stages, three CTAs per SM (72 registers), for rows whose time is
+// instruction issue rather than bytes.  Wide (ratio-1 rows that are only
+// stored): 8 consumer warps of 2 rows, one per half-warp, 2 stages, three
+// CTAs per SM (72 registers): the store-only quantizers are latency-bound
+// at two CTAs per SM.  Decode and speculative verify steps (at most 16 rows
+// per SM) take the kernel of compress_decode.cu instead.
+enum StoreShapeId : int { kShapeStream = 0, kShapeStream3 = 1, kShapeWide = 2 };
 
 template <int SHAPE>
 struct StoreShape {
   static constexpr int kWarps = 8;                                   // consumer warps
   static constexpr int kStages = SHAPE == kShapeStream ? 3 : 2;
-  static constexpr int kMinBlocks = SHAPE == kShapeWide ? 3 : 2;     // CTAs per SM
+  static constexpr int kMinBlocks = SHAPE == kShapeStream ? 2 : 3;   // CTAs per SM
   static constexpr int kThreads = (kWarps + 1) * 32;
 };
 
 // Rows per consumer warp per stage: one ratio-2 pair (4 KB), four ratio-1
 // rows when the row is only stored (32 KB stages either way), two ratio-1
-// rows with RMSNorm or RoPE, or in the wide shape (four would spill).
+// rows with RMSNorm or RoPE in the streaming shape or in the wide shape
+// (four would spill), one in the streaming-3 shape (two spill at 72
+// registers).
 template <int RATIO, bool NORM, bool ROPE, int SHAPE>
 struct StoreTile {
   static constexpr int kWarps = StoreShape<SHAPE>::kWarps;
   static constexpr int kStages = StoreShape<SHAPE>::kStages;
   static constexpr int kThreads = StoreShape<SHAPE>::kThreads;
   static constexpr int kRowsPerWarp =
-      RATIO == 2 ? 1 : (NORM || ROPE || SHAPE == kShapeWide ? 2 : 4);
+      RATIO == 2 || SHAPE == kShapeStream3 ? 1 : (NORM || ROPE || SHAPE == kShapeWide ? 2 : 4);
   static constexpr int kRows = kWarps * kRowsPerWarp;              // rows per stage
   static constexpr int kInBytes = RATIO == 2 ? 4096 : 1024;        // kv0|s0|kv1|s1, or kv
   static constexpr int kRopeBytes = ROPE ? kRopeDim * 4 : 0;
@@ -710,9 +714,9 @@ template <int L>
 static cudaError_t launch_ratio(const StoreParams& p, int ratio, cudaStream_t s) {
   if (ratio == 1) {
     const bool norm = p.norm_w != nullptr, rope = p.freqs != nullptr;
-    if (norm && rope) return launch_variant<L, 1, true, true, false, kShapeStream>(p, s);
-    if (norm) return launch_variant<L, 1, true, false, false, kShapeStream>(p, s);
-    if (rope) return launch_variant<L, 1, false, true, false, kShapeStream>(p, s);
+    if (norm && rope) return launch_variant<L, 1, true, true, false, kShapeStream3>(p, s);
+    if (norm) return launch_variant<L, 1, true, false, false, kShapeStream3>(p, s);
+    if (rope) return launch_variant<L, 1, false, true, false, kShapeStream3>(p, s);
     return launch_variant<L, 1, false, false, false, kShapeWide>(p, s);
   }
   if (p.start_pos == nullptr && p.ring == nullptr)
