@@ -751,7 +751,7 @@ def decode_verify_steps(B, dev, stream, reps=50, max_prefix=4096):
 
 
 PROFILE_LEGS = ("store_long_prefill", "step_gather", "gather_v41", "gather_fp4", "gather_v4",
-                "store_fp4_1m", "decode", "verify")
+                "store_fp4_1m", "decode", "verify", "store_c1")
 
 
 def profile_leg(name):
@@ -760,7 +760,8 @@ def profile_leg(name):
     gather (after one store); the cold gather of the 262,144 cfg4 ids from
     the 1 Mi-row pool in a layout (the pool filled by one store-only launch
     first); the FP4 store-only fill of that pool; the decode (4096 x 1) or
-    verify (1024 x 4) ring step.  Prints one JSON line; times nothing."""
+    verify (1024 x 4) ring step; the full c1 form on the long-prefill tokens.
+    Prints one JSON line; times nothing."""
     import torch
     from deepseek_v4_compressed_c2_gb300 import binding as B
     from deepseek_v4_compressed_c2_gb300 import workloads as W
@@ -791,6 +792,14 @@ def profile_leg(name):
             call = B.prepare_dequant_gather_topk(1, pool, t(cfg["topk"]), t(cfg["token_to_req"]),
                                                  t(cfg["page_table"]), 6, out, err_word=err,
                                                  stream=stream)
+    elif name == "store_c1":
+        cfg = W.c1_long_prefill()
+        pool = torch.zeros(cfg["pool_rows"] * 528, dtype=torch.uint8, device=dev)
+        call = B.prepare_compress_store(1, 1, bf(cfg["rows"]), t(cfg["ext"]), pool,
+                                        page_table=t(cfg["page_table"]), page_bits=cfg["page_bits"],
+                                        rmsnorm_w=bf(cfg["norm_w"]), eps=cfg["eps"],
+                                        freqs_cis=t(cfg["freqs"]), n_out=cfg["n_out"],
+                                        err_word=err, stream=stream)
     elif name == "store_fp4_1m":
         cfg = W.cfg4_gather()
         pool = torch.zeros(cfg["pool_rows"] * 288, dtype=torch.uint8, device=dev)
