@@ -50,7 +50,7 @@ METRIC = "compressed-KV rows/s (store, gather-dequant) and achieved HBM GB/s vs 
 LAYERS = 4
 KERNEL_SAMPLES = 100   # launches of the store / gather timed one by one (median)
 CONFIG_REPS = 50       # timed launches per workload leg (median), after 5 warm-ups
-E2E_CHUNKS = 8
+E2E_CHUNKS = 4
 # algorithmic bytes per unit (what the method must move)
 STORE_BYTES_PER_ROW = 2 * (1024 + 1024) + 256 + 528   # 2 x (kv + score) bf16, RoPE row, V41 row
 GATHER_BYTES_PER_ROW = 528 + 4 + 1024                  # V41 row + id, bf16 row out
