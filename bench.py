@@ -691,7 +691,8 @@ def c1_leg(B, dev, stream, flusher, cfg, rows, peak):
 
 def decode_verify_steps(B, dev, stream, reps=50, max_prefix=4096):
     """The ring form of the compressor on decode-shaped steps (one new token
-    per request; 1 + 3 draft tokens per request).  These are small,
+    per request; 1 + 3 draft tokens per request; a small decode step; a
+    chunked-prefill step of 16 requests x 200 tokens).  These are small,
     latency-bound launches (working set in L2).  The serving loop runs them
     inside a CUDA graph whose offsets are refreshed in place, so the device
     time per launch is taken from a captured graph of `reps` launches; the
@@ -700,7 +701,8 @@ def decode_verify_steps(B, dev, stream, reps=50, max_prefix=4096):
     import torch
     from deepseek_v4_compressed_c2_gb300 import workloads as W
     res = {}
-    for name, n_req, n_new in (("decode_4096req_1tok", 4096, 1), ("verify_1024req_4tok", 1024, 4)):
+    for name, n_req, n_new in (("decode_4096req_1tok", 4096, 1), ("verify_1024req_4tok", 1024, 4),
+                               ("decode_512req_1tok", 512, 1), ("chunked_16req_200tok", 16, 200)):
         cfg = W.decode_verify(seed=13, n_req=n_req, n_new=n_new, ring_size=4,
                               max_prefix=max_prefix)
         bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)

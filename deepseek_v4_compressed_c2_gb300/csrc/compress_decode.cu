@@ -664,7 +664,7 @@ compress_decode_kernel(const StoreParams p) {
       dest = __ldg(p.out_loc + k);
       dest_ok = true;
     }
-    if (row_computed(p, k, d, lane)) {
+    if (row_computed(p, k, d.state, lane)) {
       const long long slot =
           p.out_loc ? (long long)dest
                     : (dest_ok ? ((long long)dest << p.page_bits) |

@@ -255,20 +255,20 @@ __device__ __forceinline__ void row_store(const StoreParams& p, long long k, lon
 
 // A row that is not computed: nothing for a row another phase computes, else
 // zero debug outputs, and a fault for a bad row.  True when it is computed.
-__device__ __forceinline__ bool row_computed(const StoreParams& p, long long k, const RowDesc& d,
+__device__ __forceinline__ bool row_computed(const StoreParams& p, long long k, int state,
                                              int lane) {
-  if (d.state == kRowOk || d.state == kRowOkRing) return true;
-  if (d.state == kRowNone || d.state == kRowRing) return false;
-  if (d.state == kRowBad && lane == 0 && p.err) atomicAdd(p.err, 1);
+  if (state == kRowOk || state == kRowOkRing) return true;
+  if (state == kRowNone || state == kRowRing) return false;
+  if (state == kRowBad && lane == 0 && p.err) atomicAdd(p.err, 1);
   zero_row_outputs(p, k, lane);
   return false;
 }
 
 template <int L, int RATIO, bool NORM, bool ROPE>
-__device__ __forceinline__ void process_row(const StoreParams& p, long long k, const RowDesc& d,
+__device__ __forceinline__ void process_row(const StoreParams& p, long long k, int state,
                                             long long slot, const RowIn<RATIO, ROPE>& in,
                                             const float (&w)[16], int lane) {
-  if (!row_computed(p, k, d, lane)) return;
+  if (!row_computed(p, k, state, lane)) return;
   RowMath m;
   row_math<RATIO, NORM, ROPE>(p, in, w, lane, m, k);
   row_store<L, NORM>(p, k, slot, m, lane);

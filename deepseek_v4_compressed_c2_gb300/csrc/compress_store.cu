@@ -22,11 +22,15 @@
 //    descriptor (state, position, request, row) and issues cp.async.bulk
 //    copies of the row's source rows (one 4 KB copy for a ratio-2 pair in
 //    the fused layout) and of its RoPE row into a 3-stage shared-memory
-//    ring, an mbarrier per stage counting the bytes in flight;
+//    ring, an mbarrier per stage and consumer warp counting the bytes in
+//    flight;
 //  * eight consumer warps, each owning one row (ratio 2) or 2-4 (ratio 1) of
 //    the stage: wait for the stage, pull the row into registers, release the
 //    slot, look up the destination (out_loc or the page table), then pool,
-//    normalise, rotate, quantize and store the row.  Lane l
+//    normalise, rotate, quantize and store the row.  (The wide launch of
+//    store-only rows, which has no arithmetic to hide that lookup behind,
+//    has the producer look it up instead, after the row's copy is issued.)
+//    Lane l
 //    holds dims 8l..8l+7 and 256+8l..263+8l, so every shared-memory read is
 //    conflict-free and every global store of a row half is one contiguous
 //    warp access; the wide launch of store-only ratio-1 rows gives each
@@ -62,6 +66,31 @@ struct StoreShape {
   static constexpr int kStages = SHAPE == kShapeStream ? 3 : 2;
   static constexpr int kMinBlocks = SHAPE == kShapeStream ? 2 : 3;   // CTAs per SM
   static constexpr int kThreads = (kWarps + 1) * 32;
+};
+
+// The 16-byte descriptor of a planned row in a stage.  Streaming shapes: the
+// plan's RowDesc, and each consumer looks the destination up itself (that
+// global load overlaps the row's arithmetic; a producer waiting on it would
+// hold back the copies of the next stage).  Wide shape (rows that are only
+// stored): the state and the destination slot (out_loc[k] or the page-table
+// entry, -1 past the table), looked up by the producer while the row's copy
+// is in flight, so the consumer has no load to wait on.
+struct __align__(16) SlotDesc {
+  int state;
+  int unused;
+  long long slot;
+};
+static_assert(sizeof(SlotDesc) == sizeof(RowDesc), "one descriptor size");
+
+template <int SHAPE>
+struct StageDesc {
+  using T = RowDesc;
+  static constexpr bool kProducerSlot = false;
+};
+template <>
+struct StageDesc<kShapeWide> {
+  using T = SlotDesc;
+  static constexpr bool kProducerSlot = true;
 };
 
 // Rows per consumer warp per stage: one ratio-2 pair (4 KB), four ratio-1
@@ -324,7 +353,7 @@ __device__ __noinline__ void ring_phase(const StoreParams& p, const long long* s
       }
       slot = dest_slot(p, k, d);
     }
-    process_row<L, 2, NORM, ROPE>(p, k, d, slot, in, w, lane);
+    process_row<L, 2, NORM, ROPE>(p, k, d.state, slot, in, w, lane);
   }
   if (p.ring == nullptr) return;
   __syncwarp();
@@ -434,7 +463,7 @@ __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_
 #pragma unroll
     for (int q = 0; q < TL::kRowsPerWarp; ++q) {
       const long long k = (long long)tile * TL::kRows + warp * TL::kRowsPerWarp + q;
-      process_row<L, RATIO, NORM, ROPE>(p, k, d[q], slot[q], in[q], w, lane);
+      process_row<L, RATIO, NORM, ROPE>(p, k, d[q].state, slot[q], in[q], w, lane);
     }
   }
 }
@@ -448,7 +477,7 @@ __device__ __forceinline__ void consume_tiles(const StoreParams& p, const uint8_
 // debug outputs, and the stored row when 0 < slot < pool_rows.
 template <int L>
 __device__ __forceinline__ void consume_tiles_half(const StoreParams& p, const uint8_t* s_stage,
-                                                   const RowDesc* s_desc, uint64_t* s_full,
+                                                   const SlotDesc* s_desc, uint64_t* s_full,
                                                    uint64_t* s_empty, volatile int* abort,
                                                    int n_tiles, int warp, int lane) {
   using TL = StoreTile<1, false, false, kShapeWide>;
@@ -466,10 +495,10 @@ __device__ __forceinline__ void consume_tiles_half(const StoreParams& p, const u
     const int s = it % TL::kStages;
     const uint32_t use = (uint32_t)(it / TL::kStages);
     if (!mbar_wait(&s_full[s * TL::kWarps + warp], use & 1u, abort, p.err)) break;
-    const RowDesc d = s_desc[s * TL::kRows + t];
+    const SlotDesc d = s_desc[s * TL::kRows + t];
     const long long k = (long long)tile * TL::kRows + t;
     const bool ok = d.state == kRowOk;
-    const long long slot = ok ? dest_slot(p, k, d) : 0;
+    const long long slot = d.slot;
     const uint4* src = reinterpret_cast<const uint4*>(s_stage + s * TL::kStageBytes + t * TL::kInBytes);
     uint4 v[4];
 #pragma unroll
@@ -523,10 +552,12 @@ template <int L, int RATIO, bool NORM, bool ROPE, bool RING, int SHAPE>
 __global__ void __launch_bounds__(StoreShape<SHAPE>::kThreads, StoreShape<SHAPE>::kMinBlocks)
 compress_store_kernel(const StoreParams p) {
   using TL = StoreTile<RATIO, NORM, ROPE, SHAPE>;
+  using Desc = typename StageDesc<SHAPE>::T;
+  constexpr bool kProducerSlot = StageDesc<SHAPE>::kProducerSlot;
   constexpr int kStages = TL::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* s_stage = smem;
-  RowDesc* s_desc = reinterpret_cast<RowDesc*>(smem + kStages * TL::kStageBytes);
+  Desc* s_desc = reinterpret_cast<Desc*>(smem + kStages * TL::kStageBytes);
   uint64_t* s_full = reinterpret_cast<uint64_t*>(s_desc + kStages * TL::kRows);
   uint64_t* s_empty = s_full + kStages * TL::kWarps;
   uint64_t* s_plan = s_empty + kStages;
@@ -541,7 +572,8 @@ compress_store_kernel(const StoreParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      for (int w = 0; w < TL::kWarps; ++w) mbar_init(&s_full[s * TL::kWarps + w], 1);
+      for (int w = 0; w < TL::kWarps; ++w)
+        mbar_init(&s_full[s * TL::kWarps + w], kProducerSlot ? 2 : 1);
       mbar_init(&s_empty[s], TL::kWarps);
     }
     mbar_init(s_plan, 1);
@@ -569,16 +601,23 @@ compress_store_kernel(const StoreParams p) {
       if (use > 0 && !mbar_wait(&s_empty[s], (use - 1) & 1u, abort, p.err)) break;
       RowDesc d;
       d.state = kRowNone;
-      long long src = 0;
+      long long src = 0, slot = 0;
       if (lane < TL::kRows) {
-        d = plan_row<RATIO, ROPE, RING>(p, (long long)tile * TL::kRows + lane, total, s_base, s_first,
-                                        s_start, s_count, src);
-        s_desc[s * TL::kRows + lane] = d;
+        const long long k = (long long)tile * TL::kRows + lane;
+        d = plan_row<RATIO, ROPE, RING>(p, k, total, s_base, s_first, s_start, s_count, src);
+        if constexpr (kProducerSlot) {
+          // the destination's global load stays in flight across the copies' issue
+          if (d.state == kRowOk) slot = dest_slot(p, k, d);
+        } else {
+          s_desc[s * TL::kRows + lane] = d;
+        }
       }
       // each consumer warp's rows complete on that warp's own barrier: the
       // first lane of the warp's rows (the group leader) arms it with their
-      // bytes.  Ratio 1: a group of consecutive packed source rows comes in
-      // one copy issued by the leader.
+      // bytes before the copies (and in the wide shape arrives a second time
+      // once the group's descriptors, with their slots, are written).
+      // Ratio 1: a group of consecutive packed source rows comes in one copy
+      // issued by the leader.
       const bool copy = d.state == kRowOk || d.state == kRowOkRing;
       const int leader = lane & ~(TL::kRowsPerWarp - 1);
       bool merged = false;
@@ -594,7 +633,8 @@ compress_store_kernel(const StoreParams p) {
 #pragma unroll
       for (int o = 1; o < TL::kRowsPerWarp; o <<= 1) bytes += __shfl_xor_sync(kFullMask, bytes, o);
       __syncwarp();
-      if (lane < TL::kRows && lane % TL::kRowsPerWarp == 0) mbar_arrive_expect_tx(bar, bytes);
+      const bool group_leader = lane < TL::kRows && lane % TL::kRowsPerWarp == 0;
+      if (group_leader) mbar_arrive_expect_tx(bar, bytes);
       __syncwarp();
       if (copy) {
         uint8_t* stage = s_stage + s * TL::kStageBytes;
@@ -630,6 +670,11 @@ compress_store_kernel(const StoreParams p) {
         if constexpr (ROPE)
           bulk_g2s(stage + TL::kRows * TL::kInBytes + lane * TL::kRopeBytes,
                    p.freqs + (long long)d.pos * kRopeDim, kRopeDim * 4, bar, pol);
+      }
+      if constexpr (kProducerSlot) {
+        if (lane < TL::kRows) s_desc[s * TL::kRows + lane] = SlotDesc{d.state, 0, slot};
+        __syncwarp();
+        if (group_leader) mbar_arrive(bar);
       }
       if (++s == kStages) { s = 0; ++use; }
     }

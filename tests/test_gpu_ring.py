@@ -275,15 +275,18 @@ def test_decode_kernel_launch_forms_match_oracle(B, form):
         assert np.all(np.abs(lat_g - lat_r) <= tol)
 
 
-def test_decode_kernel_mixed_step_with_long_requests(B):
+@pytest.mark.parametrize("rows_layout", ["packed", "shuffled"])
+def test_decode_kernel_mixed_step_with_long_requests(B, rows_layout):
     """A step that mixes 600 decode requests with a few long ones, all in the
     decode kernel (at most 16 rows per SM): requests of 80 new tokens at an
     odd start make chunks of 40+ rows (overflow rows taken by other CTAs'
     spare warps) and 40 ring tokens each (more than the ring warp's 32
     stages, so it moves them in two batches); one request of 130 tokens at
     an odd start has n >= 2R, so its ring update follows its first row in
-    that row's warp.  Ring, pool bytes (given the GPU's fp32 rows) and fault
-    count equal the oracle's; pre-quant within tolerance."""
+    that row's warp.  The requests' rows either packed back to back in slot
+    order or in a shuffled order with gaps of 0-3 rows.  Ring, pool bytes
+    (given the GPU's fp32 rows) and fault count equal the oracle's; pre-quant
+    within tolerance."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     rng = np.random.default_rng(71)
     n_req, R = 600, 64
@@ -292,12 +295,20 @@ def test_decode_kernel_mixed_step_with_long_requests(B):
     for r, n in ((5, 80), (6, 80), (300, 80), (599, 80), (301, 130)):
         lengths[r] = n
         p0[r] |= 1                                   # odd start: the first pair reads the ring
-    rows = W.bf16_normal(rng, (sum(lengths), 1024))
+    if rows_layout == "packed":
+        ext = W._ext(lengths)
+    else:
+        first, cursor = np.zeros(n_req, np.int64), 0
+        for r in rng.permutation(n_req):
+            first[r] = cursor + int(rng.integers(0, 4))
+            cursor = int(first[r]) + lengths[r]
+        ext = np.stack([first, np.array(lengths)]).astype(np.int32)
+        assert (ext[0][1:] != ext[0][:-1] + ext[1][:-1]).any()
+    rows = W.bf16_normal(rng, (int((ext[0] + ext[1]).max()), 1024))
     ring0 = W.bf16_normal(rng, (n_req, R, 1024))
     norm_w = W.bf16_from_f32(rng.uniform(0.5, 1.5, 512).astype(np.float32))
     max_c = (2048 + 130) // 2 + 1
     pt, n_pages = W._page_table(rng, [-(-max_c // 64)] * n_req)
-    ext = W._ext(lengths)
     n_out = int(sum(((int(a) + n) >> 1) - (int(a) >> 1) for a, n in zip(p0, lengths)))
     assert n_out <= 16 * sms, "the step must take the decode kernel"
     cfg = dict(layout=oracle.V41, rows=rows, ext=ext, start_pos=p0, page_table=pt, page_bits=6,
