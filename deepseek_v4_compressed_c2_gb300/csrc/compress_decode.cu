@@ -96,9 +96,13 @@ __device__ __forceinline__ unsigned sat_add(unsigned a, unsigned b, unsigned cap
   return s < cap ? s : cap;
 }
 
+// rows_of_slot<2> capped at cap, in 32 bits: for n > 0,
+// floor((p0 + n) / 2) - floor(p0 / 2) = floor((n + (p0 & 1)) / 2) for every
+// int p0 (odd p0, negative ones included, completes one pair more).
 __device__ __forceinline__ unsigned capped_rows(int n, int p0, unsigned cap) {
-  const long long r = rows_of_slot<2>(n, p0);
-  return r < (long long)cap ? (unsigned)r : cap;
+  if (n <= 0) return 0u;
+  const unsigned r = ((unsigned)n + ((unsigned)p0 & 1u)) >> 1;
+  return r < cap ? r : cap;
 }
 
 __device__ __forceinline__ bool aligned16(const void* q) {

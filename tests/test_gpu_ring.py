@@ -392,3 +392,29 @@ def test_decode_steps_in_a_cuda_graph_with_metadata_refreshed_in_place(B):
                               ring=ref_ring, prequant_in=pre.cpu().numpy(), **kw)
         assert np.array_equal(host_u16(ring).reshape(ref_ring.shape), ref_ring), step
         assert np.array_equal(pool.cpu().numpy(), ref_pool), step
+
+
+@pytest.mark.parametrize("n_slots", [0, 5])
+def test_ring_form_step_without_new_tokens_writes_only_padding(B, n_slots):
+    """A ring-form step with n_out > 0 but no new tokens (no request slots, or
+    slots whose counts are all zero) takes the decode kernel and makes no
+    rows: the pre-quant output is zeroed over its sentinel, the pool and the
+    ring stay as they were, no fault."""
+    rng = np.random.default_rng(5 + n_slots)
+    R, n_out = 4, 8
+    ext = np.zeros((2, n_slots), np.int32)
+    p0 = rng.integers(0, 100, n_slots).astype(np.int32)
+    ring0 = W.bf16_normal(rng, (max(n_slots, 1), R, 1024))
+    rows = W.bf16_normal(rng, (4, 1024))
+    pt = np.ones((max(n_slots, 1), 4), np.int32)
+    pool = torch.full((4 * 64 * 528,), 0x33, dtype=torch.uint8, device="cuda")
+    pre = torch.full((n_out, 512), 7.0, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ring = dev_bf16(ring0)
+    B.dsv4kv_compress_store(oracle.V41, 2, dev_bf16(rows), dev(ext), pool, page_table=dev(pt),
+                            page_bits=6, n_out=n_out, prequant_out=pre, err_word=err,
+                            start_pos=dev(p0), ring=ring)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert bool((pool == 0x33).all()) and not bool(pre.any())
+    assert np.array_equal(host_u16(ring).reshape(ring0.shape), ring0)

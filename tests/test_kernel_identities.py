@@ -10,7 +10,10 @@ against their definitions (no GPU, no CUDA code imported).
   midpoint; checked with exact rationals for all 126 positive e4m3 scales.
 * The negative-zero clean-up on packed codes: clearing the sign of every
   e4m3 byte (e2m1 nibble) whose magnitude is zero, by one masked add, equals
-  the per-element definition and never carries into a neighbour."""
+  the per-element definition and never carries into a neighbour.
+* The ratio-2 row count of a request slot in 32 bits: the decode kernel
+  takes floor((p0 + n) / 2) - floor(p0 / 2) as (n + (p0 & 1)) >> 1 on
+  unsigned words, for n > 0 and any int32 start p0."""
 from fractions import Fraction
 
 import numpy as np
@@ -97,3 +100,16 @@ def test_negative_zero_cleanup_matches_its_definition():
                     q = (x >> (4 * i)) & 0xF
                     want |= (0 if q == 0x8 else q) << (4 * i)
                 assert y == want
+
+
+def test_ratio2_row_count_in_32_bits_equals_the_difference_of_halves():
+    rng = np.random.default_rng(3)
+    lim = np.iinfo(np.int32)
+    p0 = np.concatenate([rng.integers(lim.min, lim.max, 1 << 20, endpoint=True),
+                         np.arange(-64, 65), [lim.min, lim.min + 1, lim.max - 1, lim.max]])
+    n = np.concatenate([rng.integers(1, lim.max, 1 << 20, endpoint=True),
+                        rng.integers(1, 9, 129), [1, lim.max, 2, lim.max]])
+    p0, n = p0.astype(np.int64), n.astype(np.int64)
+    want = np.floor_divide(p0 + n, 2) - np.floor_divide(p0, 2)      # exact in int64
+    got = (n.astype(np.uint32) + (p0.astype(np.int32).view(np.uint32) & np.uint32(1))) >> np.uint32(1)
+    assert np.array_equal(got.astype(np.int64), want)
