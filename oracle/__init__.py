@@ -141,7 +141,10 @@ def bf16_bits(x) -> np.ndarray:
 
 def bf16_to_f64(bits) -> np.ndarray:
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
-    return b.view(np.float32).astype(np.float64)
+    # a signaling-NaN pattern (arbitrary bytes) widens to a quiet NaN; some
+    # hosts flag that conversion as an invalid operation, which is expected here
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
 
 
 # --------------------------------------------------------------------------
