@@ -216,8 +216,7 @@ __device__ __forceinline__ void row_math(const StoreParams& p, const RowIn<RATIO
         const float c = f[2 * q], sn = f[2 * q + 1];
         float a, b;
         f2_split(x2[4 + q], a, b);
-        const uint64_t bsc = f2_mul(f2(b, b), f2(-sn, c));          // (-b s, b c)
-        x2[4 + q] = f2_fma(f2(a, a), f2(c, sn), bsc);
+        x2[4 + q] = f2(fmaf(a, c, b * -sn), fmaf(a, sn, b * c));   // (a c - b s, a s + b c)
       }
     }
   }
@@ -248,8 +247,7 @@ __device__ __forceinline__ void row_store(const StoreParams& p, long long k, lon
     }
     if (store) store_row_split<L>(x, PagedKV<L>{p.pool, p.page_bits}.row(slot), lane);
   } else if (store) {
-    f2_unpack16(x2, x);
-    store_row_v41_scaled(x, m.inv, PagedKV<kV41>{p.pool, p.page_bits}.row(slot), lane);
+    store_row_v41_scaled(x2, m.inv, PagedKV<kV41>{p.pool, p.page_bits}.row(slot), lane);
   }
 }
 
